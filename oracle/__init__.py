@@ -1,0 +1,239 @@
+"""fp64 CPU oracle of the MSA hot path -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline and
+reference arms may import this package.  The product path (the CUDA library
+and its Python binding) never imports, links or calls anything here, and this
+package never touches the CUDA path.
+
+The arithmetic lives in ``msa_oracle.c`` (plain C, fp64, OpenMP over rows);
+this module builds it with gcc and marshals numpy arrays in and out.  bf16
+inputs are passed as their raw 16-bit patterns and widened exactly in C.
+
+Functions and the passages they follow (page title and passage):
+
+* ``prefill_scores`` / ``decode_scores`` -- block scores of the Index Branch
+  ("MiniMax M3: Como la atencion dispersa hace practicos a los agentes de largo
+  alcance", MSA paragraph and figure caption); formula fixed by this build:
+  s_t = sum_h w_h ReLU(q_idx_h . k_idx_t), c_j = max over block j.
+* ``select`` -- own block + top-(k-1) earlier blocks by (score desc, index asc)
+  (same page, bullet "Costo predecible": Bk = 128, k = 16).
+* ``prefill_attend`` / ``decode_attend`` -- exact softmax attention over the
+  selected blocks' uncompressed K/V (M2-report article, section "MiniMax Sparse
+  Attention (MSA) y escalado subcuadratico entrante").
+* ``lse_merge`` -- log-sum-exp recombination of per-block partials (M3 serving
+  report post, paragraph "KV-Block-Major").
+* ``page_table`` -- decode page table from the selected blocks with the KV
+  group flattened into the batch (same post, paragraph "MSA con paged
+  attention").
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "msa_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile msa_oracle.c into liboracle.so with gcc (-O2, OpenMP, no fast-math)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c99",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_i32p = np.ctypeslib.ndpointer(dtype=np.int32, flags="C_CONTIGUOUS")
+_i64p = np.ctypeslib.ndpointer(dtype=np.int64, flags="C_CONTIGUOUS")
+_u16p = np.ctypeslib.ndpointer(dtype=np.uint16, flags="C_CONTIGUOUS")
+_f32p = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS")
+_f64p = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
+_i, _l, _d = C.c_int, C.c_int64, C.c_double
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = C.CDLL(_LIB)
+            L.orc_num_threads.restype = _i
+            L.orc_set_num_threads.argtypes = [_i]
+            L.orc_prefill_scores.argtypes = [_i, _i, _i, _i, _i, _i, _u16p, _u16p, _f32p,
+                                             _l, _i64p, _i, _f64p]
+            L.orc_decode_scores.argtypes = [_i, _i, _i, _i, _i, _u16p, _f32p, _u16p,
+                                            _i32p, _i, _i32p, _i, _f64p]
+            L.orc_select.argtypes = [_l, _i, _f64p, _i32p, _i, _i32p, _i32p, _f64p, _f64p]
+            L.orc_prefill_attend.argtypes = [_i, _i, _i, _i, _i, _i, _d, _u16p, _u16p, _u16p,
+                                             _l, _i64p, _i, _i32p, _i32p, _f64p, _f64p]
+            L.orc_decode_attend.argtypes = [_i, _i, _i, _i, _i, _d, _u16p, _u16p, _u16p,
+                                            _i32p, _i, _i32p, _i, _i32p, _i32p, _f64p, _f64p]
+            L.orc_lse_merge.argtypes = [_l, _i, _i, _f64p, _f64p, _f64p, _f64p]
+            L.orc_page_table.argtypes = [_i, _i, _i, _i, _i32p, _i32p, _i32p, _i, _i32p,
+                                         _i32p, _i32p, _i32p]
+            _lib = L
+    return _lib
+
+
+def num_threads() -> int:
+    return lib().orc_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    lib().orc_set_num_threads(int(n))
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers (no arithmetic of the method)
+# ---------------------------------------------------------------------------
+
+def _np(t):
+    """torch tensor or array -> contiguous numpy array on the host."""
+    if hasattr(t, "detach"):
+        import torch
+        t = t.detach()
+        if t.dtype == torch.bfloat16:
+            return np.ascontiguousarray(t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+        return np.ascontiguousarray(t.cpu().contiguous().numpy())
+    return np.ascontiguousarray(t)
+
+
+def _u16(t):
+    a = _np(t)
+    assert a.dtype == np.uint16, a.dtype
+    return a
+
+
+def _f32(t):
+    return np.ascontiguousarray(_np(t), dtype=np.float32)
+
+
+def _i32(t):
+    return np.ascontiguousarray(_np(t), dtype=np.int32)
+
+
+def _i64(t):
+    return np.ascontiguousarray(_np(t), dtype=np.int64)
+
+
+# ---------------------------------------------------------------------------
+# step functions
+# ---------------------------------------------------------------------------
+
+def prefill_scores(q_idx, k_idx, w, Bk: int, rows=None):
+    """Block scores C [nrows, Hkv, nb] (fp64) for prefill query rows b*S + i."""
+    qi, ki, ww = _u16(q_idx), _u16(k_idx), _f32(w)
+    B, S, Hkv, HI, dI = qi.shape
+    nb = (S + Bk - 1) // Bk
+    rows = np.arange(B * S, dtype=np.int64) if rows is None else _i64(rows)
+    out = np.empty((len(rows), Hkv, nb), dtype=np.float64)
+    lib().orc_prefill_scores(B, S, Hkv, HI, dI, Bk, qi, ki, ww, len(rows), rows, nb, out)
+    return out
+
+
+def decode_scores(q_idx, w, kidx_pool, seq_pt, seq_len, nb_stride: int = None):
+    """Block scores C [B, Hkv, nb_stride] (fp64) of one decode step over paged k_idx."""
+    qi, ww, kp = _u16(q_idx), _f32(w), _u16(kidx_pool)
+    pt, sl = _i32(seq_pt), _i32(seq_len)
+    B, Hkv, HI, dI = qi.shape
+    Bk = kp.shape[2]
+    nb_stride = pt.shape[1] if nb_stride is None else nb_stride
+    out = np.empty((B, Hkv, nb_stride), dtype=np.float64)
+    lib().orc_decode_scores(B, Hkv, HI, dI, Bk, qi, ww, kp, pt, pt.shape[1], sl, nb_stride, out)
+    return out
+
+
+def select(Cs, own, k: int):
+    """Selection per row of scores.  Cs [..., nb] fp64, own [...] int.
+
+    Returns (sel [..., k] int32 ascending, -1 padded; count [...] int32;
+    c_last [...]; c_next [...]) where c_last / c_next are the scores of the last
+    kept and first dropped earlier block (NaN when nothing is dropped).
+    """
+    Cs = np.ascontiguousarray(Cs, dtype=np.float64)
+    lead = Cs.shape[:-1]
+    nb = Cs.shape[-1]
+    flat = Cs.reshape(-1, nb)
+    o = np.ascontiguousarray(np.broadcast_to(np.asarray(own, dtype=np.int32), lead).reshape(-1))
+    n = flat.shape[0]
+    sel = np.empty((n, k), dtype=np.int32)
+    cnt = np.empty(n, dtype=np.int32)
+    cl = np.empty(n, dtype=np.float64)
+    cn = np.empty(n, dtype=np.float64)
+    lib().orc_select(n, nb, flat, o, k, sel, cnt, cl, cn)
+    return sel.reshape(*lead, k), cnt.reshape(lead), cl.reshape(lead), cn.reshape(lead)
+
+
+def prefill_attend(Q, K, V, sel, count, Bk: int, scale: float, rows=None):
+    """Sparse attention for prefill rows with a given selection.
+
+    sel [nrows, Hkv, k], count [nrows, Hkv].  Returns O [nrows, Hq, D], LSE [nrows, Hq].
+    """
+    q, kk, vv = _u16(Q), _u16(K), _u16(V)
+    B, S, Hq, D = q.shape
+    Hkv = kk.shape[2]
+    rows = np.arange(B * S, dtype=np.int64) if rows is None else _i64(rows)
+    s, c = _i32(sel), _i32(count)
+    k = s.shape[-1]
+    assert s.shape == (len(rows), Hkv, k) and c.shape == (len(rows), Hkv)
+    O = np.empty((len(rows), Hq, D), dtype=np.float64)
+    LSE = np.empty((len(rows), Hq), dtype=np.float64)
+    lib().orc_prefill_attend(B, S, Hq, Hkv, D, Bk, float(scale), q, kk, vv, len(rows), rows, k,
+                             s, c, O, LSE)
+    return O, LSE
+
+
+def decode_attend(Q, K_pool, V_pool, seq_pt, seq_len, sel, count, scale: float):
+    """Sparse attention of one decode step.  Returns O [B, Hq, D], LSE [B, Hq]."""
+    q, kp, vp = _u16(Q), _u16(K_pool), _u16(V_pool)
+    pt, sl, s, c = _i32(seq_pt), _i32(seq_len), _i32(sel), _i32(count)
+    B, Hq, D = q.shape
+    Hkv, Bk = kp.shape[1], kp.shape[2]
+    k = s.shape[-1]
+    O = np.empty((B, Hq, D), dtype=np.float64)
+    LSE = np.empty((B, Hq), dtype=np.float64)
+    lib().orc_decode_attend(B, Hq, Hkv, D, Bk, float(scale), q, kp, vp, pt, pt.shape[1], sl, k,
+                            s, c, O, LSE)
+    return O, LSE
+
+
+def lse_merge(Op, LSEp):
+    """Merge partials Op [rows, parts, D], LSEp [rows, parts] -> O [rows, D], LSE [rows]."""
+    op = np.ascontiguousarray(Op, dtype=np.float64)
+    lp = np.ascontiguousarray(LSEp, dtype=np.float64)
+    rows, parts, D = op.shape
+    O = np.empty((rows, D), dtype=np.float64)
+    LSE = np.empty(rows, dtype=np.float64)
+    lib().orc_lse_merge(rows, parts, D, op, lp, O, LSE)
+    return O, LSE
+
+
+def page_table(sel, count, seq_pt, seq_len, Bk: int):
+    """Decode page table rows r = b*Hkv + g: (pt [B*Hkv, k], n [B*Hkv], last_len [B*Hkv])."""
+    s, c, pt, sl = _i32(sel), _i32(count), _i32(seq_pt), _i32(seq_len)
+    B, Hkv, k = s.shape
+    out_pt = np.empty((B * Hkv, k), dtype=np.int32)
+    n = np.empty(B * Hkv, dtype=np.int32)
+    ll = np.empty(B * Hkv, dtype=np.int32)
+    lib().orc_page_table(B, Hkv, k, Bk, s, c, pt, pt.shape[1], sl, out_pt, n, ll)
+    return out_pt, n, ll
+
+
+def own_blocks_prefill(S: int, Bk: int, rows):
+    """Own block b_i = floor(i / Bk) of prefill rows b*S + i (index bookkeeping)."""
+    r = _i64(rows)
+    return ((r % S) // Bk).astype(np.int32)
+
+
+def own_blocks_decode(seq_len, Bk: int):
+    """Own block (L_b - 1) // Bk of each decode sequence (index bookkeeping)."""
+    return ((_i64(seq_len) - 1) // Bk).astype(np.int32)

@@ -1,0 +1,375 @@
+"""Pins of the fp64 oracle against facts that do not come from the oracle itself.
+
+Each pin is chosen so that a plausible mistake in the oracle (a dropped term, a
+wrong sign or index, a transposed operand, a wrong head-to-group map, an
+off-by-one in causality or in the selection order) fails at least one test:
+
+* dense limit   -- with k >= number of blocks MSA is dense causal GQA attention;
+                   checked against a numpy matrix-form softmax and against
+                   torch's fp64 scaled-dot-product attention.
+* merge         -- LSE merge of a split softmax equals one softmax.
+* top-k         -- selection equals an exhaustive sort by (-score, index).
+* closed forms  -- one-hot index vectors give hand-derivable block scores;
+                   one key gives O = V, LSE = z; equal keys give the mean of V.
+* cross-path    -- decode at length L equals prefill row L-1; page order and
+                   the flattened (B*Hkv) page table do not change the result.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import DecodeWorkload, MSAShape, PrefillWorkload, decode_inputs, prefill_inputs, workload
+
+
+def f64(t):
+    return t.detach().cpu().double().numpy()
+
+
+def dense_causal_gqa_numpy(Q, K, V, scale):
+    """Dense causal GQA attention in matrix form: softmax(scale Q K^T + mask) V."""
+    q, k, v = f64(Q), f64(K), f64(V)
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    G = Hq // Hkv
+    O = np.zeros((B, S, Hq, D))
+    LSE = np.zeros((B, S, Hq))
+    mask = np.triu(np.ones((S, S), dtype=bool), 1)
+    for b in range(B):
+        for hq in range(Hq):
+            g = hq // G
+            z = scale * q[b, :, hq, :] @ k[b, :, g, :].T
+            z[mask] = -np.inf
+            m = z.max(axis=1, keepdims=True)
+            e = np.exp(z - m)
+            l = e.sum(axis=1, keepdims=True)
+            O[b, :, hq, :] = (e / l) @ v[b, :, g, :]
+            LSE[b, :, hq] = (m + np.log(l))[:, 0]
+    return O, LSE
+
+
+def run_prefill_oracle(inp, sh, rows=None):
+    B, S = inp["Q"].shape[:2]
+    rows = np.arange(B * S, dtype=np.int64) if rows is None else rows
+    C = oracle.prefill_scores(inp["q_idx"], inp["k_idx"], inp["w"], sh.Bk, rows)
+    own = oracle.own_blocks_prefill(S, sh.Bk, rows)
+    sel, cnt, _, _ = oracle.select(C, own[:, None], sh.k)
+    O, LSE = oracle.prefill_attend(inp["Q"], inp["K"], inp["V"], sel, cnt, sh.Bk,
+                                   1.0 / math.sqrt(sh.D), rows)
+    return C, sel, cnt, O, LSE
+
+
+# ---------------------------------------------------------------------------
+# P1: dense limit
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("wl", [
+    workload("prefill_tiny_s2048_k16"),
+    # GQA with ragged tail: G = 3, two KV groups, S not a multiple of Bk
+    PrefillWorkload("gqa_ragged", B=2, S=300, shape=MSAShape(Hq=6, Hkv=2, HI=2, k=3), seed=11),
+])
+def test_dense_limit_equals_causal_gqa(wl):
+    sh = wl.shape
+    assert sh.k >= wl.nb
+    inp = prefill_inputs(wl)
+    C, sel, cnt, O, LSE = run_prefill_oracle(inp, sh)
+    B, S = wl.B, wl.S
+    own = (np.arange(S) // sh.Bk)
+    # every row keeps all blocks 0..b_i
+    cnt = cnt.reshape(B, S, sh.Hkv)
+    assert np.array_equal(cnt, np.broadcast_to((own + 1)[None, :, None], cnt.shape))
+    Od, LSEd = dense_causal_gqa_numpy(inp["Q"], inp["K"], inp["V"], 1.0 / math.sqrt(sh.D))
+    np.testing.assert_allclose(O.reshape(Od.shape), Od, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(LSE.reshape(LSEd.shape), LSEd, rtol=0, atol=1e-12)
+    # second, independent check: torch fp64 SDPA with repeated KV heads
+    G = sh.G
+    q = inp["Q"].double().permute(0, 2, 1, 3)
+    k = inp["K"].double().repeat_interleave(G, dim=2).permute(0, 2, 1, 3)
+    v = inp["V"].double().repeat_interleave(G, dim=2).permute(0, 2, 1, 3)
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True,
+                                                           scale=1.0 / math.sqrt(sh.D))
+    np.testing.assert_allclose(O.reshape(Od.shape), ref.permute(0, 2, 1, 3).numpy(), rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# P2: merge of a split softmax equals one softmax
+# ---------------------------------------------------------------------------
+
+def test_merge_equals_single_softmax():
+    rng = np.random.default_rng(5)
+    rows, n, D = 64, 300, 16
+    z = rng.normal(size=(rows, n)) * 3.0
+    Vv = rng.normal(size=(n, D))
+    parts = 7
+    Op = np.full((rows, parts, D), np.nan)     # empty parts hold garbage on purpose
+    LSEp = np.full((rows, parts), -np.inf)
+    for r in range(rows):
+        # random cut points; some parts end up empty
+        cuts = np.sort(rng.integers(0, n + 1, size=parts - 1))
+        bounds = np.concatenate([[0], cuts, [n]])
+        for p in range(parts):
+            a, b = bounds[p], bounds[p + 1]
+            if a == b:
+                continue
+            zz = z[r, a:b]
+            m = zz.max()
+            e = np.exp(zz - m)
+            Op[r, p] = (e / e.sum()) @ Vv[a:b]
+            LSEp[r, p] = m + np.log(e.sum())
+    O, LSE = oracle.lse_merge(Op, LSEp)
+    m = z.max(axis=1, keepdims=True)
+    e = np.exp(z - m)
+    np.testing.assert_allclose(O, (e / e.sum(axis=1, keepdims=True)) @ Vv, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(LSE, (m + np.log(e.sum(axis=1, keepdims=True)))[:, 0], rtol=0, atol=1e-12)
+
+
+def test_merge_all_empty_row():
+    O, LSE = oracle.lse_merge(np.full((1, 3, 4), np.nan), np.full((1, 3), -np.inf))
+    assert np.all(O == 0) and LSE[0] == -np.inf
+
+
+def test_attend_per_block_then_merge_equals_attend_all():
+    """Attention restricted to each selected block, LSE-merged, equals attention over all of them."""
+    wl = PrefillWorkload("split", B=1, S=700, shape=MSAShape(Hq=4, Hkv=2, HI=2, k=6), seed=21)
+    sh = wl.shape
+    inp = prefill_inputs(wl)
+    rows = np.array([0, 127, 128, 350, 699], dtype=np.int64)
+    C, sel, cnt, O, LSE = run_prefill_oracle(inp, sh, rows)
+    k = sh.k
+    Op = np.zeros((len(rows), sh.Hq, k, sh.D))
+    LSEp = np.full((len(rows), sh.Hq, k), -np.inf)
+    for s in range(k):
+        sel1 = np.full_like(sel, -1)
+        sel1[..., 0] = sel[..., s]
+        cnt1 = (cnt > s).astype(np.int32)
+        o1, l1 = oracle.prefill_attend(inp["Q"], inp["K"], inp["V"], sel1, cnt1, sh.Bk,
+                                       1.0 / math.sqrt(sh.D), rows)
+        Op[:, :, s] = o1
+        LSEp[:, :, s] = l1
+    Om, LSEm = oracle.lse_merge(Op.reshape(-1, k, sh.D), LSEp.reshape(-1, k))
+    np.testing.assert_allclose(Om.reshape(O.shape), O, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(LSEm.reshape(LSE.shape), LSE, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# P3: selection equals an exhaustive sort
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("k", [1, 2, 4, 16])
+def test_select_equals_exhaustive_sort(k):
+    rng = np.random.default_rng(100 + k)
+    rows, nb = 400, 40
+    C = rng.integers(0, 8, size=(rows, nb)).astype(np.float64) / 8.0  # heavy ties
+    own = rng.integers(0, nb, size=rows).astype(np.int32)
+    sel, cnt, cl, cn = oracle.select(C, own, k)
+    for r in range(rows):
+        n = own[r]
+        order = sorted(range(n), key=lambda j: (-C[r, j], j))
+        keep = sorted(order[:k - 1]) + [n]
+        assert cnt[r] == len(keep)
+        assert list(sel[r, :cnt[r]]) == keep
+        assert np.all(sel[r, cnt[r]:] == -1)
+        if n > k - 1:
+            if k >= 2:
+                assert cl[r] == C[r, order[k - 2]]
+            else:
+                assert np.isnan(cl[r])
+            assert cn[r] == C[r, order[k - 1]]
+        else:
+            assert np.isnan(cl[r]) and np.isnan(cn[r])
+
+
+def test_select_ignores_future_and_own_scores():
+    C = np.array([[0.1, 0.9, 0.5, 100.0, 200.0]])
+    sel, cnt, _, _ = oracle.select(C, np.array([3], dtype=np.int32), 3)
+    # candidates are blocks 0..2 only: top-2 = {1, 2}, plus own block 3
+    assert list(sel[0]) == [1, 2, 3] and cnt[0] == 3
+
+
+# ---------------------------------------------------------------------------
+# P4: closed forms
+# ---------------------------------------------------------------------------
+
+def test_index_score_onehot_closed_form():
+    """One-hot index vectors: q_idx_h = a_h e_{d_h}, k_idx_t = x_t e_{e_t}.
+
+    Then q_idx_h . k_idx_t = a_h x_t [d_h == e_t] and
+    s_t = sum_h w_h max(0, a_h x_t [d_h == e_t]).  Values are exact in bf16.
+    """
+    Bk, HI, dI = 4, 2, 64
+    S = 3 * Bk
+    q_idx = torch.zeros(1, S, 1, HI, dI, dtype=torch.bfloat16)
+    k_idx = torch.zeros(1, S, 1, dI, dtype=torch.bfloat16)
+    w = torch.zeros(1, S, 1, HI)
+    i = S - 1                      # query in block 2: blocks 0 and 1 are scored
+    q_idx[0, i, 0, 0, 3] = 1.0     # head 0 looks at dim 3 with a = 1
+    q_idx[0, i, 0, 1, 5] = -2.0    # head 1 looks at dim 5 with a = -2
+    w[0, i, 0] = torch.tensor([0.75, 0.5])
+    tokens = {  # t: (dim, x)
+        0: (3, 0.5), 1: (5, -1.0), 2: (3, -4.0), 3: (7, 8.0),      # block 0
+        4: (5, 0.25), 5: (3, 0.125), 6: (5, -0.5), 7: (3, 0.25),   # block 1
+        8: (3, 64.0), 9: (5, -64.0), 10: (3, 1.0), 11: (3, 1.0),   # own block (not scored)
+    }
+    for t, (d, x) in tokens.items():
+        k_idx[0, t, 0, d] = x
+    # hand derivation
+    # block 0: t0: 0.75*max(0, 0.5) = 0.375; t1: 0.5*max(0, -2*-1) = 1.0;
+    #          t2: 0.75*max(0, -4) = 0;       t3: dim 7 matches no head -> 0.   max = 1.0
+    # block 1: t4: 0.5*max(0, -2*0.25) = 0;  t5: 0.75*0.125 = 0.09375;
+    #          t6: 0.5*max(0, -2*-0.5) = 0.5; t7: 0.75*0.25 = 0.1875.           max = 0.5
+    C = oracle.prefill_scores(q_idx, k_idx, w, Bk, rows=np.array([i]))
+    assert C.shape == (1, 1, 3)
+    assert C[0, 0, 0] == 1.0 and C[0, 0, 1] == 0.5 and C[0, 0, 2] == -np.inf
+
+
+def test_index_score_negative_dots_contribute_zero():
+    Bk, HI, dI = 2, 3, 64
+    q_idx = torch.zeros(1, 4, 1, HI, dI, dtype=torch.bfloat16)
+    k_idx = torch.zeros(1, 4, 1, dI, dtype=torch.bfloat16)
+    w = torch.ones(1, 4, 1, HI)
+    q_idx[0, 3, 0, :, 0] = torch.tensor([1.0, -1.0, 2.0])
+    k_idx[0, 0, 0, 0] = 1.0    # dots (1, -1, 2): ReLU keeps 1 + 2 = 3
+    k_idx[0, 1, 0, 0] = -1.0   # dots (-1, 1, -2): ReLU keeps 1
+    C = oracle.prefill_scores(q_idx, k_idx, w, Bk, rows=np.array([3]))
+    assert C[0, 0, 0] == 3.0
+
+
+def test_attention_single_key_closed_form():
+    """Query 0 sees only token 0: O = V_0, LSE = scale * Q_0 . K_0."""
+    wl = PrefillWorkload("one", B=1, S=5, shape=MSAShape(Hq=4, Hkv=2, HI=2, k=2), seed=3)
+    sh = wl.shape
+    inp = prefill_inputs(wl)
+    _, _, _, O, LSE = run_prefill_oracle(inp, sh, rows=np.array([0]))
+    q, k, v = f64(inp["Q"]), f64(inp["K"]), f64(inp["V"])
+    for hq in range(sh.Hq):
+        g = hq // sh.G
+        np.testing.assert_array_equal(O[0, hq], v[0, 0, g])
+        z = sum(q[0, 0, hq, d] * k[0, 0, g, d] for d in range(sh.D)) / math.sqrt(sh.D)
+        assert abs(LSE[0, hq] - z) < 1e-14
+
+
+def test_attention_equal_keys_closed_form():
+    """All keys equal: uniform weights, O = mean of V over t <= i, LSE = z + ln(i + 1)."""
+    wl = PrefillWorkload("eq", B=1, S=300, shape=MSAShape(Hq=2, Hkv=1, HI=2, k=3), seed=4)
+    sh = wl.shape
+    inp = prefill_inputs(wl)
+    inp["K"][:] = inp["K"][0, 0]
+    rows = np.array([0, 1, 127, 128, 299], dtype=np.int64)
+    _, _, _, O, LSE = run_prefill_oracle(inp, sh, rows)
+    q, k, v = f64(inp["Q"]), f64(inp["K"]), f64(inp["V"])
+    for r, i in enumerate(rows):
+        for hq in range(sh.Hq):
+            mean = v[0, :i + 1, 0].sum(axis=0) / (i + 1)
+            np.testing.assert_allclose(O[r, hq], mean, rtol=0, atol=1e-13)
+            z = float(np.dot(q[0, i, hq], k[0, 0, 0])) / math.sqrt(sh.D)
+            assert abs(LSE[r, hq] - (z + math.log(i + 1))) < 1e-12
+
+
+# ---------------------------------------------------------------------------
+# P5: cross-path invariants
+# ---------------------------------------------------------------------------
+
+def _decode_from_prefill(inp, sh, b, L, perm_seed):
+    """Page tokens 0..L-1 of prefill sequence b into a shuffled pool (tensor plumbing only)."""
+    npg = (L + sh.Bk - 1) // sh.Bk
+    perm = torch.randperm(npg, generator=torch.Generator().manual_seed(perm_seed))
+    P = npg
+    Kp = torch.zeros(P, sh.Hkv, sh.Bk, sh.D, dtype=torch.bfloat16)
+    Vp = torch.zeros_like(Kp)
+    KIp = torch.zeros(P, sh.Hkv, sh.Bk, sh.dI, dtype=torch.bfloat16)
+    for j in range(npg):
+        t0, t1 = j * sh.Bk, min(L, (j + 1) * sh.Bk)
+        p = int(perm[j])
+        Kp[p, :, :t1 - t0] = inp["K"][b, t0:t1].transpose(0, 1)
+        Vp[p, :, :t1 - t0] = inp["V"][b, t0:t1].transpose(0, 1)
+        KIp[p, :, :t1 - t0] = inp["k_idx"][b, t0:t1].transpose(0, 1)
+    return {
+        "Q": inp["Q"][b, L - 1][None].contiguous(),
+        "q_idx": inp["q_idx"][b, L - 1][None].contiguous(),
+        "w": inp["w"][b, L - 1][None].contiguous(),
+        "K_pool": Kp, "V_pool": Vp, "kidx_pool": KIp,
+        "seq_pt": perm.to(torch.int32)[None].contiguous(),
+        "seq_len": torch.tensor([L], dtype=torch.int32),
+    }
+
+
+def run_decode_oracle(d, sh, nb_stride=None):
+    C = oracle.decode_scores(d["q_idx"], d["w"], d["kidx_pool"], d["seq_pt"], d["seq_len"], nb_stride)
+    own = oracle.own_blocks_decode(d["seq_len"], sh.Bk)
+    sel, cnt, _, _ = oracle.select(C, own[:, None], sh.k)
+    O, LSE = oracle.decode_attend(d["Q"], d["K_pool"], d["V_pool"], d["seq_pt"], d["seq_len"],
+                                  sel, cnt, 1.0 / math.sqrt(sh.D))
+    return C, sel, cnt, O, LSE
+
+
+@pytest.mark.parametrize("L", [1, 128, 129, 500, 700])
+def test_decode_equals_last_prefill_row(L):
+    wl = PrefillWorkload("xpath", B=2, S=700, shape=MSAShape(k=3), seed=7)
+    sh = wl.shape
+    inp = prefill_inputs(wl)
+    b = 1
+    row = np.array([b * wl.S + L - 1], dtype=np.int64)
+    Cp, selp, cntp, Op, LSEp = run_prefill_oracle(inp, sh, row)
+    d = _decode_from_prefill(inp, sh, b, L, perm_seed=L)
+    nb = (L + sh.Bk - 1) // sh.Bk
+    Cd, seld, cntd, Od, LSEd = run_decode_oracle(d, sh)
+    np.testing.assert_array_equal(Cd[0, :, :nb], Cp[0, :, :nb])
+    np.testing.assert_array_equal(seld[0], selp[0])
+    np.testing.assert_array_equal(cntd[0], cntp[0])
+    np.testing.assert_allclose(Od[0], Op[0], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(LSEd[0], LSEp[0], rtol=0, atol=1e-12)
+
+
+def test_decode_page_permutation_invariance():
+    wl = PrefillWorkload("perm", B=1, S=1000, shape=MSAShape(k=4), seed=8)
+    sh = wl.shape
+    inp = prefill_inputs(wl)
+    res = [run_decode_oracle(_decode_from_prefill(inp, sh, 0, 1000, perm_seed=s), sh) for s in (1, 2)]
+    for a, b in zip(res[0], res[1]):
+        np.testing.assert_array_equal(a, b)
+
+
+def test_page_table_flattened_rows_equal_per_group():
+    """Attention through the flattened (B*Hkv) page table equals per-(b, g) attention.
+
+    Every row r = b*Hkv + g is treated as a sequence of its own with one KV head:
+    pages pt[r][0..n), length (n-1)*Bk + last_len, and its G query heads.
+    """
+    wl = DecodeWorkload("pt", lengths=(1, 200, 1000, 1300), shape=MSAShape(k=4), seed=9)
+    sh = wl.shape
+    d = decode_inputs(wl)
+    C, sel, cnt, O, LSE = run_decode_oracle(d, sh)
+    pt, n, last = oracle.page_table(sel, cnt, d["seq_pt"], d["seq_len"], sh.Bk)
+    assert np.array_equal(n, cnt.reshape(-1))
+    G = sh.G
+    for r in range(wl.B * sh.Hkv):
+        b, g = divmod(r, sh.Hkv)
+        assert np.all(pt[r, n[r]:] == -1)
+        dd = {
+            "Q": d["Q"][b, g * G:(g + 1) * G][None].contiguous(),
+            "K_pool": d["K_pool"][:, g:g + 1].contiguous(),
+            "V_pool": d["V_pool"][:, g:g + 1].contiguous(),
+        }
+        L_r = (int(n[r]) - 1) * sh.Bk + int(last[r])
+        sel_r = np.arange(sh.k, dtype=np.int32)[None, None]
+        sel_r = np.where(sel_r < n[r], sel_r, -1).astype(np.int32)
+        o, l = oracle.decode_attend(dd["Q"], dd["K_pool"], dd["V_pool"],
+                                    pt[r][None].copy(), np.array([L_r], dtype=np.int32),
+                                    sel_r, np.array([[n[r]]], dtype=np.int32), 1.0 / math.sqrt(sh.D))
+        np.testing.assert_allclose(o[0], O[b, g * G:(g + 1) * G], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(l[0], LSE[b, g * G:(g + 1) * G], rtol=0, atol=1e-12)
+
+
+def test_decode_own_block_and_last_len():
+    wl = DecodeWorkload("own", lengths=(1, 128, 129, 60001), shape=MSAShape(k=16), seed=10)
+    sh = wl.shape
+    d = decode_inputs(wl)
+    C, sel, cnt, O, LSE = run_decode_oracle(d, sh)
+    _, n, last = oracle.page_table(sel, cnt, d["seq_pt"], d["seq_len"], sh.Bk)
+    # L = 1: own block 0, nothing scored; L = 128: own block 0 full; L = 129: own block 1 holds 1 token;
+    # L = 60001: own block 468 holds 97 tokens (60001 - 468*128)
+    assert list(last.reshape(4, sh.Hkv)[:, 0]) == [1, 128, 1, 97]
+    assert list(cnt[:, 0]) == [1, 1, 2, 16]
+    assert np.all(C[0] == -np.inf) and np.all(C[3, :, 468:] == -np.inf) and np.all(np.isfinite(C[3, :, :468]))
