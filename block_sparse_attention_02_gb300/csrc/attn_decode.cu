@@ -1,0 +1,336 @@
+// attn_decode.cu -- a5: sparse attention of one decode step over the selected
+// pages, the KV-group dimension flattened into the batch.
+//
+// Row r = b * Hkv + g of the page table built from the selected blocks lists
+// n[r] physical pages; the G query heads of group g attend to each page as an
+// independent split of the softmax ("MiniMax M3 preparado para inferencia en
+// produccion", paragraph "MSA con paged attention").  For unit (r, s):
+//     z[h][t] = scale * Q[b, g*G + h] . K_page[t]      (t < valid tokens)
+//     m_h = max_t z,  l_h = sum_t e^{z - m_h},  O_h = sum_t e^{z - m_h} V_t / l_h
+//     O_part[(r*G + h), s] = O_h,   LSE_part[(r*G + h), s] = m_h + ln l_h
+// The partials are merged by the log-sum-exp merge kernel.
+//
+// tcgen05 mapping (one TMEM slot of 32 columns per unit, two slots):
+//   MMA1  S^T[t][h] = K[t][:] . Q[h][:]    M = 128 keys, N = 16 (heads, padded),
+//                                          K = D = 128 (8 MMAs, both K-major)
+//   softmax: one thread per key (TMEM lane), cross-warp max / sum per head,
+//            P^T[h][t] (bf16) written into a K-major B tile
+//   MMA2  O^T[d][h] = V^T[d][:] . P^T[:][h] M = 128 (d), N = 16, K = 128 keys;
+//                                          V is the MN-major A operand
+//   epilogue: one thread per d, coalesced fp32 partial rows.
+// Warp 0 streams K, V (64 KiB) and the row's 16 Q rows by TMA into a 3-deep
+// ring; warp 1 issues the MMAs; warps 2-5 run softmax and epilogue.
+#include "msa_internal.h"
+#include "msa_ptx.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kStages = 3;
+constexpr int kHalf = 128 * 64 * 2;                    // 16 KiB: 128 rows x 64 bf16
+constexpr int kQHalf = 16 * 64 * 2;                    // 2 KiB: 16 rows x 64 bf16
+constexpr int kStageBytes = 4 * kHalf + 2 * kQHalf;    // K0 K1 V0 V1 Q0 Q1
+constexpr int kPTile = 2 * kQHalf;                     // P^T: 16 rows x 128 keys
+constexpr int kSlots = 2;
+constexpr int kTmemCols = 64;
+constexpr int kThreads = 192;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct Params {
+  int B, Hq, Hkv, G, k;
+  float scale_log2;
+  int64_t num_pages;
+  const int32_t* pt;
+  const int32_t* n;
+  const int32_t* last_len;
+  float* o_part;
+  float* lse_part;
+  int32_t* dev_err;
+};
+
+__device__ __forceinline__ bool unit_live(const Params& p, int64_t u, int& r, int& s) {
+  r = static_cast<int>(u / p.k);
+  s = static_cast<int>(u % p.k);
+  return s < p.n[r];
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+attn_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                   const __grid_constant__ CUtensorMap qmap, const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* s_stage = smem;
+  uint8_t* s_p = smem + kStages * kStageBytes;   // kSlots P^T tiles
+
+  __shared__ __align__(8) uint64_t bar_full[kStages], bar_empty[kStages];
+  __shared__ __align__(8) uint64_t bar_sfull[kSlots], bar_pready[kSlots], bar_ofull[kSlots], bar_sfree[kSlots];
+  __shared__ __align__(8) uint64_t bar_drain;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort, s_fail;
+  __shared__ float s_red[4][kMaxG];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t units = static_cast<int64_t>(p.B) * p.Hkv * p.k;
+
+  // empty splits (s >= n[r]) carry LSE = -inf so the merge skips them
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * kThreads + tid; e < units * p.G;
+       e += static_cast<int64_t>(gridDim.x) * kThreads) {
+    const int64_t u = e / p.G;
+    const int h = static_cast<int>(e % p.G);
+    int r, s;
+    if (!unit_live(p, u, r, s)) p.lse_part[(static_cast<int64_t>(r) * p.G + h) * p.k + s] = -INFINITY;
+  }
+  // P^T rows G..15 stay zero for the whole kernel
+  for (int i = tid; i < kSlots * kPTile / 16; i += kThreads)
+    reinterpret_cast<uint4*>(s_p)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) { mbar_init(&bar_full[i], 1); mbar_init(&bar_empty[i], 1); }
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&bar_sfull[i], 1); mbar_init(&bar_pready[i], 4);
+      mbar_init(&bar_ofull[i], 1); mbar_init(&bar_sfree[i], 4);
+    }
+    mbar_init(&bar_drain, 1);
+    s_abort = 0;
+    s_fail = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(&s_tmem, kTmemCols);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  volatile int* abort_flag = &s_abort;
+
+  const int64_t per_cta = (units + gridDim.x - 1) / gridDim.x;
+  const int64_t lo = min(units, static_cast<int64_t>(blockIdx.x) * per_cta);
+  const int64_t hi = min(units, lo + per_cta);
+
+  if (warp == 0) {
+    // ===================== TMA producer =====================
+    if (lane == 0) {
+      int n = 0;
+      for (int64_t u = lo; u < hi; ++u) {
+        int r, s;
+        if (!unit_live(p, u, r, s)) continue;
+        const int st = n % kStages;
+        if (!mbar_wait(&bar_empty[st], ((n / kStages) & 1) ^ 1, abort_flag, p.dev_err)) break;
+        const int64_t page = p.pt[static_cast<int64_t>(r) * p.k + s];
+        const int b = r / p.Hkv, g = r % p.Hkv;
+        uint8_t* sb = s_stage + st * kStageBytes;
+        if (page < 0 || page >= p.num_pages) {
+          mbar_arrive(&bar_full[st]);
+        } else {
+          const int pg = static_cast<int>(page);
+          mbar_arrive_expect_tx(&bar_full[st], kStageBytes);
+          tma_load_4d(sb + 0 * kHalf, &kmap, &bar_full[st], 0, 0, g, pg);
+          tma_load_4d(sb + 1 * kHalf, &kmap, &bar_full[st], 64, 0, g, pg);
+          tma_load_4d(sb + 2 * kHalf, &vmap, &bar_full[st], 0, 0, g, pg);
+          tma_load_4d(sb + 3 * kHalf, &vmap, &bar_full[st], 64, 0, g, pg);
+          tma_load_3d(sb + 4 * kHalf, &qmap, &bar_full[st], 0, g * p.G, b);
+          tma_load_3d(sb + 4 * kHalf + kQHalf, &qmap, &bar_full[st], 64, g * p.G, b);
+        }
+        ++n;
+      }
+      if (*abort_flag) {
+        for (int i = max(0, n - kStages); i < n; ++i) {
+          uint64_t t0 = global_timer_ns();
+          while (!mbar_try_wait(&bar_full[i % kStages], (i / kStages) & 1) &&
+                 global_timer_ns() - t0 < MSA_WAIT_LIMIT_NS) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ===================== tcgen05 issuer =====================
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(128, 16, false, false);
+      constexpr uint32_t idesc_o = idesc_bf16(128, 16, true, false);
+      int n = 0;
+      for (int64_t u = lo; u < hi; ++u) {
+        int r, s;
+        if (!unit_live(p, u, r, s)) continue;
+        const int st = n % kStages, slot = n % kSlots;
+        const uint32_t ph_slot = (n / kSlots) & 1;
+        if (!mbar_wait(&bar_full[st], (n / kStages) & 1, abort_flag, p.dev_err)) break;
+        if (!mbar_wait(&bar_sfree[slot], ph_slot ^ 1, abort_flag, p.dev_err)) break;
+        tc_fence_after();
+        const uint32_t sb = smem_u32(s_stage + st * kStageBytes);
+        const uint32_t d_s = tmem + slot * 32, d_o = tmem + slot * 32 + 16;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalf + 32 * (kk & 3);
+          const uint32_t qoff = 4 * kHalf + (kk >> 2) * kQHalf + 32 * (kk & 3);
+          umma_bf16(d_s, sdesc_sw128(sb + off, 16, 1024), sdesc_sw128(sb + qoff, 16, 1024), idesc_s, kk > 0);
+        }
+        umma_commit(&bar_sfull[slot]);
+        if (!mbar_wait(&bar_pready[slot], ph_slot, abort_flag, p.dev_err)) break;
+        tc_fence_after();
+        const uint32_t pb = smem_u32(s_p + slot * kPTile);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t voff = 2 * kHalf + kk * 2048;          // 16 keys per step
+          const uint32_t poff = (kk >> 2) * kQHalf + 32 * (kk & 3);
+          umma_bf16(d_o, sdesc_sw128(sb + voff, kHalf, 1024), sdesc_sw128(pb + poff, 16, 1024), idesc_o, kk > 0);
+        }
+        umma_commit(&bar_ofull[slot]);
+        umma_commit(&bar_empty[st]);
+        ++n;
+      }
+      umma_commit(&bar_drain);
+      uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(&bar_drain, 0) && global_timer_ns() - t0 < MSA_WAIT_LIMIT_NS) {
+      }
+    }
+    __syncwarp();
+  } else {
+    // ===================== softmax + epilogue (warps 2..5) =====================
+    const int q = warp & 3;
+    const int t = q * 32 + lane;                 // key index (MMA1) / d index (MMA2)
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    const int G = p.G;
+    int n = 0;
+    for (int64_t u = lo; u < hi; ++u) {
+      int r, s;
+      if (!unit_live(p, u, r, s)) continue;
+      const int slot = n % kSlots;
+      const uint32_t ph_slot = (n / kSlots) & 1;
+      // ---- S^T ready: every epilogue warp decides together whether to go on
+      if (!mbar_wait(&bar_sfull[slot], ph_slot, abort_flag, p.dev_err)) s_fail = 1;
+      named_bar_sync(1, 128);
+      if (s_fail) break;
+      tc_fence_after();
+      uint32_t sv[8];
+      tmem_ld8(tmem + lane_addr + slot * 32, sv);
+      tmem_ld_wait();
+      const int valid = (s == p.n[r] - 1) ? p.last_len[r] : kBk;
+      float z[kMaxG];
+      float mx[kMaxG];
+#pragma unroll
+      for (int h = 0; h < kMaxG; ++h) {
+        z[h] = (t < valid) ? __uint_as_float(sv[h]) * p.scale_log2 : -INFINITY;
+        float v = z[h];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+        mx[h] = v;
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < kMaxG; ++h) s_red[q][h] = mx[h];
+      }
+      named_bar_sync(1, 128);
+      float l[kMaxG];
+#pragma unroll
+      for (int h = 0; h < kMaxG; ++h) {
+        mx[h] = fmaxf(fmaxf(s_red[0][h], s_red[1][h]), fmaxf(s_red[2][h], s_red[3][h]));
+        const float e = (t < valid) ? exp2f(z[h] - mx[h]) : 0.f;
+        z[h] = e;
+        float v = e;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        l[h] = v;
+      }
+      named_bar_sync(1, 128);           // everyone has read the maxima
+      if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < kMaxG; ++h) s_red[q][h] = l[h];
+      }
+      // P^T[h][t] into the K-major B tile of this slot
+      uint8_t* pt_tile = s_p + slot * kPTile + (t >> 6) * kQHalf;
+      const uint32_t tc = static_cast<uint32_t>(t & 63);
+#pragma unroll
+      for (int h = 0; h < kMaxG; ++h) {
+        if (h < G) {
+          __nv_bfloat16 b = __float2bfloat16_rn(z[h]);
+          *reinterpret_cast<__nv_bfloat16*>(pt_tile + sw128_offset(h, tc >> 3) + (tc & 7) * 2) = b;
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_pready[slot]);
+      named_bar_sync(1, 128);
+#pragma unroll
+      for (int h = 0; h < kMaxG; ++h) l[h] = s_red[0][h] + s_red[1][h] + s_red[2][h] + s_red[3][h];
+      // ---- O^T ready
+      if (!mbar_wait(&bar_ofull[slot], ph_slot, abort_flag, p.dev_err)) s_fail = 1;
+      named_bar_sync(1, 128);
+      if (s_fail) break;
+      tc_fence_after();
+      uint32_t ov[8];
+      tmem_ld8(tmem + lane_addr + slot * 32 + 16, ov);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_sfree[slot]);
+      const int64_t page = p.pt[static_cast<int64_t>(r) * p.k + s];
+      const bool bad = page < 0 || page >= p.num_pages;
+      if (bad && t == 0) report(p.dev_err, MSA_DEVERR_BAD_PAGE);
+#pragma unroll
+      for (int h = 0; h < kMaxG; ++h) {
+        if (h < G) {
+          const int64_t row = (static_cast<int64_t>(r) * G + h) * p.k + s;
+          p.o_part[row * kD + t] = bad ? 0.f : __uint_as_float(ov[h]) / l[h];
+          if (t == h) p.lse_part[row] = bad ? -INFINITY : (mx[h] + log2f(l[h])) * kLn2;
+        }
+      }
+      ++n;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+msa_status launch_attn_decode(const msa_decode_args& a, float* o_part, float* lse_part, cudaStream_t stream) {
+  DeviceInfo dev;
+  if (msa_status st = current_device(&dev); st != MSA_OK) return st;
+  CUtensorMap kmap, vmap, qmap;
+  const uint64_t kv_dims[4] = {static_cast<uint64_t>(a.D), static_cast<uint64_t>(a.Bk), static_cast<uint64_t>(a.Hkv),
+                               static_cast<uint64_t>(a.num_pages)};
+  const uint64_t kv_strides[3] = {static_cast<uint64_t>(a.kv_stride[2]) * 2, static_cast<uint64_t>(a.kv_stride[1]) * 2,
+                                  static_cast<uint64_t>(a.kv_stride[0]) * 2};
+  const uint32_t kv_box[4] = {64, 128, 1, 1};
+  if (msa_status st = encode_tiled_map(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, a.K_pool, kv_dims, kv_strides,
+                                       kv_box, CU_TENSOR_MAP_SWIZZLE_128B, "K page pool");
+      st != MSA_OK)
+    return st;
+  if (msa_status st = encode_tiled_map(&vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, a.V_pool, kv_dims, kv_strides,
+                                       kv_box, CU_TENSOR_MAP_SWIZZLE_128B, "V page pool");
+      st != MSA_OK)
+    return st;
+  const uint64_t q_dims[3] = {static_cast<uint64_t>(a.D), static_cast<uint64_t>(a.Hq), static_cast<uint64_t>(a.B)};
+  const uint64_t q_strides[2] = {static_cast<uint64_t>(a.Q_stride[1]) * 2, static_cast<uint64_t>(a.Q_stride[0]) * 2};
+  const uint32_t q_box[3] = {64, 16, 1};
+  if (msa_status st = encode_tiled_map(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.Q, q_dims, q_strides, q_box,
+                                       CU_TENSOR_MAP_SWIZZLE_128B, "Q");
+      st != MSA_OK)
+    return st;
+
+  Params p;
+  p.B = a.B; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = a.Hq / a.Hkv; p.k = a.k;
+  const float scale = a.softmax_scale > 0.f ? a.softmax_scale : 1.0f / sqrtf(static_cast<float>(a.D));
+  p.scale_log2 = scale * kLog2e;
+  p.num_pages = a.num_pages; p.pt = a.pt; p.n = a.n; p.last_len = a.last_len;
+  p.o_part = o_part; p.lse_part = lse_part; p.dev_err = a.dev_err;
+
+  const size_t smem = 1024 + static_cast<size_t>(kStages) * kStageBytes + kSlots * kPTile;
+  if (smem > dev.max_smem_optin) return fail(MSA_ERR_UNSUPPORTED, "decode attention: not enough shared memory");
+  cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attn_decode)");
+  const int64_t units = static_cast<int64_t>(a.B) * a.Hkv * a.k;
+  const int grid = static_cast<int>(std::min<int64_t>(dev.num_sms, std::max<int64_t>(units, 1)));
+  attn_decode_kernel<<<grid, kThreads, smem, stream>>>(kmap, vmap, qmap, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "attn_decode_kernel launch");
+  return MSA_OK;
+}
+
+}  // namespace msa

@@ -1,0 +1,346 @@
+// index_decode.cu -- a1 (decode): block scores of the Index Branch over a paged
+// index-key cache.
+//
+// For every sequence b, KV group g and block j strictly before the query's own
+// block ((L_b - 1) / Bk):
+//     c_j = max_{t in block j} sum_{h < HI} w[b,g,h] * ReLU(q_idx[b,g,h] . k_idx_t)
+// ("MiniMax M3: Como la atencion dispersa hace practicos a los agentes de largo
+// alcance", MSA paragraph and caption: a light Index Branch scores the context
+// in blocks; the formula is this library's, the pages give none.)
+//
+// This is an HBM stream: each (page, group) block of k_idx is 16 KiB, read
+// once.  A persistent CTA per SM walks a contiguous range of the flattened
+// (b, g, j) items:
+//   warp 0    TMA producer: one 4-D tiled load (128 tokens x 64 dims, 128-byte
+//             swizzle) per block into an 8-deep shared-memory ring;
+//   warp 1    tcgen05 issuer: D[t, h] = k_idx_t . q_idx_h as one M=128 (tokens)
+//             x N=16 (index heads, zero-padded) x K=64 contraction (4 MMAs)
+//             into one of 8 TMEM slots; it also stages q_idx of the current
+//             (b, g) as the B operand (double-buffered);
+//   warps 2-5 epilogue: thread = token; w-weighted ReLU sum over heads, max
+//             over the block's 128 tokens, one fp32 store per block.
+#include "msa_internal.h"
+#include "msa_ptx.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kStages = 8;
+constexpr int kSlots = 8;
+constexpr int kSlotCols = 16;
+constexpr int kTmemCols = 128;
+constexpr int kStageBytes = kBk * kDI * 2;   // 16 KiB
+constexpr int kQTileBytes = 16 * kDI * 2;    // 2 KiB: 16 rows (HI used) x 64
+constexpr int kThreads = 192;
+// Partial-max buffers of the epilogue.  A warp can be at most kSlots items
+// ahead of the slowest one (TMEM slots are released by all four), so twice
+// that many buffers are never reused while still being read.
+constexpr int kRedBufs = 2 * kSlots;
+
+struct Params {
+  int B, Hkv, HI, Bk;
+  const __nv_bfloat16* q_idx;
+  int64_t qs0, qs1, qs2;
+  const float* w;
+  int64_t ws0, ws1;
+  int64_t num_pages;
+  const int32_t* seq_pt;
+  int64_t max_pages;
+  const int32_t* seq_len;
+  float* C;
+  int64_t cs0, cs1;
+  int nb_stride;
+  int32_t* dev_err;
+};
+
+struct Walker {  // position in the flattened (b, g, j) item space
+  int b, g, j;
+};
+
+__device__ __forceinline__ void walk_init(Walker& w, int64_t n, const int* pre, const int* own, int B, int Hkv) {
+  // largest b with pre[b] <= n (pre is non-decreasing; items of b are [pre[b], pre[b+1]))
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (pre[mid] <= n) lo = mid; else hi = mid - 1;
+  }
+  int b = lo;
+  while (b < B - 1 && pre[b + 1] <= n) ++b;   // skip sequences with no items
+  int64_t rem = n - pre[b];
+  w.b = b;
+  w.g = static_cast<int>(rem / own[b]);
+  w.j = static_cast<int>(rem % own[b]);
+  (void)Hkv;
+}
+
+__device__ __forceinline__ void walk_next(Walker& w, const int* own, int B, int Hkv) {
+  if (++w.j < own[w.b]) return;
+  w.j = 0;
+  if (++w.g < Hkv) return;
+  w.g = 0;
+  do { ++w.b; } while (w.b < B && own[w.b] == 0);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* s_stage = smem;                                   // kStages x 16 KiB
+  uint8_t* s_q = smem + kStages * kStageBytes;               // 2 x 2 KiB
+  int* s_pre = reinterpret_cast<int*>(s_q + 2 * kQTileBytes); // B + 1
+  int* s_own = s_pre + (p.B + 1);                             // B
+
+  __shared__ __align__(8) uint64_t bar_full[kStages], bar_empty[kStages];
+  __shared__ __align__(8) uint64_t bar_tfull[kSlots], bar_tempty[kSlots];
+  __shared__ __align__(8) uint64_t bar_qdone[2], bar_drain;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ float s_red[kRedBufs][4];
+  __shared__ int s_cnt[kRedBufs];
+  __shared__ int s_chunk[kThreads];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- per-sequence own blocks and the prefix over (b, g, j) items ----
+  for (int b = tid; b < p.B; b += kThreads) {
+    const int L = p.seq_len[b];
+    int own = 0;
+    if (L < 1 || static_cast<int64_t>(L) > p.max_pages * p.Bk || (L - 1) / p.Bk >= p.nb_stride) {
+      if (blockIdx.x == 0) report(p.dev_err, MSA_DEVERR_BAD_LEN);
+    } else {
+      own = (L - 1) / p.Bk;
+    }
+    s_own[b] = own;
+  }
+  __syncthreads();
+  {
+    const int per = (p.B + kThreads - 1) / kThreads;
+    const int b0 = tid * per, b1 = min(p.B, b0 + per);
+    int sum = 0;
+    for (int b = b0; b < b1; ++b) sum += s_own[b] * p.Hkv;
+    s_chunk[tid] = sum;
+    __syncthreads();
+    if (tid == 0) {
+      int run = 0;
+      for (int t = 0; t < kThreads; ++t) { int v = s_chunk[t]; s_chunk[t] = run; run += v; }
+      s_pre[p.B] = run;
+    }
+    __syncthreads();
+    int run = s_chunk[tid];
+    for (int b = b0; b < b1; ++b) { s_pre[b] = run; run += s_own[b] * p.Hkv; }
+  }
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) { mbar_init(&bar_full[i], 1); mbar_init(&bar_empty[i], 1); }
+    for (int i = 0; i < kSlots; ++i) { mbar_init(&bar_tfull[i], 1); mbar_init(&bar_tempty[i], 4); }
+    mbar_init(&bar_qdone[0], 1); mbar_init(&bar_qdone[1], 1); mbar_init(&bar_drain, 1);
+    s_abort = 0;
+    for (int i = 0; i < kRedBufs; ++i) s_cnt[i] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(&s_tmem, kTmemCols);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  volatile int* abort_flag = &s_abort;
+
+  // ---- -inf for the own block and everything after it ----
+  {
+    const int64_t total = static_cast<int64_t>(p.B) * p.Hkv * p.nb_stride;
+    for (int64_t e = static_cast<int64_t>(blockIdx.x) * kThreads + tid; e < total;
+         e += static_cast<int64_t>(gridDim.x) * kThreads) {
+      int j = static_cast<int>(e % p.nb_stride);
+      int64_t bg = e / p.nb_stride;
+      int b = static_cast<int>(bg / p.Hkv), g = static_cast<int>(bg % p.Hkv);
+      if (j >= s_own[b]) p.C[b * p.cs0 + g * p.cs1 + j] = -INFINITY;
+    }
+  }
+
+  const int64_t total_items = s_pre[p.B];
+  const int64_t per_cta = (total_items + gridDim.x - 1) / gridDim.x;
+  const int64_t lo = min(total_items, static_cast<int64_t>(blockIdx.x) * per_cta);
+  const int64_t hi = min(total_items, lo + per_cta);
+  const int count = static_cast<int>(hi - lo);
+
+  if (warp == 0) {
+    // ===================== TMA producer =====================
+    if (lane == 0 && count > 0) {
+      Walker it;
+      walk_init(it, lo, s_pre, s_own, p.B, p.Hkv);
+      int issued = 0;
+      for (int n = 0; n < count; ++n) {
+        const int st = n % kStages;
+        const uint32_t ph = (n / kStages) & 1;
+        if (!mbar_wait(&bar_empty[st], ph ^ 1, abort_flag, p.dev_err)) break;
+        const int64_t page = p.seq_pt[it.b * p.max_pages + it.j];
+        if (page < 0 || page >= p.num_pages) {
+          mbar_arrive(&bar_full[st]);   // nothing to load; the epilogue reports the bad page
+        } else {
+          mbar_arrive_expect_tx(&bar_full[st], kStageBytes);
+          tma_load_4d(s_stage + st * kStageBytes, &kmap, &bar_full[st], 0, 0, it.g, static_cast<int>(page));
+        }
+        ++issued;
+        walk_next(it, s_own, p.B, p.Hkv);
+      }
+      if (*abort_flag) {  // drain loads still in flight before the CTA exits
+        for (int n = max(0, issued - kStages); n < issued; ++n) {
+          uint64_t t0 = global_timer_ns();
+          while (!mbar_try_wait(&bar_full[n % kStages], (n / kStages) & 1) &&
+                 global_timer_ns() - t0 < MSA_WAIT_LIMIT_NS) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ===================== tcgen05 issuer =====================
+    constexpr uint32_t idesc = idesc_bf16(128, 16, false, false);
+    Walker it;
+    if (count > 0) walk_init(it, lo, s_pre, s_own, p.B, p.Hkv);
+    int cur_b = -1, cur_g = -1, seg = -1;
+    for (int n = 0; n < count; ++n) {
+      const int st = n % kStages, slot = n % kSlots;
+      if (it.b != cur_b || it.g != cur_g) {
+        // new (b, g): stage its q_idx as the B operand in the other buffer
+        if (lane == 0 && seg >= 0) umma_commit(&bar_qdone[seg & 1]);
+        ++seg;
+        const int buf = seg & 1;
+        bool ok = true;
+        if (seg >= 2 && lane == 0) ok = mbar_wait(&bar_qdone[buf], ((seg >> 1) - 1) & 1, abort_flag, p.dev_err);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        uint8_t* qt = s_q + buf * kQTileBytes;
+        for (int c = lane; c < 16 * 8; c += 32) {
+          const int r = c >> 3, ch = c & 7;
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (r < p.HI)
+            v = *reinterpret_cast<const uint4*>(p.q_idx + it.b * p.qs0 + it.g * p.qs1 + r * p.qs2 + ch * 8);
+          *reinterpret_cast<uint4*>(qt + sw128_offset(r, ch)) = v;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        cur_b = it.b;
+        cur_g = it.g;
+      }
+      bool ok = true;
+      if (lane == 0) {
+        ok = mbar_wait(&bar_full[st], (n / kStages) & 1, abort_flag, p.dev_err) &&
+             mbar_wait(&bar_tempty[slot], ((n / kSlots) & 1) ^ 1, abort_flag, p.dev_err);
+        if (ok) {
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(s_stage + st * kStageBytes);
+          const uint32_t b0 = smem_u32(s_q + (seg & 1) * kQTileBytes);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            umma_bf16(tmem + slot * kSlotCols, sdesc_sw128(a0 + 32 * k, 16, 1024), sdesc_sw128(b0 + 32 * k, 16, 1024),
+                      idesc, k > 0);
+          umma_commit(&bar_empty[st]);
+          umma_commit(&bar_tfull[slot]);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      walk_next(it, s_own, p.B, p.Hkv);
+    }
+    if (lane == 0) {  // every MMA issued by this thread is complete before TMEM is freed
+      umma_commit(&bar_drain);
+      uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(&bar_drain, 0) && global_timer_ns() - t0 < MSA_WAIT_LIMIT_NS) {
+      }
+    }
+    __syncwarp();
+  } else {
+    // ===================== epilogue (warps 2..5) =====================
+    const int q = warp & 3;                       // TMEM lane quarter of this warp
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    Walker it;
+    if (count > 0) walk_init(it, lo, s_pre, s_own, p.B, p.Hkv);
+    int cur_b = -1, cur_g = -1;
+    float wv[kMaxHI] = {0.f, 0.f, 0.f, 0.f};
+    for (int n = 0; n < count; ++n) {
+      const int slot = n % kSlots;
+      if (it.b != cur_b || it.g != cur_g) {
+        for (int h = 0; h < kMaxHI; ++h) wv[h] = h < p.HI ? p.w[it.b * p.ws0 + it.g * p.ws1 + h] : 0.f;
+        cur_b = it.b;
+        cur_g = it.g;
+      }
+      if (!mbar_wait(&bar_tfull[slot], (n / kSlots) & 1, abort_flag, p.dev_err)) break;
+      tc_fence_after();
+      uint32_t v[4];
+      tmem_ld4(tmem + lane_addr + slot * kSlotCols, v);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_tempty[slot]);
+      float s = 0.f;
+#pragma unroll
+      for (int h = 0; h < kMaxHI; ++h) s = fmaf(wv[h], fmaxf(__uint_as_float(v[h]), 0.f), s);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s = fmaxf(s, __shfl_xor_sync(0xffffffffu, s, o));
+      // cross-warp max without a barrier: the last of the four warps to arrive
+      // combines the partial maxima and stores the block score.
+      if (lane == 0) {
+        const int rb = n % kRedBufs;
+        s_red[rb][q] = s;
+        __threadfence_block();
+        if (atomicAdd(&s_cnt[rb], 1) == 3) {
+          __threadfence_block();
+          float m = fmaxf(fmaxf(s_red[rb][0], s_red[rb][1]), fmaxf(s_red[rb][2], s_red[rb][3]));
+          s_cnt[rb] = 0;
+          const int64_t page = p.seq_pt[it.b * p.max_pages + it.j];
+          if (page < 0 || page >= p.num_pages) {
+            m = -INFINITY;
+            report(p.dev_err, MSA_DEVERR_BAD_PAGE);
+          }
+          p.C[it.b * p.cs0 + it.g * p.cs1 + it.j] = m;
+        }
+      }
+      walk_next(it, s_own, p.B, p.Hkv);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+msa_status launch_index_decode(const msa_index_args& a, cudaStream_t stream) {
+  DeviceInfo dev;
+  if (msa_status st = current_device(&dev); st != MSA_OK) return st;
+  // k_idx pool as a 4-D tensor (dI, t, g, page) with a 64 x 128 x 1 x 1 box
+  CUtensorMap kmap;
+  const uint64_t dims[4] = {static_cast<uint64_t>(a.dI), static_cast<uint64_t>(a.Bk),
+                            static_cast<uint64_t>(a.Hkv), static_cast<uint64_t>(a.num_pages)};
+  const uint64_t strides[3] = {static_cast<uint64_t>(a.k_idx_stride[2]) * 2, static_cast<uint64_t>(a.k_idx_stride[1]) * 2,
+                               static_cast<uint64_t>(a.k_idx_stride[0]) * 2};
+  const uint32_t box[4] = {64, 128, 1, 1};
+  if (msa_status st = encode_tiled_map(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, a.k_idx, dims, strides, box,
+                                       CU_TENSOR_MAP_SWIZZLE_128B, "k_idx page pool");
+      st != MSA_OK)
+    return st;
+
+  Params p;
+  p.B = a.B; p.Hkv = a.Hkv; p.HI = a.HI; p.Bk = a.Bk;
+  p.q_idx = static_cast<const __nv_bfloat16*>(a.q_idx);
+  p.qs0 = a.q_idx_stride[0]; p.qs1 = a.q_idx_stride[1]; p.qs2 = a.q_idx_stride[2];
+  p.w = a.w; p.ws0 = a.w_stride[0]; p.ws1 = a.w_stride[1];
+  p.num_pages = a.num_pages; p.seq_pt = a.seq_pt; p.max_pages = a.max_pages; p.seq_len = a.seq_len;
+  p.C = a.C; p.cs0 = a.C_stride[0]; p.cs1 = a.C_stride[1]; p.nb_stride = a.nb_stride;
+  p.dev_err = a.dev_err;
+
+  const size_t smem = 1024 + kStages * kStageBytes + 2 * kQTileBytes + (2 * static_cast<size_t>(a.B) + 1) * 4;
+  if (smem > dev.max_smem_optin) return fail(MSA_ERR_UNSUPPORTED, "decode index score: batch too large for shared memory");
+  cudaError_t e = cudaFuncSetAttribute(index_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(index_decode)");
+  const int grid = dev.num_sms;
+  index_decode_kernel<<<grid, kThreads, smem, stream>>>(kmap, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "index_decode_kernel launch");
+  return MSA_OK;
+}
+
+}  // namespace msa

@@ -1,0 +1,80 @@
+// lse_merge.cu -- a6: log-sum-exp merge of partial softmax results.
+//
+// The KV-block-major kernels compute partial outputs per block and recombine
+// them with a final log-sum-exp based reduction ("MiniMax M3 preparado para
+// inferencia en produccion", paragraph "KV-Block-Major"):
+//     LSE = ln sum_p e^{LSE_p},   O = sum_p e^{LSE_p - LSE} O_p.
+// One warp per output row; each lane owns float4 column groups.  Parts with
+// LSE_p = -inf are empty and are neither weighted nor read.
+#include "msa_internal.h"
+#include "msa_ptx.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kWarps = 8;
+
+__global__ void __launch_bounds__(kWarps * 32)
+lse_merge_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part, int64_t rows, int parts, int D,
+                 __nv_bfloat16* __restrict__ O, float* __restrict__ LSE) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const float* lp = lse_part + row * parts;
+  // two parts per lane cover parts <= 64
+  const float l0 = lane < parts ? lp[lane] : -INFINITY;
+  const float l1 = lane + 32 < parts ? lp[lane + 32] : -INFINITY;
+  float m = fmaxf(l0, l1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __nv_bfloat16* orow = O + row * D;
+  if (m == -INFINITY) {
+    for (int c = lane * 4; c < D; c += 128) {
+      *reinterpret_cast<uint2*>(orow + c) = make_uint2(0, 0);
+    }
+    if (lane == 0 && LSE != nullptr) LSE[row] = -INFINITY;
+    return;
+  }
+  float sum = (l0 == -INFINITY ? 0.f : __expf(l0 - m)) + (l1 == -INFINITY ? 0.f : __expf(l1 - m));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float lse = m + __logf(sum);
+  const float inv = 1.0f / sum;
+  const float* op = o_part + row * static_cast<int64_t>(parts) * D;
+  for (int c = lane * 4; c < D; c += 128) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int pi = 0; pi < parts; ++pi) {
+      const float lpi = __shfl_sync(0xffffffffu, pi < 32 ? l0 : l1, pi & 31);
+      if (lpi == -INFINITY) continue;
+      const float wgt = __expf(lpi - m) * inv;
+      const float4 v = *reinterpret_cast<const float4*>(op + static_cast<int64_t>(pi) * D + c);
+      acc.x = fmaf(wgt, v.x, acc.x);
+      acc.y = fmaf(wgt, v.y, acc.y);
+      acc.z = fmaf(wgt, v.z, acc.z);
+      acc.w = fmaf(wgt, v.w, acc.w);
+    }
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 packed;
+    packed.x = *reinterpret_cast<uint32_t*>(&lo);
+    packed.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(orow + c) = packed;
+  }
+  if (lane == 0 && LSE != nullptr) LSE[row] = lse;
+}
+
+}  // namespace
+
+msa_status launch_lse_merge(const float* o_part, const float* lse_part, int64_t rows, int parts, int D, void* O,
+                            float* LSE, int32_t* dev_err, cudaStream_t stream) {
+  (void)dev_err;
+  if (rows == 0) return MSA_OK;
+  const int64_t grid = (rows + kWarps - 1) / kWarps;
+  lse_merge_kernel<<<static_cast<unsigned>(grid), kWarps * 32, 0, stream>>>(
+      o_part, lse_part, rows, parts, D, static_cast<__nv_bfloat16*>(O), LSE);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "lse_merge_kernel launch");
+  return MSA_OK;
+}
+
+}  // namespace msa

@@ -1,0 +1,272 @@
+// topk.cu -- a2: per (query, KV group) block selection.
+//
+// Keep the query's own block plus the k-1 best earlier blocks, ranked by
+// (score desc, block index asc); with at most k-1 earlier blocks keep them all
+// ("MiniMax M3: Como la atencion dispersa hace practicos a los agentes de largo
+// alcance", bullet "Costo predecible a cualquier longitud": k = 16 blocks,
+// own block included).  The output row is ascending, own block last, padded
+// with -1.
+//
+// Scores are mapped to order-preserving 32-bit keys (NaN lowest, -0 == +0);
+// the composite key (key << 32 | ~j) makes every candidate distinct, so the
+// selected set is unique.
+//
+// Short rows (<= 32 * NPL candidates, all prefill rows and short decode rows):
+// one warp per row, candidates in registers.  A threshold T0 = the m-th largest
+// of the 32 lane maxima (m = k-1 <= 32) is a lower bound of the m-th largest
+// key, so every selected candidate has key >= T0.  The survivors (usually a
+// few dozen) are compacted in index order into shared memory and ranked
+// exactly; more than kCap survivors (massive ties) take an exact successive
+// arg-max over the registers instead.
+// Long decode rows: one 256-thread CTA per row, successive block-wide arg-max.
+#include "msa_internal.h"
+#include "msa_ptx.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kWarpsPerCta = 8;
+constexpr int kCap = 128;          // survivors ranked in shared memory per warp
+constexpr int kCtaThreads = 256;
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+  if (f != f) return 0u;           // NaN below everything
+  f = f + 0.0f;                    // -0 -> +0
+  uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ uint64_t comp_key(uint32_t u, int j) {
+  return (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(j));
+}
+__device__ __forceinline__ int comp_index(uint64_t K) {
+  return static_cast<int>(~static_cast<uint32_t>(K & 0xffffffffu));
+}
+
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    uint64_t x = __shfl_xor_sync(0xffffffffu, v, o);
+    v = x > v ? x : v;
+  }
+  return v;
+}
+
+struct RowInfo {
+  const float* c;     // score row
+  int own;            // own block = number of candidates
+  int32_t* sel;
+  int32_t* cnt;
+  bool valid;
+};
+
+__device__ __forceinline__ RowInfo row_info(const msa_topk_args& a, int64_t row) {
+  RowInfo r;
+  if (a.mode == MSA_MODE_PREFILL) {
+    const int64_t g = row % a.Hkv, bs = row / a.Hkv;
+    const int64_t s = bs % a.S, b = bs / a.S;
+    r.c = a.C + b * a.C_stride[0] + s * a.C_stride[1] + g * a.C_stride[2];
+    r.own = static_cast<int>(s / a.Bk);
+    r.valid = true;
+  } else {
+    const int64_t g = row % a.Hkv, b = row / a.Hkv;
+    r.c = a.C + b * a.C_stride[0] + g * a.C_stride[1];
+    const int L = a.seq_len[b];
+    r.valid = L >= 1 && (L - 1) / a.Bk < a.nb_stride;
+    r.own = r.valid ? (L - 1) / a.Bk : 0;
+  }
+  r.sel = a.sel + row * a.k;
+  r.cnt = a.count + row;
+  return r;
+}
+
+// Rows with own <= k - 1 (and invalid rows): keep every earlier block.
+__device__ __forceinline__ void write_all(const RowInfo& r, int k, int lane_or_tid, int stride) {
+  for (int x = lane_or_tid; x < k; x += stride) r.sel[x] = (r.valid && x <= r.own) ? x : -1;
+  if (lane_or_tid == 0) *r.cnt = r.valid ? r.own + 1 : 0;
+}
+
+template <int NPL>
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+topk_warp_kernel(const msa_topk_args a, int64_t rows) {
+  __shared__ uint64_t s_surv[kWarpsPerCta][kCap];
+  __shared__ int s_pick[kWarpsPerCta][kMaxK];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + wid;
+  if (row >= rows) return;
+  RowInfo r = row_info(a, row);
+  if (!r.valid && lane == 0) report(a.dev_err, MSA_DEVERR_BAD_LEN);
+  const int m = a.k - 1;
+  const int n = r.own;
+  if (!r.valid || n <= m) {
+    write_all(r, a.k, lane, 32);
+    return;
+  }
+  uint32_t u[NPL];
+  uint32_t lmax = 0;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int j = lane + 32 * i;
+    u[i] = (j < n) ? order_key(r.c[j]) : 0u;
+    lmax = max(lmax, u[i]);
+  }
+  // T0 = m-th largest lane maximum (bitonic sort, descending over lanes)
+  uint32_t T0 = 0;
+  if (m <= 32) {
+    uint32_t v = lmax;
+#pragma unroll
+    for (int kk = 2; kk <= 32; kk <<= 1) {
+#pragma unroll
+      for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+        const uint32_t o = __shfl_xor_sync(0xffffffffu, v, jj);
+        const bool desc = (lane & kk) == 0;
+        const bool lower = (lane & jj) == 0;
+        v = (lower == desc) ? max(v, o) : min(v, o);
+      }
+    }
+    T0 = __shfl_sync(0xffffffffu, v, m - 1);
+  }
+  // compact survivors (key >= T0) in index order
+  int c = 0;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int j = lane + 32 * i;
+    const bool f = (j < n) && u[i] >= T0;
+    const uint32_t mask = __ballot_sync(0xffffffffu, f);
+    const int pos = c + __popc(mask & ((1u << lane) - 1u));
+    if (f && pos < kCap) s_surv[wid][pos] = comp_key(u[i], j);
+    c += __popc(mask);
+  }
+  __syncwarp();
+  int out = 0;
+  if (c <= kCap) {
+    // exact rank of every survivor; the m best have rank < m
+    for (int base = 0; base < c; base += 32) {
+      const int x = base + lane;
+      bool pick = false;
+      int jx = 0;
+      if (x < c) {
+        const uint64_t Kx = s_surv[wid][x];
+        int rank = 0;
+        for (int y = 0; y < c; ++y) rank += s_surv[wid][y] > Kx;
+        pick = rank < m;
+        jx = comp_index(Kx);
+      }
+      const uint32_t mask = __ballot_sync(0xffffffffu, pick);
+      if (pick) r.sel[out + __popc(mask & ((1u << lane) - 1u))] = jx;
+      out += __popc(mask);
+    }
+  } else {
+    // exact fallback: m rounds of arg-max below the previous pick
+    uint64_t prev = ~0ull;
+    for (int t = 0; t < m; ++t) {
+      uint64_t best = 0;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) {
+        const int j = lane + 32 * i;
+        if (j < n) {
+          const uint64_t K = comp_key(u[i], j);
+          if (K < prev && K > best) best = K;
+        }
+      }
+      best = warp_max_u64(best);
+      prev = best;
+      if (lane == 0) s_pick[wid][t] = comp_index(best);
+    }
+    __syncwarp();
+    // ascending order by counting
+    for (int t = lane; t < m; t += 32) {
+      const int jt = s_pick[wid][t];
+      int pos = 0;
+      for (int y = 0; y < m; ++y) pos += s_pick[wid][y] < jt;
+      r.sel[pos] = jt;
+    }
+    out = m;
+  }
+  if (lane == 0) {
+    r.sel[m] = n;          // own block, the largest selected index
+    *r.cnt = m + 1;
+  }
+  for (int x = m + 1 + lane; x < a.k; x += 32) r.sel[x] = -1;
+  (void)out;
+}
+
+// One CTA per long row: m rounds of block-wide arg-max below the previous pick.
+__global__ void __launch_bounds__(kCtaThreads)
+topk_cta_kernel(const msa_topk_args a, int64_t rows) {
+  __shared__ uint64_t s_wmax[kCtaThreads / 32];
+  __shared__ uint64_t s_best;
+  __shared__ int s_pick[kMaxK];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int64_t row = blockIdx.x;
+  if (row >= rows) return;
+  RowInfo r = row_info(a, row);
+  if (!r.valid && tid == 0) report(a.dev_err, MSA_DEVERR_BAD_LEN);
+  const int m = a.k - 1;
+  const int n = r.own;
+  if (!r.valid || n <= m) {
+    write_all(r, a.k, tid, kCtaThreads);
+    return;
+  }
+  uint64_t prev = ~0ull;
+  for (int t = 0; t < m; ++t) {
+    uint64_t best = 0;
+    for (int j = tid; j < n; j += kCtaThreads) {
+      const uint64_t K = comp_key(order_key(r.c[j]), j);
+      if (K < prev && K > best) best = K;
+    }
+    best = warp_max_u64(best);
+    if (lane == 0) s_wmax[wid] = best;
+    __syncthreads();
+    if (wid == 0) {
+      uint64_t v = lane < kCtaThreads / 32 ? s_wmax[lane] : 0ull;
+      v = warp_max_u64(v);
+      if (lane == 0) { s_pick[t] = comp_index(v); s_best = v; }
+    }
+    __syncthreads();
+    prev = s_best;
+  }
+  for (int t = tid; t < m; t += kCtaThreads) {
+    const int jt = s_pick[t];
+    int pos = 0;
+    for (int y = 0; y < m; ++y) pos += s_pick[y] < jt;
+    r.sel[pos] = jt;
+  }
+  if (tid == 0) {
+    r.sel[m] = n;
+    *r.cnt = m + 1;
+  }
+  for (int x = m + 1 + tid; x < a.k; x += kCtaThreads) r.sel[x] = -1;
+}
+
+template <int NPL>
+msa_status launch_warp(const msa_topk_args& a, int64_t rows, cudaStream_t stream) {
+  const int64_t grid = (rows + kWarpsPerCta - 1) / kWarpsPerCta;
+  topk_warp_kernel<NPL><<<static_cast<unsigned>(grid), kWarpsPerCta * 32, 0, stream>>>(a, rows);
+  return MSA_OK;
+}
+
+}  // namespace
+
+msa_status launch_topk(const msa_topk_args& a, cudaStream_t stream) {
+  const int64_t rows = (a.mode == MSA_MODE_PREFILL) ? static_cast<int64_t>(a.B) * a.S * a.Hkv
+                                                    : static_cast<int64_t>(a.B) * a.Hkv;
+  if (rows == 0) return MSA_OK;
+  // the largest candidate count of any row
+  const int64_t maxc = (a.mode == MSA_MODE_PREFILL) ? (a.S - 1) / a.Bk : a.nb_stride;
+  msa_status st = MSA_OK;
+  if (maxc <= 32) st = launch_warp<1>(a, rows, stream);
+  else if (maxc <= 64) st = launch_warp<2>(a, rows, stream);
+  else if (maxc <= 128) st = launch_warp<4>(a, rows, stream);
+  else if (maxc <= 256) st = launch_warp<8>(a, rows, stream);
+  else if (maxc <= 512) st = launch_warp<16>(a, rows, stream);
+  else if (maxc <= 1024) st = launch_warp<32>(a, rows, stream);
+  else if (maxc <= 2048 && a.mode == MSA_MODE_PREFILL) st = launch_warp<64>(a, rows, stream);
+  else topk_cta_kernel<<<static_cast<unsigned>(rows), kCtaThreads, 0, stream>>>(a, rows);
+  if (st != MSA_OK) return st;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "top-k kernel launch");
+  return MSA_OK;
+}
+
+}  // namespace msa

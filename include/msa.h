@@ -1,0 +1,289 @@
+/*
+ * msa.h -- C ABI of the MiniMax Sparse Attention (MSA) layer hot path on one
+ * GB300 (sm_103a).
+ *
+ * MSA runs in two stages.  An Index Branch scores every Bk-token KV block for
+ * each query and KV (GQA) group and keeps k blocks; exact softmax attention
+ * then runs against only those blocks, in causal prefill and in paged decode.
+ * Sources, by page title and passage:
+ *   [serving]  "MiniMax M3 preparado para inferencia en produccion" (community
+ *              post on the M3 serving report), paragraphs "KV-Block-Major",
+ *              "MSA con paged attention" and "MSA opera en dos etapas".
+ *   [agents]   "MiniMax M3: Como la atencion dispersa hace practicos a los
+ *              agentes de largo alcance", MSA paragraph, its figure caption and
+ *              the bullet "Costo predecible a cualquier longitud" (Bk = 128,
+ *              k = 16: 2048 tokens per query and GQA group).
+ *   [M2]       article on the MiniMax M2 report, section "MiniMax Sparse
+ *              Attention (MSA) y escalado subcuadratico entrante" (block
+ *              selection on real, uncompressed KV over a GQA backbone).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument is a DEVICE pointer owned by the caller, unless a
+ *    comment says otherwise.  The library never allocates device memory, never
+ *    synchronises the device or a stream, and keeps no state between calls
+ *    except a per-device cache of kernel attributes.
+ *  - Work is enqueued on `stream` and runs asynchronously.  A call that returns
+ *    MSA_OK has enqueued all of its work; results are ready when the stream is.
+ *  - Arguments are validated on the host first.  On any error nothing is
+ *    enqueued and msa_last_error_string() (thread-local) says why.
+ *  - bf16 tensors are raw 16-bit bfloat16 storage (`void*`); accumulation is
+ *    fp32.  Strides are given in ELEMENTS for every dimension except the
+ *    innermost, which is always contiguous.  Strides of tensors that the
+ *    kernels stage with TMA must be multiples of 16 bytes and their base
+ *    pointers 16-byte aligned; bf16 vectors read with 16-byte loads likewise.
+ *  - `dev_err` (optional, may be NULL) is a caller-owned device int32.  Kernels
+ *    OR MSA_DEVERR_* bits into it when a device-side check fails (a bounded
+ *    wait that ran out, a page id or block index outside its range); they then
+ *    skip the offending work and return without trapping.  The caller clears
+ *    it and reads it back when convenient.
+ *  - Supported shapes: D = 128, dI = 64, Bk = 128, 1 <= HI <= 4,
+ *    1 <= k <= 64, GQA ratio G = Hq / Hkv in 1..8 (Hq a multiple of Hkv).
+ *    Anything else returns MSA_ERR_UNSUPPORTED.
+ */
+#ifndef MSA_H
+#define MSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without pulling in the CUDA headers */
+typedef struct CUstream_st *msa_stream_t;
+
+typedef enum msa_status {
+    MSA_OK = 0,
+    MSA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad stride, ... */
+    MSA_ERR_UNSUPPORTED = 2,   /* a shape outside the supported set above */
+    MSA_ERR_CUDA = 3,          /* a CUDA runtime call failed */
+    MSA_ERR_DEVICE_CHECK = 4,  /* reserved for callers that read dev_err back */
+    MSA_ERR_WORKSPACE = 5      /* workspace pointer or size too small */
+} msa_status;
+
+/* bits OR-ed into *dev_err by the kernels */
+#define MSA_DEVERR_TIMEOUT 0x1   /* a bounded barrier wait ran out */
+#define MSA_DEVERR_BAD_PAGE 0x2  /* a page id outside [0, num_pages) */
+#define MSA_DEVERR_BAD_SEL 0x4   /* a selected block outside the causal range */
+#define MSA_DEVERR_BAD_LEN 0x8   /* seq_len[b] outside [1, max_pages * Bk] or past nb_stride */
+
+typedef enum msa_mode {
+    MSA_MODE_PREFILL = 0,
+    MSA_MODE_DECODE = 1
+} msa_mode;
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int msa_version(void);
+
+/* Human-readable text of the last host-side error of this thread. */
+const char *msa_last_error_string(void);
+
+/* Name of a status code. */
+const char *msa_status_string(msa_status s);
+
+/* --------------------------------------------------------------------------
+ * a1. Index score
+ *
+ * Block relevance scores of the Index Branch ([agents], MSA paragraph and
+ * caption).  The pages never print the formula; this library computes
+ *     s_t = sum_{h < HI} w_h * ReLU(q_idx_h . k_idx_t)        (fp32 accumulate)
+ *     c_j = max over the Bk tokens t of block j of s_t
+ * for every block j strictly before the query's own block, and writes -inf for
+ * the own block and every later entry up to nb_stride.  The own block is always
+ * kept by selection and is never scored.
+ *
+ * PREFILL: query i of sequence b has own block i / Bk and scores blocks of the
+ *   same sequence's index keys.
+ *     q_idx [B, S, Hkv, HI, dI] bf16, strides q_idx_stride = (b, s, g, h)
+ *     w     [B, S, Hkv, HI]     fp32, strides w_stride     = (b, s, g)
+ *     k_idx [B, S, Hkv, dI]     bf16, strides k_idx_stride = (b, s, g)
+ *     C     [B, S, Hkv, nb_stride] fp32, strides C_stride = (b, s, g),
+ *           nb_stride >= ceil(S / Bk)
+ * DECODE: one query per sequence at position L_b - 1 (its own token already in
+ *   the cache); its own block is (L_b - 1) / Bk.  Index keys live in pages of
+ *   Bk tokens: logical block j of sequence b is page seq_pt[b][j].
+ *     q_idx [B, Hkv, HI, dI] bf16, strides (b, g, h, unused)
+ *     w     [B, Hkv, HI]     fp32, strides (b, g, unused)
+ *     k_idx page pool [num_pages, Hkv, Bk, dI] bf16, strides (page, g, t)
+ *     seq_pt [B, max_pages] int32 (row stride max_pages), seq_len [B] int32
+ *     C     [B, Hkv, nb_stride] fp32, strides (b, g, unused);
+ *           nb_stride >= max over b of ceil(L_b / Bk) (entries past the own
+ *           block, up to nb_stride, are written -inf).
+ *   Page ids outside [0, num_pages) are not read: the block gets -inf and
+ *   MSA_DEVERR_BAD_PAGE is raised.  A sequence whose length is outside
+ *   [1, max_pages * Bk], or whose own block is not below nb_stride, is not
+ *   scored (its row stays -inf) and raises MSA_DEVERR_BAD_LEN.
+ * ------------------------------------------------------------------------ */
+typedef struct msa_index_args {
+    msa_mode mode;
+    int B, S, Hkv, HI, dI, Bk;
+    const void *q_idx;
+    int64_t q_idx_stride[4];
+    const float *w;
+    int64_t w_stride[3];
+    const void *k_idx;
+    int64_t k_idx_stride[3];
+    int64_t num_pages;            /* decode */
+    const int32_t *seq_pt;        /* decode */
+    int64_t max_pages;            /* decode */
+    const int32_t *seq_len;       /* decode */
+    float *C;
+    int64_t C_stride[3];
+    int nb_stride;
+    int32_t *dev_err;
+} msa_index_args;
+
+msa_status msa_index_score(const msa_index_args *args, msa_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * a2. Top-k block selection
+ *
+ * Per (query, KV group) row keep the own block and the k-1 best earlier blocks,
+ * ordered by (score descending, block index ascending); when the row has at
+ * most k-1 earlier blocks keep them all ([agents], "Costo predecible": k
+ * blocks including the query's own).  Output is ascending and padded with -1;
+ * the own block, the largest selected index, comes last.
+ *   PREFILL rows (b, s, g): own block s / Bk.   C strides (b, s, g).
+ *     sel [B, S, Hkv, k] int32, count [B, S, Hkv] int32 (dense).
+ *   DECODE rows (b, g): own block (seq_len[b] - 1) / Bk.  C strides (b, g, -).
+ *     sel [B, Hkv, k] int32, count [B, Hkv] int32 (dense).
+ * Scores are compared as fp32 (-0 equals +0); NaN scores rank below -inf.
+ * A decode row whose length is outside [1, nb_stride * Bk] gets count 0, an
+ * all -1 selection and MSA_DEVERR_BAD_LEN.
+ * ------------------------------------------------------------------------ */
+typedef struct msa_topk_args {
+    msa_mode mode;
+    int B, S, Hkv, Bk, k;
+    const float *C;
+    int64_t C_stride[3];
+    int nb_stride;                /* entries per score row (as given to msa_index_score) */
+    const int32_t *seq_len;       /* decode */
+    int32_t *sel;
+    int32_t *count;
+    int32_t *dev_err;
+} msa_topk_args;
+
+msa_status msa_topk_blocks(const msa_topk_args *args, msa_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * a3. Decode page table from the selected blocks
+ *
+ * The KV-group dimension is flattened into the batch so that a fixed-page
+ * attention kernel can serve per-group selections ([serving], "MSA con paged
+ * attention").  Row r = b * Hkv + g:
+ *     pt[r][s]    = seq_pt[b][sel[b][g][s]]  for s < count[b][g], else -1
+ *     n[r]        = count[b][g]
+ *     last_len[r] = valid tokens of the row's last selected page (its own
+ *                   block): seq_len[b] - Bk * ((seq_len[b] - 1) / Bk).
+ * sel [B, Hkv, k], count [B, Hkv], seq_pt [B, max_pages], seq_len [B];
+ * pt [B*Hkv, k], n [B*Hkv], last_len [B*Hkv] (all int32, dense).
+ * A selected index outside [0, own block] yields page -1 and MSA_DEVERR_BAD_SEL.
+ * ------------------------------------------------------------------------ */
+msa_status msa_build_page_table(const int32_t *sel, const int32_t *count,
+                                const int32_t *seq_pt, int64_t max_pages,
+                                const int32_t *seq_len, int B, int Hkv, int k, int Bk,
+                                int32_t *pt, int32_t *n, int32_t *last_len,
+                                int32_t *dev_err, msa_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * a3'-a4-a6. Sparse attention, causal prefill (KV-block-major)
+ *
+ * For every query i, q-head hq (KV group g = hq / G) and selected block j of
+ * (i, g): exact softmax attention over the tokens t of the selected blocks with
+ * t <= i ([M2]).  The kernel iterates over KV blocks in the outer loop: it
+ * inverts the selection into per-(b, g, j) query lists, stages each selected
+ * block's K and V once in shared memory, runs every query that chose it
+ * against it, and combines the per-block partials with a log-sum-exp merge
+ * ([serving], "KV-Block-Major").
+ *     Q [B, S, Hq, D] bf16 strides (b, s, h); K, V [B, S, Hkv, D] bf16 strides
+ *     (b, s, g); sel [B, S, Hkv, k] and count [B, S, Hkv] int32 (dense, as
+ *     written by msa_topk_blocks);
+ *     O [B, S, Hq, D] bf16 (dense), LSE [B, S, Hq] fp32 (dense, natural log,
+ *     softmax_scale included).
+ * Workspace: caller-owned device scratch of ws_bytes.  Queries are processed in
+ * chunks sized to fit; msa_sparse_attn_prefill_workspace_size(args, q) gives
+ * the bytes needed for chunks of q queries (q >= 1); larger workspaces mean
+ * fewer passes.  The workspace must stay untouched until the stream has run
+ * the call.  softmax_scale <= 0 selects 1 / sqrt(D).
+ * ------------------------------------------------------------------------ */
+typedef struct msa_prefill_args {
+    int B, S, Hq, Hkv, D, Bk, k;
+    float softmax_scale;
+    const void *Q;
+    int64_t Q_stride[3];
+    const void *K;
+    int64_t K_stride[3];
+    const void *V;
+    int64_t V_stride[3];
+    const int32_t *sel;
+    const int32_t *count;
+    void *O;
+    float *LSE;
+    int32_t *dev_err;
+} msa_prefill_args;
+
+size_t msa_sparse_attn_prefill_workspace_size(const msa_prefill_args *args, int64_t chunk_queries);
+msa_status msa_sparse_attn_prefill(const msa_prefill_args *args, void *ws, size_t ws_bytes,
+                                   msa_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * a5-a6. Sparse attention, paged decode
+ *
+ * One query token per sequence.  Row r = b * Hkv + g of the flattened page
+ * table (msa_build_page_table) lists the row's selected pages; the G query
+ * heads of group g attend to the first n[r] pages, the last of which holds
+ * last_len[r] valid tokens ([serving], "MSA con paged attention").  Each
+ * (row, page) pair is an independent split of the softmax; the partials go to
+ * the workspace and are combined by the log-sum-exp merge.
+ *     Q [B, Hq, D] bf16 strides (b, h); K_pool, V_pool [num_pages, Hkv, Bk, D]
+ *     bf16 with common strides kv_stride = (page, g, t);
+ *     pt [B*Hkv, k], n [B*Hkv], last_len [B*Hkv] int32;
+ *     O [B, Hq, D] bf16 (dense), LSE [B, Hq] fp32 (dense).
+ * Workspace: msa_sparse_attn_decode_workspace_size(args) bytes (fp32 partial
+ * outputs and LSEs, B*Hq*k*(D+1)*4 bytes).  Page ids outside [0, num_pages)
+ * are skipped (MSA_DEVERR_BAD_PAGE).  softmax_scale <= 0 selects 1/sqrt(D).
+ * ------------------------------------------------------------------------ */
+typedef struct msa_decode_args {
+    int B, Hq, Hkv, D, Bk, k;
+    float softmax_scale;
+    const void *Q;
+    int64_t Q_stride[2];
+    const void *K_pool;
+    const void *V_pool;
+    int64_t kv_stride[3];
+    int64_t num_pages;
+    const int32_t *pt;
+    const int32_t *n;
+    const int32_t *last_len;
+    void *O;
+    float *LSE;
+    int32_t *dev_err;
+} msa_decode_args;
+
+size_t msa_sparse_attn_decode_workspace_size(const msa_decode_args *args);
+msa_status msa_sparse_attn_decode(const msa_decode_args *args, void *ws, size_t ws_bytes,
+                                  msa_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * a6. Log-sum-exp merge of partial softmax results
+ *
+ * Partial outputs over blocks recombined by a final log-sum-exp reduction
+ * ([serving], "KV-Block-Major"):
+ *     LSE[r] = ln sum_p exp(LSE_part[r][p])
+ *     O[r]   = sum_p exp(LSE_part[r][p] - LSE[r]) * O_part[r][p]
+ * Parts with LSE_part = -inf are empty and skipped (their O_part is not read);
+ * a row with no non-empty part gets O = 0 and LSE = -inf.
+ *     O_part [rows, parts, D] fp32, LSE_part [rows, parts] fp32 (dense);
+ *     O [rows, D] bf16 (dense), LSE [rows] fp32 (may be NULL).
+ * D must be a multiple of 4 and at most 512; parts at most 64.
+ * ------------------------------------------------------------------------ */
+msa_status msa_lse_merge(const float *O_part, const float *LSE_part, int64_t rows, int parts,
+                         int D, void *O, float *LSE, int32_t *dev_err, msa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_H */

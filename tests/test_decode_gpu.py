@@ -1,0 +1,174 @@
+"""Decode path (a1 index score -> a2 top-k -> a3 page table -> a5/a6 attention)
+against the fp64 oracle, through the C ABI, on a GB300.
+
+Small cases cover ragged lengths (1 token, partial and full own blocks, fewer
+than k earlier blocks), GQA ratios 1/6/8, HI = 1..4 and k = 1/4/16/64.  The
+full-size cases run the decode step at concurrency 8 over a 60,000-token cached
+prefix, the 1M-token batch-1 step, and the ragged batch of 64 (checked on a
+sample of its sequences, which the oracle computes one by one).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from msa_check import check_attention, check_scores, check_selection
+from workloads import DecodeWorkload, MSAShape, decode_inputs, workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def msa():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from block_sparse_attention_02_gb300 import build as b
+    b.build()
+    import block_sparse_attention_02_gb300 as m
+    return m
+
+
+def run_gpu(msa, inp, k):
+    bufs = msa.decode_step(inp, k)
+    torch.cuda.synchronize()
+    assert int(bufs["dev_err"].item()) == 0, f"device error word {int(bufs['dev_err'].item()):#x}"
+    return {n: t.cpu() for n, t in bufs.items() if n != "ws"}
+
+
+def check_decode(msa, wl, inp_dev, k, seq_subset=None):
+    """Full GPU step, then oracle checks on all (or a subset of) sequences."""
+    sh = wl.shape
+    out = run_gpu(msa, inp_dev, k)
+    small = ("Q", "q_idx", "w", "seq_pt", "seq_len")
+    inp = {n: inp_dev[n].cpu() for n in small}
+    bs = list(range(wl.B)) if seq_subset is None else list(seq_subset)
+    if seq_subset is not None:
+        # compact host copy of the sampled sequences (tensor plumbing, no arithmetic)
+        pages = sorted({int(p) for b in bs for p in inp["seq_pt"][b].tolist() if p >= 0})
+        remap = torch.full((inp_dev["K_pool"].shape[0],), -1, dtype=torch.int32)
+        remap[torch.tensor(pages)] = torch.arange(len(pages), dtype=torch.int32)
+        idx = torch.tensor(pages, device=inp_dev["K_pool"].device)
+        sub = {
+            "Q": inp["Q"][bs], "q_idx": inp["q_idx"][bs], "w": inp["w"][bs],
+            "kidx_pool": inp_dev["kidx_pool"].index_select(0, idx).cpu(),
+            "K_pool": inp_dev["K_pool"].index_select(0, idx).cpu(),
+            "V_pool": inp_dev["V_pool"].index_select(0, idx).cpu(),
+            "seq_len": inp["seq_len"][bs],
+        }
+        spt = inp["seq_pt"][bs].clone()
+        spt[spt >= 0] = remap[spt[spt >= 0].long()]
+        sub["seq_pt"] = spt
+        inp = sub
+    else:
+        for n in ("kidx_pool", "K_pool", "V_pool"):
+            inp[n] = inp_dev[n].cpu()
+    nb_stride = out["C"].shape[-1]
+    C_orc = oracle.decode_scores(inp["q_idx"], inp["w"], inp["kidx_pool"], inp["seq_pt"], inp["seq_len"], nb_stride)
+    C_gpu = out["C"].numpy()[bs]
+    check_scores(C_gpu, C_orc)
+    own = oracle.own_blocks_decode(inp["seq_len"], sh.Bk)
+    own_rows = np.repeat(own, sh.Hkv)
+    sel_gpu = out["sel"].numpy()[bs]
+    cnt_gpu = out["count"].numpy()[bs]
+    exact, tie = check_selection(sel_gpu.reshape(-1, k), cnt_gpu.reshape(-1), C_orc.reshape(-1, nb_stride),
+                                 own_rows, k)
+    # page table: bit-exact against the oracle's construction from the GPU selection
+    pt_o, n_o, ll_o = oracle.page_table(out["sel"].numpy(), out["count"].numpy(), inp_dev["seq_pt"].cpu(),
+                                        inp_dev["seq_len"].cpu(), sh.Bk)
+    assert np.array_equal(out["pt"].numpy(), pt_o)
+    assert np.array_equal(out["n"].numpy(), n_o)
+    assert np.array_equal(out["last_len"].numpy(), ll_o)
+    # attention on the GPU's own selection
+    O_o, LSE_o = oracle.decode_attend(inp["Q"], inp["K_pool"], inp["V_pool"], inp["seq_pt"], inp["seq_len"],
+                                      sel_gpu, cnt_gpu, 1.0 / math.sqrt(sh.D))
+    O_g = out["O"].float().numpy()[bs]
+    L_g = out["LSE"].numpy()[bs]
+    errs = check_attention(O_g, L_g, O_o, LSE_o)
+    return exact, tie, errs
+
+
+SMALL = [
+    DecodeWorkload("edge_lengths", lengths=(1, 2, 127, 128, 129, 255, 256, 257, 1000, 2049, 5000),
+                   shape=MSAShape(), seed=31),
+    DecodeWorkload("gqa1_hi1", lengths=(300, 4100, 777), shape=MSAShape(Hq=8, Hkv=8, HI=1, k=4), seed=32),
+    DecodeWorkload("gqa8_hi3", lengths=(9000, 1, 640), shape=MSAShape(Hq=16, Hkv=2, HI=3, k=16), seed=33),
+    DecodeWorkload("k1", lengths=(3000, 129), shape=MSAShape(Hq=12, Hkv=2, HI=2, k=1), seed=34),
+    DecodeWorkload("k64", lengths=(20000, 8000, 64 * 128 + 5), shape=MSAShape(Hq=24, Hkv=4, k=64), seed=35),
+    DecodeWorkload("unshuffled", lengths=(2500,) * 3, shape=MSAShape(), seed=36, shuffle_pages=False),
+]
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=[w.name for w in SMALL])
+def test_decode_small(msa, wl):
+    inp = decode_inputs(wl, device="cuda")
+    exact, tie, errs = check_decode(msa, wl, inp, wl.shape.k)
+    print(f"{wl.name}: exact rows {exact}, near-tie rows {tie}, O max/mean {errs[0]:.2e}/{errs[1]:.2e}")
+
+
+def test_decode_b8_l60001(msa):
+    wl = workload("decode_b8_l60001")
+    inp = decode_inputs(wl, device="cuda")
+    exact, tie, errs = check_decode(msa, wl, inp, wl.shape.k)
+    assert exact + tie == 64
+    print(f"decode_b8_l60001: exact rows {exact}, near-tie rows {tie}, errs {errs}")
+
+
+def test_decode_b1_l1048576(msa):
+    wl = workload("decode_b1_l1048576")
+    inp = decode_inputs(wl, device="cuda")
+    exact, tie, errs = check_decode(msa, wl, inp, wl.shape.k)
+    print(f"decode_b1_l1048576: exact rows {exact}, near-tie rows {tie}, errs {errs}")
+
+
+def test_decode_ragged_b64_sampled(msa):
+    wl = workload("decode_ragged_b64")
+    inp = decode_inputs(wl, device="cuda")
+    L = np.array(wl.lengths)
+    rng = np.random.default_rng(0)
+    sample = sorted({int(L.argmin()), int(L.argmax())} | set(rng.choice(wl.B, 4, replace=False).tolist()))
+    exact, tie, errs = check_decode(msa, wl, inp, wl.shape.k, seq_subset=sample)
+    print(f"decode_ragged_b64 sample {sample}: exact rows {exact}, near-tie rows {tie}, errs {errs}")
+
+
+def test_decode_is_deterministic(msa):
+    wl = workload("decode_b8_l60001")
+    inp = decode_inputs(wl, device="cuda")
+    a = run_gpu(msa, inp, 16)
+    b = run_gpu(msa, inp, 16)
+    for n in ("C", "sel", "count", "pt", "O", "LSE"):
+        assert torch.equal(a[n], b[n]), n
+
+
+def test_decode_bad_page_is_reported_not_read(msa):
+    """A page id outside the pool is skipped and flagged; nothing faults."""
+    wl = DecodeWorkload("badpage", lengths=(1000, 1000), shape=MSAShape(), seed=37)
+    inp = decode_inputs(wl, device="cuda")
+    inp["seq_pt"][1, 2] = inp["K_pool"].shape[0] + 5
+    bufs = msa.decode_step(inp, 16)
+    torch.cuda.synchronize()
+    assert int(bufs["dev_err"].item()) & msa.MSA_DEVERR_BAD_PAGE
+    C = bufs["C"].cpu()
+    assert torch.isneginf(C[1, :, 2]).all()
+    assert torch.isfinite(bufs["O"].float()).all()
+
+
+def test_standalone_lse_merge(msa):
+    """msa_lse_merge on random partials with empty parts against the oracle merge."""
+    g = torch.Generator(device="cuda").manual_seed(5)
+    rows, parts, D = 1000, 16, 128
+    Op = torch.randn(rows, parts, D, device="cuda", generator=g)
+    Lp = torch.randn(rows, parts, device="cuda", generator=g) * 4
+    Lp[torch.rand(rows, parts, device="cuda", generator=g) < 0.2] = -float("inf")
+    Lp[7] = -float("inf")                       # a row with nothing in it
+    O = torch.empty(rows, D, dtype=torch.bfloat16, device="cuda")
+    L = torch.empty(rows, device="cuda")
+    msa.msa_lse_merge(Op, Lp, O, L)
+    torch.cuda.synchronize()
+    Oo, Lo = oracle.lse_merge(Op.cpu().double().numpy(), Lp.cpu().double().numpy())
+    fin = np.isfinite(Lo)
+    assert np.array_equal(np.isneginf(L.cpu().numpy()), ~fin)
+    np.testing.assert_allclose(O.float().cpu().numpy(), Oo, atol=1e-2, rtol=1e-2)
+    np.testing.assert_allclose(L.cpu().numpy()[fin], Lo[fin], atol=1e-4)
+    assert torch.all(O[7] == 0)
