@@ -1,0 +1,501 @@
+"""Benchmark of the MSA layer hot path on one GB300 (or N replicas).
+
+Default workload: one MSA decode step at concurrency 8 over a 60,000-token
+cached prefix (B = 8, L = 60,001, Hq = 48, Hkv = 8, D = 128, index 4 x 64,
+Bk = 128, k = 16, shuffled 128-token pages).  A step runs the whole hot path:
+index score -> top-k -> page table -> paged sparse attention -> LSE merge.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-cpu-baseline]
+
+Prints one JSON line (rank 0).  ``value`` is decode tokens/s (sequences
+advanced by one token per second, all ranks), timed with CUDA events on the
+launching stream over exactly K steps bracketed by barrier + synchronize; the
+inputs (the 491 MB index-key pool alone) exceed the 129 MB L2, so no flush is
+needed between steps.  ``roofline`` reports the dominant kernel (decode index
+scoring): algorithmic bytes per launch / its mean event-timed duration against
+the measured HBM copy bandwidth.  ``e2e`` repeats the step through the same C
+ABI with the step's inputs copied from pinned host memory and its output read
+back inside the timed region.  ``cpu_baseline`` times the fp64 oracle on a
+bounded sample of the same workload on the host cores.
+
+``--impl reference`` times the oracle itself (the only reference this method
+has: the pages ship no code) on the same workload and prints the same line
+with "impl": "reference".  Under torchrun only rank 0 runs it.
+
+``--workload prefill_s131072`` times one prefill layer instead (tokens/s =
+B*S per layer), with the tensor-core roofline of the sparse attention.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MSA layer prefill & decode tokens/s on 1 GB300; % of HBM / bf16 TC roofline"
+UNIT = "tokens/s"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def read_profile_traffic(name: str, kernel_files):
+    """dram bytes per launch from a committed ncu summary, if it matches the current kernel source."""
+    p = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(p):
+        return None, "no profile"
+    kv = {}
+    for line in open(p):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("source_sha256_16") != source_hash(kernel_files):
+        return None, "kernel changed since the capture"
+    try:
+        return float(kv["dram_bytes_per_launch"]), p
+    except (KeyError, ValueError):
+        return None, "no dram bytes in profile"
+
+
+# ---------------------------------------------------------------------------
+# decode workload
+# ---------------------------------------------------------------------------
+
+DECODE_INDEX_FILES = ["block_sparse_attention_02_gb300/csrc/index_decode.cu",
+                      "block_sparse_attention_02_gb300/csrc/msa_ptx.cuh"]
+
+
+def decode_algorithmic_bytes(wl):
+    """Algorithmic HBM bytes of one decode step (unmasked, selected work only)."""
+    sh = wl.shape
+    idx = 0
+    kv = 0
+    for L in wl.lengths:
+        own = (L - 1) // sh.Bk
+        idx += sh.Hkv * own * sh.Bk * sh.dI * 2                  # k_idx of every scored block
+        nsel = min(own, sh.k - 1)
+        kv += sh.Hkv * (nsel * sh.Bk + (L - own * sh.Bk)) * sh.D * 2 * 2   # selected K and V tokens
+    small_idx = wl.B * sh.Hkv * (sh.HI * sh.dI * 2 + sh.HI * 4) + wl.B * sh.Hkv * max(
+        (L + sh.Bk - 1) // sh.Bk for L in wl.lengths) * 4          # q_idx, w, C
+    q_o = wl.B * sh.Hq * sh.D * 2 * 2                              # Q read, O written
+    return {"index_kernel": idx + small_idx, "step": idx + small_idx + kv + q_o}
+
+
+def run_decode_ours(args, wl, world, rank):
+    import torch
+    import block_sparse_attention_02_gb300 as msa
+    from workloads import decode_inputs
+    sh = wl.shape
+    inp = decode_inputs(wl, device="cuda")
+    bufs = msa.decode_buffers(wl.B, sh.Hq, sh.Hkv, sh.k, inp["seq_pt"].shape[1], "cuda")
+    stream = torch.cuda.current_stream()
+
+    def index_part():
+        msa.msa_index_score(msa.MSA_MODE_DECODE, inp["q_idx"], inp["w"], inp["kidx_pool"], bufs["C"],
+                            seq_pt=inp["seq_pt"], seq_len=inp["seq_len"], dev_err=bufs["dev_err"])
+
+    def rest_part():
+        e = bufs["dev_err"]
+        msa.msa_topk_blocks(msa.MSA_MODE_DECODE, bufs["C"], sh.k, bufs["sel"], bufs["count"],
+                            seq_len=inp["seq_len"], dev_err=e)
+        msa.msa_build_page_table(bufs["sel"], bufs["count"], inp["seq_pt"], inp["seq_len"], bufs["pt"], bufs["n"],
+                                 bufs["last_len"], dev_err=e)
+        msa.msa_sparse_attn_decode(inp["Q"], inp["K_pool"], inp["V_pool"], bufs["pt"], bufs["n"], bufs["last_len"],
+                                   bufs["O"], bufs["LSE"], bufs["ws"], dev_err=e)
+
+    # warm up eagerly (sets kernel attributes), then capture each part in a CUDA graph
+    for _ in range(max(1, args.warmup)):
+        index_part()
+        rest_part()
+    torch.cuda.synchronize()
+    graphs = True
+    try:
+        g_idx, g_rest = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_idx):
+            index_part()
+        with torch.cuda.graph(g_rest):
+            rest_part()
+        run_idx, run_rest = g_idx.replay, g_rest.replay
+    except Exception:  # capture unavailable: launch directly
+        graphs = False
+        run_idx, run_rest = index_part, rest_part
+    for _ in range(args.warmup):
+        run_idx()
+        run_rest()
+    torch.cuda.synchronize()
+    assert int(bufs["dev_err"].item()) == 0, "device error during warm-up"
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        run_idx()
+        ev[i][1].record(stream)
+        run_rest()
+        ev[i][2].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    total_ms = max_over_ranks(start.elapsed_time(end), world)
+    idx_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    rest_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    assert int(bufs["dev_err"].item()) == 0, "device error during the timed steps"
+
+    # ---- end to end through the C ABI with host buffers ----
+    small = ("Q", "q_idx", "w", "seq_pt", "seq_len")
+    host_in = {n: inp[n].cpu().pin_memory() for n in small}
+    host_out = {"O": torch.empty_like(bufs["O"], device="cpu").pin_memory(),
+                "LSE": torch.empty_like(bufs["LSE"], device="cpu").pin_memory()}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def e2e_step():
+        for n in small:
+            inp[n].copy_(host_in[n], non_blocking=True)
+        run_idx()
+        run_rest()
+        host_out["O"].copy_(bufs["O"], non_blocking=True)
+        host_out["LSE"].copy_(bufs["LSE"], non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record(stream)
+    for _ in range(K):
+        e2e_step()
+    e2.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(s2.elapsed_time(e2), world)
+
+    peaks = load_peaks()
+    alg = decode_algorithmic_bytes(wl)
+    achieved = alg["index_kernel"] / (idx_ms * 1e-3) / 1e9
+    traffic, traffic_src = read_profile_traffic("index_decode_b8_l60001.txt", DECODE_INDEX_FILES)
+    tokens_per_step = wl.B * world
+    step_ms = total_ms / K
+    res = {
+        "metric": METRIC, "value": tokens_per_step / (step_ms * 1e-3), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "batch": wl.B, "context": wl.lengths[0], "Hq": wl.shape.Hq,
+                   "Hkv": wl.shape.Hkv, "D": wl.shape.D, "HI": wl.shape.HI, "dI": wl.shape.dI, "Bk": wl.shape.Bk,
+                   "k": wl.shape.k, "pages": "128-token, shuffled", "cuda_graphs": graphs,
+                   "l2": "no flush: inputs larger than L2 (491 MB k_idx pool read per step)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "index_decode_kernel", "achieved": achieved,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "peak_src": peaks["src"], "traffic": traffic, "traffic_src": traffic_src,
+                     "algorithmic_bytes_per_launch": alg["index_kernel"], "launch_ms": idx_ms,
+                     "step_algorithmic_bytes": alg["step"],
+                     "step_frac": alg["step"] / (step_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+        "breakdown_ms": {"index_score": idx_ms, "topk+page_table+attention+merge": rest_ms},
+        "e2e": {"value": tokens_per_step / (e2e_ms / K * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 5 * K,
+        "clocks": clocks,
+    }
+    return res, host_in, inp
+
+
+def oracle_decode_step(h, sh):
+    import oracle
+    C = oracle.decode_scores(h["q_idx"], h["w"], h["kidx_pool"], h["seq_pt"], h["seq_len"])
+    own = oracle.own_blocks_decode(h["seq_len"], sh.Bk)
+    sel, cnt, _, _ = oracle.select(C, own[:, None], sh.k)
+    return oracle.decode_attend(h["Q"], h["K_pool"], h["V_pool"], h["seq_pt"], h["seq_len"], sel, cnt,
+                                1.0 / math.sqrt(sh.D))
+
+
+def cpu_decode_baseline(wl, inp_host, budget_s: float, min_steps: int = 1):
+    """Oracle decode steps on the host cores until the time budget is used."""
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    steps = 0
+    while steps < min_steps or time.perf_counter() - t0 < budget_s:
+        oracle_decode_step(inp_host, wl.shape)
+        steps += 1
+    dt = time.perf_counter() - t0
+    return {"value": wl.B * steps / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{steps} full decode step(s) of {wl.name} (B={wl.B}) in {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------------------
+# prefill workload (optional)
+# ---------------------------------------------------------------------------
+
+def prefill_attention_flops(sel, count, S, Bk, G, D):
+    """4*D*G FLOPs per (query, group, key) over the unmasked selected keys (count from the selection)."""
+    import torch
+    i = torch.arange(S, device=sel.device).view(1, S, 1, 1)
+    s = sel.long()
+    keys = torch.where(s < 0, torch.zeros_like(s),
+                       torch.clamp(i + 1 - s * Bk, min=0, max=Bk))
+    return float(keys.sum().item()) * 4 * D * G
+
+
+def run_prefill_ours(args, wl, world, rank):
+    import torch
+    import block_sparse_attention_02_gb300 as msa
+    from workloads import prefill_inputs
+    sh = wl.shape
+    inp = prefill_inputs(wl, device="cuda")
+    ws_q = min(wl.S, args.prefill_chunk) * wl.B
+    sel_probe = torch.empty(1, 1, 1, sh.k, dtype=torch.int32)
+    ws_bytes = msa.msa_sparse_attn_prefill_workspace_size(inp["Q"], inp["K"], sel_probe, ws_q)
+    bufs = msa.prefill_buffers(wl.B, wl.S, sh.Hq, sh.Hkv, sh.k, "cuda", ws_bytes)
+    stream = torch.cuda.current_stream()
+    e = bufs["dev_err"]
+
+    def parts():
+        return [
+            lambda: msa.msa_index_score(msa.MSA_MODE_PREFILL, inp["q_idx"], inp["w"], inp["k_idx"], bufs["C"],
+                                        dev_err=e),
+            lambda: msa.msa_topk_blocks(msa.MSA_MODE_PREFILL, bufs["C"], sh.k, bufs["sel"], bufs["count"], dev_err=e),
+            lambda: msa.msa_sparse_attn_prefill(inp["Q"], inp["K"], inp["V"], bufs["sel"], bufs["count"], bufs["O"],
+                                                bufs["LSE"], bufs["ws"], dev_err=e),
+        ]
+    fns = parts()
+    for _ in range(max(1, args.warmup)):
+        for f in fns:
+            f()
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(K):
+        for j, f in enumerate(fns):
+            ev[i][j].record(stream)
+            f()
+        ev[i][3].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    total_ms = max_over_ranks(start.elapsed_time(end), world)
+    part_ms = [statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)) for j in range(3)]
+    flops = prefill_attention_flops(bufs["sel"], bufs["count"], wl.S, sh.Bk, sh.G, sh.D)
+    idx_flops = 2.0 * sh.HI * sh.dI * sh.Hkv * wl.B * sum(sh.Bk * (i // sh.Bk) for i in range(wl.S))
+    peaks = load_peaks()
+    tc = flops / (part_ms[2] * 1e-3) / 1e12
+    step_ms = total_ms / K
+    res = {
+        "metric": METRIC, "value": wl.B * wl.S * world / (step_ms * 1e-3), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "batch": wl.B, "seq_len": wl.S, "Hq": sh.Hq, "Hkv": sh.Hkv, "D": sh.D,
+                   "HI": sh.HI, "dI": sh.dI, "Bk": sh.Bk, "k": sh.k, "query_chunk": ws_q,
+                   "l2": "no flush: inputs larger than L2", "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "kernel": "sparse attention (a4+a6)", "achieved": tc,
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": tc / peaks["bf16_tflops"],
+                     "peak_src": peaks["src"], "traffic": None, "algorithmic_flops_per_launch": flops,
+                     "launch_ms": part_ms[2],
+                     "index_tflops": idx_flops / (part_ms[0] * 1e-3) / 1e12,
+                     "index_frac": idx_flops / (part_ms[0] * 1e-3) / 1e12 / peaks["bf16_tflops"]},
+        "breakdown_ms": {"index_score": part_ms[0], "topk": part_ms[1], "sparse_attention": part_ms[2]},
+        "gpu_launches": None,
+        "clocks": clocks,
+    }
+    return res, None, inp
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode_b8_l60001")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--prefill-chunk", type=int, default=16384)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    import torch
+    from workloads import workload
+    wl = workload(args.workload)
+    world, rank, _ = dist_setup()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        if not hasattr(wl, "lengths"):
+            print(json.dumps({"impl": "reference", "unavailable": "reference arm implemented for decode workloads"}))
+            return
+        from workloads import decode_inputs
+        h = decode_inputs(wl, device="cpu")
+        import oracle
+        oracle.build()
+        for _ in range(args.warmup):
+            oracle_decode_step(h, wl.shape)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            oracle_decode_step(h, wl.shape)
+        dt = time.perf_counter() - t0
+        val = wl.B * args.steps / dt
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "batch": wl.B, "context": wl.lengths[0]},
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": f"{args.steps} full decode steps of {wl.name}"},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }))
+        return
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device for --impl ours")
+    from block_sparse_attention_02_gb300 import build as b
+    b.build()
+    if hasattr(wl, "lengths"):
+        res, host_in, inp = run_decode_ours(args, wl, world, rank)
+    else:
+        res, host_in, inp = run_prefill_ours(args, wl, world, rank)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and hasattr(wl, "lengths"):
+        h = {n: t.cpu() for n, t in inp.items()}
+        res["cpu_baseline"] = cpu_decode_baseline(wl, h, args.cpu_budget_s)
+    elif rank == 0:
+        res["cpu_baseline"] = None
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

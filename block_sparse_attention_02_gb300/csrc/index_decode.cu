@@ -95,7 +95,7 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
   __shared__ __align__(8) uint64_t bar_qdone[2], bar_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ float s_red[kRedBufs][4];
+  __shared__ uint32_t s_red[kRedBufs][4];
   __shared__ int s_cnt[kRedBufs];
   __shared__ int s_chunk[kThreads];
 
@@ -252,11 +252,22 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
     const int q = warp & 3;                       // TMEM lane quarter of this warp
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     Walker it;
-    if (count > 0) walk_init(it, lo, s_pre, s_own, p.B, p.Hkv);
+    int64_t page_cur = 0;
+    if (count > 0) {
+      walk_init(it, lo, s_pre, s_own, p.B, p.Hkv);
+      page_cur = p.seq_pt[it.b * p.max_pages + it.j];
+    }
     int cur_b = -1, cur_g = -1;
     float wv[kMaxHI] = {0.f, 0.f, 0.f, 0.f};
     for (int n = 0; n < count; ++n) {
       const int slot = n % kSlots;
+      // the next item's page id is loaded one item ahead, off the critical path
+      Walker nxt = it;
+      int64_t page_next = 0;
+      if (n + 1 < count) {
+        walk_next(nxt, s_own, p.B, p.Hkv);
+        page_next = p.seq_pt[nxt.b * p.max_pages + nxt.j];
+      }
       if (it.b != cur_b || it.g != cur_g) {
         for (int h = 0; h < kMaxHI; ++h) wv[h] = h < p.HI ? p.w[it.b * p.ws0 + it.g * p.ws1 + h] : 0.f;
         cur_b = it.b;
@@ -273,27 +284,28 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
       float s = 0.f;
 #pragma unroll
       for (int h = 0; h < kMaxHI; ++h) s = fmaf(wv[h], fmaxf(__uint_as_float(v[h]), 0.f), s);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s = fmaxf(s, __shfl_xor_sync(0xffffffffu, s, o));
+      // warp max in one step on order-preserving integer keys
+      const uint32_t wmax = redux_max_u32(float_order_key(s));
       // cross-warp max without a barrier: the last of the four warps to arrive
       // combines the partial maxima and stores the block score.
       if (lane == 0) {
         const int rb = n % kRedBufs;
-        s_red[rb][q] = s;
+        s_red[rb][q] = wmax;
         __threadfence_block();
         if (atomicAdd(&s_cnt[rb], 1) == 3) {
           __threadfence_block();
-          float m = fmaxf(fmaxf(s_red[rb][0], s_red[rb][1]), fmaxf(s_red[rb][2], s_red[rb][3]));
+          const uint32_t mk = max(max(s_red[rb][0], s_red[rb][1]), max(s_red[rb][2], s_red[rb][3]));
           s_cnt[rb] = 0;
-          const int64_t page = p.seq_pt[it.b * p.max_pages + it.j];
-          if (page < 0 || page >= p.num_pages) {
+          float m = float_from_order_key(mk);
+          if (page_cur < 0 || page_cur >= p.num_pages) {
             m = -INFINITY;
             report(p.dev_err, MSA_DEVERR_BAD_PAGE);
           }
           p.C[it.b * p.cs0 + it.g * p.cs1 + it.j] = m;
         }
       }
-      walk_next(it, s_own, p.B, p.Hkv);
+      it = nxt;
+      page_cur = page_next;
     }
   }
 
