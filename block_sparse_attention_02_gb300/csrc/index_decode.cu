@@ -273,7 +273,8 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
         cur_b = it.b;
         cur_g = it.g;
       }
-      if (!mbar_wait(&bar_tfull[slot], (n / kSlots) & 1, abort_flag, p.dev_err)) break;
+      // the warp decides together: the TMEM load below is warp-collective
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar_tfull[slot], (n / kSlots) & 1, abort_flag, p.dev_err))) break;
       tc_fence_after();
       uint32_t v[4];
       tmem_ld4(tmem + lane_addr + slot * kSlotCols, v);
