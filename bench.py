@@ -440,6 +440,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--prefill-chunk", type=int, default=16384)
+    ap.add_argument("--seq", type=int, default=None, help="override the prefill sequence length (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -447,6 +448,9 @@ def main():
     import torch
     from workloads import workload
     wl = workload(args.workload)
+    if args.seq is not None and hasattr(wl, "S"):
+        from dataclasses import replace
+        wl = replace(wl, name=f"{wl.name}_s{args.seq}", S=args.seq)
     world, rank, _ = dist_setup()
 
     if args.impl == "reference":

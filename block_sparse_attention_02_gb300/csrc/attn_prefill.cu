@@ -83,7 +83,7 @@ __global__ void csr_count_kernel(const CsrParams p) {
 
 // single CTA: exclusive scans of counts and of tiles per item
 __global__ void __launch_bounds__(1024) csr_scan_kernel(const CsrParams p, int64_t n_items) {
-  __shared__ int64_t s_sum[1024][2];
+  __shared__ int64_t s_sum[32][2];
   const int tid = threadIdx.x;
   const int64_t per = (n_items + 1023) / 1024;
   const int64_t i0 = tid * per, i1 = min(n_items, i0 + per);
@@ -93,24 +93,35 @@ __global__ void __launch_bounds__(1024) csr_scan_kernel(const CsrParams p, int64
     c += v;
     t += (static_cast<int64_t>(v) * p.G + 127) / 128;
   }
-  s_sum[tid][0] = c;
-  s_sum[tid][1] = t;
+  // inclusive warp scans, then a scan of the 32 warp totals
+  const int lane = tid & 31, wid = tid >> 5;
+  int64_t ic = c, it = t;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t xc = __shfl_up_sync(0xffffffffu, ic, o);
+    const int64_t xt = __shfl_up_sync(0xffffffffu, it, o);
+    if (lane >= o) { ic += xc; it += xt; }
+  }
+  if (lane == 31) { s_sum[wid][0] = ic; s_sum[wid][1] = it; }
   __syncthreads();
-  if (tid == 0) {
-    int64_t rc = 0, rt = 0;
-    for (int x = 0; x < 1024; ++x) {
-      const int64_t a = s_sum[x][0], b = s_sum[x][1];
-      s_sum[x][0] = rc;
-      s_sum[x][1] = rt;
-      rc += a;
-      rt += b;
+  if (wid == 0) {
+    int64_t wc = s_sum[lane][0], wt = s_sum[lane][1];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t xc = __shfl_up_sync(0xffffffffu, wc, o);
+      const int64_t xt = __shfl_up_sync(0xffffffffu, wt, o);
+      if (lane >= o) { wc += xc; wt += xt; }
     }
-    p.off[n_items] = static_cast<int32_t>(rc);
-    p.tile_off[n_items] = static_cast<int32_t>(rt);
+    s_sum[lane][0] = wc;   // inclusive over warps
+    s_sum[lane][1] = wt;
+    if (lane == 31) {
+      p.off[n_items] = static_cast<int32_t>(wc);
+      p.tile_off[n_items] = static_cast<int32_t>(wt);
+    }
   }
   __syncthreads();
-  c = s_sum[tid][0];
-  t = s_sum[tid][1];
+  c = ic - c + (wid > 0 ? s_sum[wid - 1][0] : 0);   // exclusive prefix of this thread
+  t = it - t + (wid > 0 ? s_sum[wid - 1][1] : 0);
   for (int64_t x = i0; x < i1; ++x) {
     const int v = p.cnt[x];
     p.off[x] = static_cast<int32_t>(c);
@@ -154,7 +165,7 @@ struct AttnParams {
   const int32_t* off;
   const int32_t* tile_off;
   const int32_t* list;
-  float* o_part;
+  __nv_bfloat16* o_part;
   float* lse_part;
   int32_t* dev_err;
 };
@@ -233,9 +244,11 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     int64_t prev_item = -1;
     int kvn = 0, last_kv = -1;   // last K/V load issued by this group's leader
     bool ok = true;
+    // tiles of this CTA are contiguous: walk their items forward instead of searching
+    int64_t item = ntiles > 0 ? find_item(p, t0) : 0;
     for (int n = 0; n < ntiles; ++n) {
       const int64_t t = t0 + n;
-      const int64_t item = find_item(p, t);
+      while (p.tile_off[item + 1] <= t) ++item;
       const bool kv_new = item != prev_item;
       prev_item = item;
       if (kv_new) ++kvn;
@@ -250,7 +263,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       const int nrows = min(128, rows_item - row0);
       const int kvb = (kvn - 1) & 1;
       if (leader) {
-        const bool release = (n + 1 == ntiles) || find_item(p, t + 1) != item;
+        const bool release = (n + 1 == ntiles) || p.tile_off[item + 1] <= t + 1;
         ok = mbar_wait(&bar_qempty[st], ((n >> 1) & 1) ^ 1, abort_flag, p.dev_err);
         if (ok && kv_new) {
           ok = mbar_wait(&bar_kvempty[kvb], (((kvn - 1) >> 1) & 1) ^ 1, abort_flag, p.dev_err);
@@ -432,7 +445,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       if (s_fail) break;
       tc_fence_after();
       const float inv = 1.0f / l;
-      float* orow = p.o_part + ((static_cast<int64_t>(qi) * p.Hq + hq) * p.k + slot_sel) * kD;
+      __nv_bfloat16* orow = p.o_part + ((static_cast<int64_t>(qi) * p.Hq + hq) * p.k + slot_sel) * kD;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t v[32];
@@ -440,10 +453,16 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         tmem_ld_wait();
         if (valid) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(orow + cc * 32 + e) =
-                make_float4(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv,
-                            __uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
+          for (int e = 0; e < 32; e += 8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[e + 2 * x]) * inv,
+                                                        __uint_as_float(v[e + 2 * x + 1]) * inv);
+              w[x] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+            *reinterpret_cast<uint4*>(orow + cc * 32 + e) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
         }
       }
       if (valid) p.lse_part[(static_cast<int64_t>(qi) * p.Hq + hq) * p.k + slot_sel] = (m + log2f(l)) * kLn2;
@@ -476,7 +495,7 @@ WsLayout ws_layout(const msa_prefill_args& a, int64_t cq) {
   L.off = o; o = al(o + (n_items + 1) * 4);
   L.tile_off = o; o = al(o + (n_items + 1) * 4);
   L.list = o; o = al(o + static_cast<size_t>(cq) * a.Hkv * a.k * 4);
-  L.o_part = o; o = al(o + static_cast<size_t>(cq) * a.Hq * a.k * kD * 4);
+  L.o_part = o; o = al(o + static_cast<size_t>(cq) * a.Hq * a.k * kD * 2);   // bf16 partials
   L.lse_part = o; o = al(o + static_cast<size_t>(cq) * a.Hq * a.k * 4);
   L.total = o + 256;
   return L;
@@ -562,15 +581,15 @@ msa_status launch_attn_prefill(const msa_prefill_args& a, void* ws, size_t ws_by
     p.Q = static_cast<const __nv_bfloat16*>(a.Q);
     p.qs0 = a.Q_stride[0]; p.qs1 = a.Q_stride[1]; p.qs2 = a.Q_stride[2];
     p.off = c.off; p.tile_off = c.tile_off; p.list = c.list;
-    p.o_part = reinterpret_cast<float*>(w + L.o_part);
+    p.o_part = reinterpret_cast<__nv_bfloat16*>(w + L.o_part);
     p.lse_part = c.lse_part;
     p.dev_err = a.dev_err;
     attn_prefill_kernel<<<dev.num_sms, kAttnThreads, smem, stream>>>(kmap, vmap, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
-    msa_status st = launch_lse_merge(p.o_part, p.lse_part, static_cast<int64_t>(nq) * a.Hq, a.k, kD,
-                                     static_cast<__nv_bfloat16*>(a.O) + q0 * a.Hq * kD,
-                                     a.LSE != nullptr ? a.LSE + q0 * a.Hq : nullptr, a.dev_err, stream);
+    msa_status st = launch_lse_merge_bf16(p.o_part, p.lse_part, static_cast<int64_t>(nq) * a.Hq, a.k, kD,
+                                          static_cast<__nv_bfloat16*>(a.O) + q0 * a.Hq * kD,
+                                          a.LSE != nullptr ? a.LSE + q0 * a.Hq : nullptr, stream);
     if (st != MSA_OK) return st;
   }
   return MSA_OK;

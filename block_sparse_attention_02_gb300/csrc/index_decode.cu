@@ -25,10 +25,10 @@
 namespace msa {
 namespace {
 
-constexpr int kStages = 8;
-constexpr int kSlots = 8;
+constexpr int kStages = 12;
+constexpr int kSlots = 16;
 constexpr int kSlotCols = 16;
-constexpr int kTmemCols = 128;
+constexpr int kTmemCols = 256;
 constexpr int kStageBytes = kBk * kDI * 2;   // 16 KiB
 constexpr int kQTileBytes = 16 * kDI * 2;    // 2 KiB: 16 rows (HI used) x 64
 constexpr int kThreads = 192;

@@ -240,16 +240,19 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
               uint64_t acc[16];
 #pragma unroll
               for (int e = 0; e < 16; ++e) acc[e] = 0ull;
+              // issue the loads of every head, then wait once
+              uint32_t v[kMaxHI][32];
+#pragma unroll
+              for (int h = 0; h < kMaxHI; ++h)
+                if (h < p.HI) tmem_ld32(base + h * 64 + cc * 32, v[h]);
+              tmem_ld_wait();
 #pragma unroll
               for (int h = 0; h < kMaxHI; ++h) {
                 if (h < p.HI) {
-                  uint32_t v[32];
-                  tmem_ld32(base + h * 64 + cc * 32, v);
-                  tmem_ld_wait();
 #pragma unroll
                   for (int e = 0; e < 16; ++e) {
-                    const uint64_t rl = pack2(fmaxf(__uint_as_float(v[2 * e]), 0.f),
-                                              fmaxf(__uint_as_float(v[2 * e + 1]), 0.f));
+                    const uint64_t rl = pack2(fmaxf(__uint_as_float(v[h][2 * e]), 0.f),
+                                              fmaxf(__uint_as_float(v[h][2 * e + 1]), 0.f));
                     acc[e] = fma2(w2[h], rl, acc[e]);
                   }
                 }

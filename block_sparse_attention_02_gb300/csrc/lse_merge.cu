@@ -14,8 +14,18 @@ namespace {
 
 constexpr int kWarps = 8;
 
+__device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// Partials are fp32 (public entry point, decode) or bf16 (prefill workspace).
+template <typename TP>
 __global__ void __launch_bounds__(kWarps * 32)
-lse_merge_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part, int64_t rows, int parts, int D,
+lse_merge_kernel(const TP* __restrict__ o_part, const float* __restrict__ lse_part, int64_t rows, int parts, int D,
                  __nv_bfloat16* __restrict__ O, float* __restrict__ LSE) {
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
@@ -40,14 +50,14 @@ lse_merge_kernel(const float* __restrict__ o_part, const float* __restrict__ lse
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
   const float lse = m + __logf(sum);
   const float inv = 1.0f / sum;
-  const float* op = o_part + row * static_cast<int64_t>(parts) * D;
+  const TP* op = o_part + row * static_cast<int64_t>(parts) * D;
   for (int c = lane * 4; c < D; c += 128) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int pi = 0; pi < parts; ++pi) {
       const float lpi = __shfl_sync(0xffffffffu, pi < 32 ? l0 : l1, pi & 31);
       if (lpi == -INFINITY) continue;
       const float wgt = __expf(lpi - m) * inv;
-      const float4 v = *reinterpret_cast<const float4*>(op + static_cast<int64_t>(pi) * D + c);
+      const float4 v = load4(op + static_cast<int64_t>(pi) * D + c);
       acc.x = fmaf(wgt, v.x, acc.x);
       acc.y = fmaf(wgt, v.y, acc.y);
       acc.z = fmaf(wgt, v.z, acc.z);
@@ -70,10 +80,21 @@ msa_status launch_lse_merge(const float* o_part, const float* lse_part, int64_t 
   (void)dev_err;
   if (rows == 0) return MSA_OK;
   const int64_t grid = (rows + kWarps - 1) / kWarps;
-  lse_merge_kernel<<<static_cast<unsigned>(grid), kWarps * 32, 0, stream>>>(
+  lse_merge_kernel<float><<<static_cast<unsigned>(grid), kWarps * 32, 0, stream>>>(
       o_part, lse_part, rows, parts, D, static_cast<__nv_bfloat16*>(O), LSE);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "lse_merge_kernel launch");
+  return MSA_OK;
+}
+
+msa_status launch_lse_merge_bf16(const __nv_bfloat16* o_part, const float* lse_part, int64_t rows, int parts, int D,
+                                 __nv_bfloat16* O, float* LSE, cudaStream_t stream) {
+  if (rows == 0) return MSA_OK;
+  const int64_t grid = (rows + kWarps - 1) / kWarps;
+  lse_merge_kernel<__nv_bfloat16><<<static_cast<unsigned>(grid), kWarps * 32, 0, stream>>>(o_part, lse_part, rows,
+                                                                                          parts, D, O, LSE);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "lse_merge_kernel<bf16> launch");
   return MSA_OK;
 }
 

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -41,6 +42,8 @@ msa_status launch_page_table(const int32_t* sel, const int32_t* count, const int
 msa_status launch_attn_decode(const msa_decode_args& a, float* o_part, float* lse_part, cudaStream_t stream);
 msa_status launch_lse_merge(const float* o_part, const float* lse_part, int64_t rows, int parts, int D,
                             void* O, float* LSE, int32_t* dev_err, cudaStream_t stream);
+msa_status launch_lse_merge_bf16(const __nv_bfloat16* o_part, const float* lse_part, int64_t rows, int parts, int D,
+                                 __nv_bfloat16* O, float* LSE, cudaStream_t stream);
 msa_status launch_attn_prefill(const msa_prefill_args& a, void* ws, size_t ws_bytes, cudaStream_t stream);
 size_t attn_prefill_workspace_size(const msa_prefill_args& a, int64_t chunk_queries);
 
