@@ -23,7 +23,7 @@ from ._abi import (MSA_DEVERR_BAD_LEN, MSA_DEVERR_BAD_PAGE, MSA_DEVERR_BAD_SEL, 
 
 __all__ = [
     "msa_index_score", "msa_topk_blocks", "msa_build_page_table", "msa_sparse_attn_prefill",
-    "msa_sparse_attn_decode", "msa_lse_merge", "msa_sparse_attn_prefill_workspace_size",
+    "msa_sparse_attn_decode", "msa_sparse_attn_decode_noalloc", "msa_lse_merge", "msa_sparse_attn_prefill_workspace_size",
     "msa_sparse_attn_decode_workspace_size", "decode_step", "prefill_layer", "lib", "MSAError",
     "MSA_MODE_PREFILL", "MSA_MODE_DECODE", "MSA_DEVERR_TIMEOUT", "MSA_DEVERR_BAD_PAGE",
     "MSA_DEVERR_BAD_SEL", "MSA_DEVERR_BAD_LEN", "Bk", "D", "dI",
@@ -223,6 +223,17 @@ def msa_sparse_attn_decode(Q, K_pool, V_pool, pt, n, last_len, O, LSE, ws: torch
     a = _decode_args(Q, K_pool, V_pool, pt, n, last_len, O, LSE, softmax_scale, dev_err)
     _abi.check(lib().msa_sparse_attn_decode(C.byref(a), _ptr(ws), ws.numel() * ws.element_size(),
                                             _stream(stream)), "msa_sparse_attn_decode")
+
+
+def msa_sparse_attn_decode_noalloc(Q, K_pool, V_pool, pt, n, last_len, O, LSE, *, softmax_scale: float = 0.0,
+                                   dev_err=None, stream=None) -> None:
+    """Same as msa_sparse_attn_decode, for callers that cannot allocate: the
+    scratch is the library's built-in device array (see msa.h).  Calls that
+    overlap on the GPU share that array and must be serialised."""
+    if not (pt.is_contiguous() and n.is_contiguous() and last_len.is_contiguous() and O.is_contiguous()):
+        raise ValueError("pt, n, last_len and O must be contiguous")
+    a = _decode_args(Q, K_pool, V_pool, pt, n, last_len, O, LSE, softmax_scale, dev_err)
+    _abi.check(lib().msa_sparse_attn_decode_noalloc(C.byref(a), _stream(stream)), "msa_sparse_attn_decode_noalloc")
 
 
 def msa_lse_merge(O_part: torch.Tensor, LSE_part: torch.Tensor, O: torch.Tensor, LSE: Optional[torch.Tensor] = None,

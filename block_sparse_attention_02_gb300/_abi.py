@@ -87,6 +87,7 @@ SIGNATURES = {
     "msa_sparse_attn_prefill": (C.c_int, [C.POINTER(PrefillArgs), _p, C.c_size_t, _p]),
     "msa_sparse_attn_decode_workspace_size": (C.c_size_t, [C.POINTER(DecodeArgs)]),
     "msa_sparse_attn_decode": (C.c_int, [C.POINTER(DecodeArgs), _p, C.c_size_t, _p]),
+    "msa_sparse_attn_decode_noalloc": (C.c_int, [C.POINTER(DecodeArgs), _p]),
     "msa_lse_merge": (C.c_int, [_p, _p, C.c_int64, C.c_int, C.c_int, _p, _p, _p, _p]),
 }
 

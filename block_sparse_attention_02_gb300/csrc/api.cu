@@ -123,6 +123,29 @@ msa_status check_common_shape(int Bk, int dI_or_D, int want, const char* name) {
 
 using namespace msa;
 
+msa_status msa::check_decode_args(const msa_decode_args* a) {
+  MSA_REQUIRE(a != nullptr, MSA_ERR_INVALID_ARG, "args is NULL");
+  MSA_REQUIRE(a->B >= 0 && a->Hkv >= 1 && a->Hq >= 1, MSA_ERR_INVALID_ARG, "B = %d, Hq = %d, Hkv = %d", a->B, a->Hq,
+              a->Hkv);
+  MSA_REQUIRE(a->Hq % a->Hkv == 0 && a->Hq / a->Hkv <= kMaxG, MSA_ERR_UNSUPPORTED,
+              "GQA ratio Hq/Hkv = %d/%d not in 1..%d", a->Hq, a->Hkv, kMaxG);
+  if (msa_status st = check_common_shape(a->Bk, a->D, kD, "D"); st != MSA_OK) return st;
+  MSA_REQUIRE(a->k >= 1 && a->k <= kMaxK, MSA_ERR_UNSUPPORTED, "k = %d, supported 1..%d", a->k, kMaxK);
+  MSA_REQUIRE(a->Q && a->K_pool && a->V_pool && a->pt && a->n && a->last_len && a->O, MSA_ERR_INVALID_ARG,
+              "Q, K_pool, V_pool, pt, n, last_len and O must be non-NULL");
+  MSA_REQUIRE(aligned16(a->Q) && aligned16(a->K_pool) && aligned16(a->V_pool) && aligned16(a->O), MSA_ERR_INVALID_ARG,
+              "Q, K_pool, V_pool and O must be 16-byte aligned");
+  MSA_REQUIRE(a->num_pages >= 1 && a->num_pages < (int64_t(1) << 31), MSA_ERR_INVALID_ARG, "num_pages = %" PRId64,
+              a->num_pages);
+  for (int i = 0; i < 2; ++i)
+    MSA_REQUIRE(vec_stride_ok(a->Q_stride[i], 2), MSA_ERR_INVALID_ARG,
+                "Q_stride[%d] = %" PRId64 " must be a positive multiple of 8 elements", i, a->Q_stride[i]);
+  for (int i = 0; i < 3; ++i)
+    MSA_REQUIRE(vec_stride_ok(a->kv_stride[i], 2), MSA_ERR_INVALID_ARG,
+                "kv_stride[%d] = %" PRId64 " must be a positive multiple of 8 elements", i, a->kv_stride[i]);
+  return MSA_OK;
+}
+
 extern "C" {
 
 int msa_version(void) { return 100; }
@@ -226,28 +249,6 @@ msa_status msa_build_page_table(const int32_t* sel, const int32_t* count, const 
 }
 
 // ---------------------------------------------------------------------------
-static msa_status check_decode(const msa_decode_args* a) {
-  MSA_REQUIRE(a != nullptr, MSA_ERR_INVALID_ARG, "args is NULL");
-  MSA_REQUIRE(a->B >= 0 && a->Hkv >= 1 && a->Hq >= 1, MSA_ERR_INVALID_ARG, "B = %d, Hq = %d, Hkv = %d", a->B, a->Hq,
-              a->Hkv);
-  MSA_REQUIRE(a->Hq % a->Hkv == 0 && a->Hq / a->Hkv <= kMaxG, MSA_ERR_UNSUPPORTED,
-              "GQA ratio Hq/Hkv = %d/%d not in 1..%d", a->Hq, a->Hkv, kMaxG);
-  if (msa_status st = check_common_shape(a->Bk, a->D, kD, "D"); st != MSA_OK) return st;
-  MSA_REQUIRE(a->k >= 1 && a->k <= kMaxK, MSA_ERR_UNSUPPORTED, "k = %d, supported 1..%d", a->k, kMaxK);
-  MSA_REQUIRE(a->Q && a->K_pool && a->V_pool && a->pt && a->n && a->last_len && a->O, MSA_ERR_INVALID_ARG,
-              "Q, K_pool, V_pool, pt, n, last_len and O must be non-NULL");
-  MSA_REQUIRE(aligned16(a->Q) && aligned16(a->K_pool) && aligned16(a->V_pool) && aligned16(a->O), MSA_ERR_INVALID_ARG,
-              "Q, K_pool, V_pool and O must be 16-byte aligned");
-  MSA_REQUIRE(a->num_pages >= 1 && a->num_pages < (int64_t(1) << 31), MSA_ERR_INVALID_ARG, "num_pages = %" PRId64,
-              a->num_pages);
-  for (int i = 0; i < 2; ++i)
-    MSA_REQUIRE(vec_stride_ok(a->Q_stride[i], 2), MSA_ERR_INVALID_ARG,
-                "Q_stride[%d] = %" PRId64 " must be a positive multiple of 8 elements", i, a->Q_stride[i]);
-  for (int i = 0; i < 3; ++i)
-    MSA_REQUIRE(vec_stride_ok(a->kv_stride[i], 2), MSA_ERR_INVALID_ARG,
-                "kv_stride[%d] = %" PRId64 " must be a positive multiple of 8 elements", i, a->kv_stride[i]);
-  return MSA_OK;
-}
 
 size_t msa_sparse_attn_decode_workspace_size(const msa_decode_args* a) {
   if (a == nullptr || a->B < 0 || a->Hq < 1 || a->k < 1 || a->D < 1) return 0;
@@ -257,7 +258,7 @@ size_t msa_sparse_attn_decode_workspace_size(const msa_decode_args* a) {
 
 msa_status msa_sparse_attn_decode(const msa_decode_args* a, void* ws, size_t ws_bytes, msa_stream_t stream) {
   g_last_error.clear();
-  if (msa_status st = check_decode(a); st != MSA_OK) return st;
+  if (msa_status st = check_decode_args(a); st != MSA_OK) return st;
   const size_t need = msa_sparse_attn_decode_workspace_size(a);
   MSA_REQUIRE(ws != nullptr && ws_bytes >= need, MSA_ERR_WORKSPACE, "workspace %zu bytes, need %zu", ws_bytes, need);
   MSA_REQUIRE(aligned16(ws), MSA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");

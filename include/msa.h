@@ -267,6 +267,32 @@ msa_status msa_sparse_attn_decode(const msa_decode_args *args, void *ws, size_t 
                                   msa_stream_t stream);
 
 /* --------------------------------------------------------------------------
+ * Paged decode attention without caller-provided scratch.
+ *
+ * The MSA pages have no counterpart to this call; it exists for callers that
+ * cannot allocate device memory or pass a workspace: a serving loop whose
+ * allocator is frozen after start-up, a plug-in whose host framework owns every
+ * device allocation, or code running where an allocation could synchronise the
+ * device.  It computes exactly what msa_sparse_attn_decode computes, with the
+ * same arguments and checks, but keeps its partial outputs in one array of
+ * MSA_NOALLOC_SCRATCH_BYTES that is part of the library's device image and
+ * stays resident on every device that loads the library until the process
+ * exits.  It allocates nothing and frees nothing.
+ *   - Sizes whose scratch, B*Hq*k*(D+1)*4 + 256 bytes, exceeds the array are
+ *     rejected with MSA_ERR_WORKSPACE and a message; use msa_sparse_attn_decode
+ *     with a workspace for those.
+ *   - The first call on a device looks up the array's device address with that
+ *     device current; make that first call before any stream capture.
+ *   - All calls share the array, which keeps the last call's contents.  Calls
+ *     whose kernels overlap on the GPU (other streams, other host threads)
+ *     race on it: serialise them.  Nothing needs clearing between calls, since
+ *     every value the merge reads is written by the same call first.
+ * ------------------------------------------------------------------------ */
+#define MSA_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+msa_status msa_sparse_attn_decode_noalloc(const msa_decode_args *args, msa_stream_t stream);
+
+/* --------------------------------------------------------------------------
  * a6. Log-sum-exp merge of partial softmax results
  *
  * Partial outputs over blocks recombined by a final log-sum-exp reduction
