@@ -202,15 +202,14 @@ def run_decode_ours(args, wl, world, rank):
     stream = torch.cuda.current_stream()
 
     def index_part():
+        # a1 index score with a2 selection and a3 page table fused into the same kernel
         msa.msa_index_score(msa.MSA_MODE_DECODE, inp["q_idx"], inp["w"], inp["kidx_pool"], bufs["C"],
-                            seq_pt=inp["seq_pt"], seq_len=inp["seq_len"], dev_err=bufs["dev_err"])
+                            seq_pt=inp["seq_pt"], seq_len=inp["seq_len"], dev_err=bufs["dev_err"], k=sh.k,
+                            sel=bufs["sel"], count=bufs["count"], pt=bufs["pt"], n=bufs["n"],
+                            last_len=bufs["last_len"], row_scratch=bufs["row_scratch"])
 
     def rest_part():
         e = bufs["dev_err"]
-        msa.msa_topk_blocks(msa.MSA_MODE_DECODE, bufs["C"], sh.k, bufs["sel"], bufs["count"],
-                            seq_len=inp["seq_len"], dev_err=e)
-        msa.msa_build_page_table(bufs["sel"], bufs["count"], inp["seq_pt"], inp["seq_len"], bufs["pt"], bufs["n"],
-                                 bufs["last_len"], dev_err=e)
         msa.msa_sparse_attn_decode(inp["Q"], inp["K_pool"], inp["V_pool"], bufs["pt"], bufs["n"], bufs["last_len"],
                                    bufs["O"], bufs["LSE"], bufs["ws"], dev_err=e)
 
@@ -260,6 +259,41 @@ def run_decode_ours(args, wl, world, rank):
     rest_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     assert int(bufs["dev_err"].item()) == 0, "device error during the timed steps"
 
+    # ---- per-call breakdown (separate pass, one graph per C-ABI call; not part of `value`) ----
+    calls = {
+        "index_score+topk+page_table": index_part,
+        "topk (standalone)": lambda: msa.msa_topk_blocks(msa.MSA_MODE_DECODE, bufs["C"], sh.k, bufs["sel"],
+                                                         bufs["count"], seq_len=inp["seq_len"],
+                                                         dev_err=bufs["dev_err"]),
+        "page_table (standalone)": lambda: msa.msa_build_page_table(bufs["sel"], bufs["count"], inp["seq_pt"],
+                                                                    inp["seq_len"], bufs["pt"], bufs["n"],
+                                                                    bufs["last_len"], dev_err=bufs["dev_err"]),
+        "attention+merge": lambda: msa.msa_sparse_attn_decode(inp["Q"], inp["K_pool"], inp["V_pool"], bufs["pt"],
+                                                              bufs["n"], bufs["last_len"], bufs["O"], bufs["LSE"],
+                                                              bufs["ws"], dev_err=bufs["dev_err"]),
+    }
+    per_call = {}
+    try:
+        gs = {}
+        for name, f in calls.items():
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                f()
+            gs[name] = g
+        runs = [gs[n].replay for n in calls]
+    except Exception:
+        runs = list(calls.values())
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(runs) + 1)] for _ in range(K)]
+    torch.cuda.synchronize()
+    for i in range(K):
+        for j, f in enumerate(runs):
+            evs[i][j].record(stream)
+            f()
+        evs[i][-1].record(stream)
+    torch.cuda.synchronize()
+    for j, name in enumerate(calls):
+        per_call[name] = statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
+
     # ---- end to end through the C ABI with host buffers ----
     small = ("Q", "q_idx", "w", "seq_pt", "seq_len")
     host_in = {n: inp[n].cpu().pin_memory() for n in small}
@@ -304,16 +338,17 @@ def run_decode_ours(args, wl, world, rank):
                    "k": wl.shape.k, "pages": "128-token, shuffled", "cuda_graphs": graphs,
                    "l2": "no flush: inputs larger than L2 (491 MB k_idx pool read per step)",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "kernel": "index_decode_kernel", "achieved": achieved,
+        "roofline": {"bound": "hbm", "kernel": "index_decode_kernel (with fused selection)", "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                      "peak_src": peaks["src"], "traffic": traffic, "traffic_src": traffic_src,
                      "algorithmic_bytes_per_launch": alg["index_kernel"], "launch_ms": idx_ms,
                      "step_algorithmic_bytes": alg["step"],
                      "step_frac": alg["step"] / (step_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
-        "breakdown_ms": {"index_score": idx_ms, "topk+page_table+attention+merge": rest_ms},
+        "breakdown_ms": {"index_score+topk+page_table": idx_ms, "attention+merge": rest_ms,
+                         "per_call_graphs": per_call},
         "e2e": {"value": tokens_per_step / (e2e_ms / K * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 5 * K,
+        "gpu_launches": 2 * K,
         "clocks": clocks,
     }
     return res, host_in, inp
@@ -422,7 +457,7 @@ def run_prefill_ours(args, wl, world, rank):
                      "index_tflops": idx_flops / (part_ms[0] * 1e-3) / 1e12,
                      "index_frac": idx_flops / (part_ms[0] * 1e-3) / 1e12 / peaks["bf16_tflops"]},
         "breakdown_ms": {"index_score": part_ms[0], "topk": part_ms[1], "sparse_attention": part_ms[2]},
-        "gpu_launches": None,
+        "gpu_launches": K * (2 + 5 * ((wl.B * wl.S + ws_q - 1) // ws_q)),
         "clocks": clocks,
     }
     return res, None, inp

@@ -66,15 +66,21 @@ def _strides(t: torch.Tensor, n: int):
 
 def msa_index_score(mode: int, q_idx: torch.Tensor, w: torch.Tensor, k_idx: torch.Tensor, C_out: torch.Tensor,
                     *, seq_pt: Optional[torch.Tensor] = None, seq_len: Optional[torch.Tensor] = None,
-                    dev_err: Optional[torch.Tensor] = None, stream=None) -> None:
+                    dev_err: Optional[torch.Tensor] = None, stream=None, k: int = 0,
+                    sel: Optional[torch.Tensor] = None, count: Optional[torch.Tensor] = None,
+                    pt: Optional[torch.Tensor] = None, n: Optional[torch.Tensor] = None,
+                    last_len: Optional[torch.Tensor] = None, row_scratch: Optional[torch.Tensor] = None) -> None:
     """Block scores of the Index Branch into ``C_out`` (see msa.h, a1).
 
     PREFILL: q_idx [B,S,Hkv,HI,dI], w [B,S,Hkv,HI], k_idx [B,S,Hkv,dI], C_out [B,S,Hkv,nb_stride].
     DECODE:  q_idx [B,Hkv,HI,dI], w [B,Hkv,HI], k_idx pool [P,Hkv,Bk,dI], C_out [B,Hkv,nb_stride],
              seq_pt [B,max_pages] int32 (contiguous rows), seq_len [B] int32.
+    DECODE with ``sel`` given: the same call also selects (a2) into sel/count and,
+    with ``pt`` given, builds the page table (a3) into pt/n/last_len; ``row_scratch``
+    is B*Hkv int32 of scratch.
     """
-    for t, n in ((q_idx, "q_idx"), (w, "w"), (k_idx, "k_idx"), (C_out, "C")):
-        _inner_contig(t, n)
+    for t, nm in ((q_idx, "q_idx"), (w, "w"), (k_idx, "k_idx"), (C_out, "C")):
+        _inner_contig(t, nm)
     a = _abi.IndexArgs()
     a.mode = mode
     a.q_idx, a.w, a.k_idx, a.C = _ptr(q_idx), _ptr(w), _ptr(k_idx), _ptr(C_out)
@@ -98,6 +104,13 @@ def msa_index_score(mode: int, q_idx: torch.Tensor, w: torch.Tensor, k_idx: torc
             raise ValueError("seq_pt must be contiguous")
         a.num_pages = k_idx.shape[0]
         a.seq_pt, a.max_pages, a.seq_len = _ptr(seq_pt), seq_pt.shape[1], _ptr(seq_len)
+        if sel is not None:
+            for t, nm in ((sel, "sel"), (count, "count"), (row_scratch, "row_scratch")):
+                if t is None or not t.is_contiguous():
+                    raise ValueError(f"fused selection: {nm} must be a contiguous tensor")
+            a.k, a.sel, a.count, a.row_scratch = k, _ptr(sel), _ptr(count), _ptr(row_scratch)
+            if pt is not None:
+                a.pt, a.n, a.last_len = _ptr(pt), _ptr(n), _ptr(last_len)
     _abi.check(lib().msa_index_score(C.byref(a), _stream(stream)), "msa_index_score")
 
 
@@ -209,9 +222,9 @@ def _decode_args(Q, K_pool, V_pool, pt, n, last_len, O, LSE, softmax_scale, dev_
     return a
 
 
-def msa_sparse_attn_decode_workspace_size(B: int, Hq: int, k: int, D_: int = D) -> int:
+def msa_sparse_attn_decode_workspace_size(B: int, Hq: int, Hkv: int, k: int, D_: int = D) -> int:
     a = _abi.DecodeArgs()
-    a.B, a.Hq, a.k, a.D = B, Hq, k, D_
+    a.B, a.Hq, a.Hkv, a.k, a.D = B, Hq, Hkv, k, D_
     return int(lib().msa_sparse_attn_decode_workspace_size(C.byref(a)))
 
 
@@ -263,29 +276,38 @@ def decode_buffers(B: int, Hq: int, Hkv: int, k: int, nb_stride: int, device) ->
         "last_len": torch.empty(B * Hkv, dtype=torch.int32, device=dev),
         "O": torch.empty(B, Hq, D, dtype=torch.bfloat16, device=dev),
         "LSE": torch.empty(B, Hq, dtype=torch.float32, device=dev),
-        "ws": torch.empty(msa_sparse_attn_decode_workspace_size(B, Hq, k) // 4 + 64, dtype=torch.float32,
+        "ws": torch.empty(msa_sparse_attn_decode_workspace_size(B, Hq, Hkv, k) // 4 + 64, dtype=torch.float32,
                           device=dev),
+        "row_scratch": torch.empty(B * Hkv, dtype=torch.int32, device=dev),
         "dev_err": torch.zeros(1, dtype=torch.int32, device=dev),
     }
 
 
 def decode_step(inp: Dict[str, torch.Tensor], k: int, bufs: Optional[Dict[str, torch.Tensor]] = None,
-                softmax_scale: float = 0.0, stream=None) -> Dict[str, torch.Tensor]:
+                softmax_scale: float = 0.0, stream=None, fused: bool = True) -> Dict[str, torch.Tensor]:
     """One MSA decode step: a1 index score -> a2 top-k -> a3 page table -> a5/a6 attention.
 
     ``inp`` holds Q, q_idx, w, kidx_pool, K_pool, V_pool, seq_pt, seq_len (device tensors).
+    With ``fused`` (default) a1-a3 run in one index-score call; otherwise the
+    four entry points are called one by one.
     """
     B, Hq, _ = inp["Q"].shape
     Hkv = inp["K_pool"].shape[1]
     if bufs is None:
         bufs = decode_buffers(B, Hq, Hkv, k, inp["seq_pt"].shape[1], inp["Q"].device)
     e = bufs["dev_err"]
-    msa_index_score(MSA_MODE_DECODE, inp["q_idx"], inp["w"], inp["kidx_pool"], bufs["C"], seq_pt=inp["seq_pt"],
-                    seq_len=inp["seq_len"], dev_err=e, stream=stream)
-    msa_topk_blocks(MSA_MODE_DECODE, bufs["C"], k, bufs["sel"], bufs["count"], seq_len=inp["seq_len"], dev_err=e,
-                    stream=stream)
-    msa_build_page_table(bufs["sel"], bufs["count"], inp["seq_pt"], inp["seq_len"], bufs["pt"], bufs["n"],
-                         bufs["last_len"], dev_err=e, stream=stream)
+    if fused:
+        msa_index_score(MSA_MODE_DECODE, inp["q_idx"], inp["w"], inp["kidx_pool"], bufs["C"], seq_pt=inp["seq_pt"],
+                        seq_len=inp["seq_len"], dev_err=e, stream=stream, k=k, sel=bufs["sel"],
+                        count=bufs["count"], pt=bufs["pt"], n=bufs["n"], last_len=bufs["last_len"],
+                        row_scratch=bufs["row_scratch"])
+    else:
+        msa_index_score(MSA_MODE_DECODE, inp["q_idx"], inp["w"], inp["kidx_pool"], bufs["C"], seq_pt=inp["seq_pt"],
+                        seq_len=inp["seq_len"], dev_err=e, stream=stream)
+        msa_topk_blocks(MSA_MODE_DECODE, bufs["C"], k, bufs["sel"], bufs["count"], seq_len=inp["seq_len"],
+                        dev_err=e, stream=stream)
+        msa_build_page_table(bufs["sel"], bufs["count"], inp["seq_pt"], inp["seq_len"], bufs["pt"], bufs["n"],
+                             bufs["last_len"], dev_err=e, stream=stream)
     msa_sparse_attn_decode(inp["Q"], inp["K_pool"], inp["V_pool"], bufs["pt"], bufs["n"], bufs["last_len"],
                            bufs["O"], bufs["LSE"], bufs["ws"], softmax_scale=softmax_scale, dev_err=e,
                            stream=stream)

@@ -44,6 +44,8 @@ class IndexArgs(C.Structure):
         ("num_pages", C.c_int64), ("seq_pt", _p), ("max_pages", C.c_int64), ("seq_len", _p),
         ("C", _p), ("C_stride", _i64x3), ("nb_stride", C.c_int),
         ("dev_err", _p),
+        ("k", C.c_int), ("sel", _p), ("count", _p), ("pt", _p), ("n", _p), ("last_len", _p),
+        ("row_scratch", _p),
     ]
 
 

@@ -207,6 +207,14 @@ msa_status msa_index_score(const msa_index_args* a, msa_stream_t stream) {
   }
   MSA_REQUIRE(a->w_stride[0] > 0 && a->w_stride[1] > 0 && a->C_stride[0] > 0 && a->C_stride[1] > 0,
               MSA_ERR_INVALID_ARG, "w / C strides must be positive");
+  if (a->sel != nullptr) {
+    MSA_REQUIRE(a->k >= 1 && a->k <= kMaxK, MSA_ERR_UNSUPPORTED, "fused selection: k = %d, supported 1..%d", a->k,
+                kMaxK);
+    MSA_REQUIRE(a->count != nullptr && a->row_scratch != nullptr, MSA_ERR_INVALID_ARG,
+                "fused selection needs count and row_scratch");
+    MSA_REQUIRE(a->pt == nullptr || (a->n != nullptr && a->last_len != nullptr), MSA_ERR_INVALID_ARG,
+                "fused page table needs n and last_len");
+  }
   if (a->B == 0) return MSA_OK;
   return launch_index_decode(*a, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -253,7 +261,8 @@ msa_status msa_build_page_table(const int32_t* sel, const int32_t* count, const 
 size_t msa_sparse_attn_decode_workspace_size(const msa_decode_args* a) {
   if (a == nullptr || a->B < 0 || a->Hq < 1 || a->k < 1 || a->D < 1) return 0;
   const size_t parts = static_cast<size_t>(a->B) * a->Hq * a->k;
-  return parts * static_cast<size_t>(a->D) * 4 + parts * 4 + 256;
+  const size_t rows = static_cast<size_t>(a->B) * (a->Hkv > 0 ? a->Hkv : 1);
+  return parts * static_cast<size_t>(a->D) * 4 + parts * 4 + rows * 4 + 256;
 }
 
 msa_status msa_sparse_attn_decode(const msa_decode_args* a, void* ws, size_t ws_bytes, msa_stream_t stream) {
@@ -266,10 +275,8 @@ msa_status msa_sparse_attn_decode(const msa_decode_args* a, void* ws, size_t ws_
   float* o_part = static_cast<float*>(ws);
   const size_t parts = static_cast<size_t>(a->B) * a->Hq * a->k;
   float* lse_part = o_part + parts * a->D;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (msa_status st = launch_attn_decode(*a, o_part, lse_part, s); st != MSA_OK) return st;
-  return launch_lse_merge(o_part, lse_part, static_cast<int64_t>(a->B) * a->Hq, a->k, a->D, a->O, a->LSE,
-                          a->dev_err, s);
+  int32_t* counter = reinterpret_cast<int32_t*>(lse_part + parts);
+  return launch_attn_decode(*a, o_part, lse_part, counter, reinterpret_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------------------------

@@ -1,5 +1,6 @@
-// attn_decode.cu -- a5: sparse attention of one decode step over the selected
-// pages, the KV-group dimension flattened into the batch.
+// attn_decode.cu -- a5 + a6: sparse attention of one decode step over the
+// selected pages, the KV-group dimension flattened into the batch, with the
+// log-sum-exp merge fused in.
 //
 // Row r = b * Hkv + g of the page table built from the selected blocks lists
 // n[r] physical pages; the G query heads of group g attend to each page as an
@@ -8,7 +9,9 @@
 //     z[h][t] = scale * Q[b, g*G + h] . K_page[t]      (t < valid tokens)
 //     m_h = max_t z,  l_h = sum_t e^{z - m_h},  O_h = sum_t e^{z - m_h} V_t / l_h
 //     O_part[(r*G + h), s] = O_h,   LSE_part[(r*G + h), s] = m_h + ln l_h
-// The partials are merged by the log-sum-exp merge kernel.
+// and the CTA that finishes the last split of a row merges the row's partials
+// (LSE = ln sum_s e^{LSE_s}, O = sum_s e^{LSE_s - LSE} O_s; paragraph
+// "KV-Block-Major" of the same post) while they are still in L2.
 //
 // tcgen05 mapping (one TMEM slot of 32 columns per unit, two slots):
 //   MMA1  S^T[t][h] = K[t][:] . Q[h][:]    M = 128 keys, N = 16 (heads, padded),
@@ -19,7 +22,9 @@
 //                                          V is the MN-major A operand
 //   epilogue: one thread per d, coalesced fp32 partial rows.
 // Warp 0 streams K, V (64 KiB) and the row's 16 Q rows by TMA into a 3-deep
-// ring; warp 1 issues the MMAs; warps 2-5 run softmax and epilogue.
+// ring; warp 1 issues the MMAs; warps 2-5 run softmax, epilogue and merge.
+// Each CTA first copies its units' page ids and valid lengths into shared
+// memory, so no role waits on a global load per unit.
 #include "msa_internal.h"
 #include "msa_ptx.cuh"
 
@@ -33,9 +38,10 @@ constexpr int kStageBytes = 4 * kHalf + 2 * kQHalf;    // K0 K1 V0 V1 Q0 Q1
 constexpr int kPTile = 2 * kQHalf;                     // P^T: 16 rows x 128 keys
 constexpr int kSlots = 2;
 constexpr int kTmemCols = 64;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;   // w0 TMA, w1 MMA, w2-5 and w6-9 softmax/epilogue
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kMaxUnits = 512;          // (row, page) units per CTA, kept in shared memory
 
 struct Params {
   int B, Hq, Hkv, G, k;
@@ -46,14 +52,11 @@ struct Params {
   const int32_t* last_len;
   float* o_part;
   float* lse_part;
+  int32_t* counter;                     // [B*Hkv] splits finished per row, zero on entry
+  __nv_bfloat16* O;                     // [B, Hq, D]
+  float* LSE;                           // [B, Hq] or null
   int32_t* dev_err;
 };
-
-__device__ __forceinline__ bool unit_live(const Params& p, int64_t u, int& r, int& s) {
-  r = static_cast<int>(u / p.k);
-  s = static_cast<int>(u % p.k);
-  return s < p.n[r];
-}
 
 __global__ void __launch_bounds__(kThreads, 1)
 attn_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -67,19 +70,50 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
   __shared__ __align__(8) uint64_t bar_sfull[kSlots], bar_pready[kSlots], bar_ofull[kSlots], bar_sfree[kSlots];
   __shared__ __align__(8) uint64_t bar_drain;
   __shared__ uint32_t s_tmem;
-  __shared__ int s_abort, s_fail;
-  __shared__ float s_red[4][kMaxG];
+  __shared__ int s_abort;
+  __shared__ float s_red[2][4][kMaxG];
+  __shared__ int s_upage[kMaxUnits];    // physical page of each unit of this CTA
+  __shared__ int s_uvalid[kMaxUnits];   // valid tokens of the page; 0 = no such split
+  __shared__ int s_un[kMaxUnits];       // selected pages of the unit's row
+  __shared__ int s_last[2], s_fail[2];
+  __shared__ float s_mlse[2][kMaxG][kMaxK];   // merge: LSE of each (head, split) of the row
+  __shared__ float s_mm[2][kMaxG], s_minv[2][kMaxG];
+  __shared__ short s_live[kMaxUnits];         // offsets of the live units of this CTA, in order
+  __shared__ int s_nlive;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t units = static_cast<int64_t>(p.B) * p.Hkv * p.k;
+  const int64_t per_cta = (units + gridDim.x - 1) / gridDim.x;
+  const int64_t lo = min(units, static_cast<int64_t>(blockIdx.x) * per_cta);
+  const int64_t hi = min(units, lo + per_cta);
 
-  // empty splits (s >= n[r]) carry LSE = -inf so the merge skips them
-  for (int64_t e = static_cast<int64_t>(blockIdx.x) * kThreads + tid; e < units * p.G;
-       e += static_cast<int64_t>(gridDim.x) * kThreads) {
-    const int64_t u = e / p.G;
-    const int h = static_cast<int>(e % p.G);
-    int r, s;
-    if (!unit_live(p, u, r, s)) p.lse_part[(static_cast<int64_t>(r) * p.G + h) * p.k + s] = -INFINITY;
+  // this CTA's units: page id, valid length and row size, read once
+  for (int64_t u = lo + tid; u < hi; u += kThreads) {
+    const int r = static_cast<int>(u / p.k), s = static_cast<int>(u % p.k);
+    const int nr = min(max(p.n[r], 0), p.k);
+    const bool live = s < nr;
+    s_upage[u - lo] = live ? p.pt[u] : -1;
+    s_uvalid[u - lo] = live ? (s == nr - 1 ? min(max(p.last_len[r], 1), kBk) : kBk) : 0;
+    s_un[u - lo] = nr;
+    if (nr == 0 && s == 0) {   // a row with nothing selected: O = 0, LSE = -inf
+      for (int h = 0; h < p.G; ++h) {
+        const int64_t row = static_cast<int64_t>(r) * p.G + h;
+        for (int d = 0; d < kD; d += 8) *reinterpret_cast<uint4*>(p.O + row * kD + d) = make_uint4(0, 0, 0, 0);
+        if (p.LSE != nullptr) p.LSE[row] = -INFINITY;
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {   // compact the live units, in order
+    int c = 0;
+    const int cnt = static_cast<int>(hi - lo);
+    for (int base = 0; base < cnt; base += 32) {
+      const bool live = base + lane < cnt && s_uvalid[base + lane] > 0;
+      const uint32_t m = __ballot_sync(0xffffffffu, live);
+      if (live) s_live[c + __popc(m & ((1u << lane) - 1u))] = static_cast<short>(base + lane);
+      c += __popc(m);
+    }
+    if (lane == 0) s_nlive = c;
   }
   // P^T rows G..15 stay zero for the whole kernel
   for (int i = tid; i < kSlots * kPTile / 16; i += kThreads)
@@ -93,7 +127,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     }
     mbar_init(&bar_drain, 1);
     s_abort = 0;
-    s_fail = 0;
+    s_fail[0] = s_fail[1] = 0;
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(&s_tmem, kTmemCols);
@@ -102,20 +136,17 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
   const uint32_t tmem = s_tmem;
   volatile int* abort_flag = &s_abort;
 
-  const int64_t per_cta = (units + gridDim.x - 1) / gridDim.x;
-  const int64_t lo = min(units, static_cast<int64_t>(blockIdx.x) * per_cta);
-  const int64_t hi = min(units, lo + per_cta);
-
   if (warp == 0) {
     // ===================== TMA producer =====================
     if (lane == 0) {
+      const int nlive = s_nlive;
       int n = 0;
-      for (int64_t u = lo; u < hi; ++u) {
-        int r, s;
-        if (!unit_live(p, u, r, s)) continue;
+      for (; n < nlive; ++n) {
+        const int64_t u = lo + s_live[n];
+        const int r = static_cast<int>(u / p.k);
         const int st = n % kStages;
         if (!mbar_wait(&bar_empty[st], ((n / kStages) & 1) ^ 1, abort_flag, p.dev_err)) break;
-        const int64_t page = p.pt[static_cast<int64_t>(r) * p.k + s];
+        const int64_t page = s_upage[u - lo];
         const int b = r / p.Hkv, g = r % p.Hkv;
         uint8_t* sb = s_stage + st * kStageBytes;
         if (page < 0 || page >= p.num_pages) {
@@ -130,7 +161,6 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
           tma_load_3d(sb + 4 * kHalf, &qmap, &bar_full[st], 0, g * p.G, b);
           tma_load_3d(sb + 4 * kHalf + kQHalf, &qmap, &bar_full[st], 64, g * p.G, b);
         }
-        ++n;
       }
       if (*abort_flag) {
         for (int i = max(0, n - kStages); i < n; ++i) {
@@ -143,39 +173,49 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     }
   } else if (warp == 1) {
     // ===================== tcgen05 issuer =====================
+    // S of unit n+1 is issued before O of unit n, so the two softmax warpgroups
+    // (slot n mod 2) overlap.
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 16, false, false);
       constexpr uint32_t idesc_o = idesc_bf16(128, 16, true, false);
-      int n = 0;
-      for (int64_t u = lo; u < hi; ++u) {
-        int r, s;
-        if (!unit_live(p, u, r, s)) continue;
-        const int st = n % kStages, slot = n % kSlots;
-        const uint32_t ph_slot = (n / kSlots) & 1;
-        if (!mbar_wait(&bar_full[st], (n / kStages) & 1, abort_flag, p.dev_err)) break;
-        if (!mbar_wait(&bar_sfree[slot], ph_slot ^ 1, abort_flag, p.dev_err)) break;
+      const int nlive = s_nlive;
+      auto issue_s = [&](int n) -> bool {
+        const int st = n % kStages, slot = n & 1;
+        if (!mbar_wait(&bar_full[st], (n / kStages) & 1, abort_flag, p.dev_err)) return false;
+        if (!mbar_wait(&bar_sfree[slot], ((n >> 1) & 1) ^ 1, abort_flag, p.dev_err)) return false;
         tc_fence_after();
         const uint32_t sb = smem_u32(s_stage + st * kStageBytes);
-        const uint32_t d_s = tmem + slot * 32, d_o = tmem + slot * 32 + 16;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * kHalf + 32 * (kk & 3);
           const uint32_t qoff = 4 * kHalf + (kk >> 2) * kQHalf + 32 * (kk & 3);
-          umma_bf16(d_s, sdesc_sw128(sb + off, 16, 1024), sdesc_sw128(sb + qoff, 16, 1024), idesc_s, kk > 0);
+          umma_bf16(tmem + slot * 32, sdesc_sw128(sb + off, 16, 1024), sdesc_sw128(sb + qoff, 16, 1024), idesc_s,
+                    kk > 0);
         }
         umma_commit(&bar_sfull[slot]);
-        if (!mbar_wait(&bar_pready[slot], ph_slot, abort_flag, p.dev_err)) break;
+        return true;
+      };
+      auto issue_o = [&](int n) -> bool {
+        const int st = n % kStages, slot = n & 1;
+        if (!mbar_wait(&bar_pready[slot], (n >> 1) & 1, abort_flag, p.dev_err)) return false;
         tc_fence_after();
+        const uint32_t sb = smem_u32(s_stage + st * kStageBytes);
         const uint32_t pb = smem_u32(s_p + slot * kPTile);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t voff = 2 * kHalf + kk * 2048;          // 16 keys per step
           const uint32_t poff = (kk >> 2) * kQHalf + 32 * (kk & 3);
-          umma_bf16(d_o, sdesc_sw128(sb + voff, kHalf, 1024), sdesc_sw128(pb + poff, 16, 1024), idesc_o, kk > 0);
+          umma_bf16(tmem + slot * 32 + 16, sdesc_sw128(sb + voff, kHalf, 1024), sdesc_sw128(pb + poff, 16, 1024),
+                    idesc_o, kk > 0);
         }
         umma_commit(&bar_ofull[slot]);
         umma_commit(&bar_empty[st]);
-        ++n;
+        return true;
+      };
+      bool ok = nlive > 0 ? issue_s(0) : true;
+      for (int n = 0; n < nlive && ok; ++n) {
+        if (n + 1 < nlive) ok = issue_s(n + 1);
+        if (ok) ok = issue_o(n);
       }
       umma_commit(&bar_drain);
       uint64_t t0 = global_timer_ns();
@@ -184,26 +224,79 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     }
     __syncwarp();
   } else {
-    // ===================== softmax + epilogue (warps 2..5) =====================
+    // ===================== softmax + epilogue: two warpgroups =====================
+    // Warpgroup wg (warps 2-5 or 6-9) takes the units n = wg (mod 2), i.e. TMEM
+    // slot wg, so two softmax chains run at once.
+    const int wg = (warp - 2) >> 2;
+    const int bar_id = 1 + wg;
     const int q = warp & 3;
     const int t = q * 32 + lane;                 // key index (MMA1) / d index (MMA2)
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     const int G = p.G;
-    int n = 0;
-    for (int64_t u = lo; u < hi; ++u) {
-      int r, s;
-      if (!unit_live(p, u, r, s)) continue;
-      const int slot = n % kSlots;
-      const uint32_t ph_slot = (n / kSlots) & 1;
-      // ---- S^T ready: every epilogue warp decides together whether to go on
-      if (!mbar_wait(&bar_sfull[slot], ph_slot, abort_flag, p.dev_err)) s_fail = 1;
-      named_bar_sync(1, 128);
-      if (s_fail) break;
+    const int nlive = s_nlive;
+    int cur_r = -1, cur_nr = 0, seg_cnt = 0;
+    // splits of row cur_r finished by this warpgroup are published in one step;
+    // the warpgroup whose step completes the row merges the row's partials
+    auto flush = [&]() {
+      if (cur_r < 0) return;
+      __threadfence();
+      named_bar_sync(bar_id, 128);
+      if (t == 0) s_last[wg] = atomicAdd(&p.counter[cur_r], seg_cnt) + seg_cnt == cur_nr;
+      named_bar_sync(bar_id, 128);
+      if (!s_last[wg]) return;
+      __threadfence();
+      const int r = cur_r, nr = cur_nr;
+      for (int e = t; e < G * nr; e += 128) {
+        const int h = e / nr, x = e % nr;
+        s_mlse[wg][h][x] = __ldcg(p.lse_part + (static_cast<int64_t>(r) * G + h) * p.k + x);
+      }
+      named_bar_sync(bar_id, 128);
+      if (t < G) {
+        float m = -INFINITY;
+        for (int x = 0; x < nr; ++x) m = fmaxf(m, s_mlse[wg][t][x]);
+        float sum = 0.f;
+        if (m != -INFINITY)
+          for (int x = 0; x < nr; ++x) sum += s_mlse[wg][t][x] == -INFINITY ? 0.f : __expf(s_mlse[wg][t][x] - m);
+        s_mm[wg][t] = m;
+        s_minv[wg][t] = m == -INFINITY ? 0.f : 1.0f / sum;
+        if (p.LSE != nullptr) p.LSE[static_cast<int64_t>(r) * G + t] = m == -INFINITY ? -INFINITY : m + __logf(sum);
+      }
+      named_bar_sync(bar_id, 128);
+      for (int h = 0; h < G; ++h) {           // thread = d; all partial loads independent
+        const int64_t row = static_cast<int64_t>(r) * G + h;
+        const float m = s_mm[wg][h], inv = s_minv[wg][h];
+        float acc = 0.f;
+#pragma unroll 8
+        for (int x = 0; x < nr; ++x) {
+          const float lx = s_mlse[wg][h][x];
+          const float wgt = (lx == -INFINITY) ? 0.f : __expf(lx - m) * inv;
+          acc = fmaf(wgt, __ldcg(p.o_part + (row * p.k + x) * kD + t), acc);
+        }
+        p.O[row * kD + t] = __float2bfloat16_rn(acc);
+      }
+      if (t == 0) p.counter[r] = 0;           // ready for the next call
+      named_bar_sync(bar_id, 128);            // s_mlse / s_mm are reused
+    };
+    for (int n = wg; n < nlive; n += 2) {
+      const int64_t u = lo + s_live[n];
+      const int valid = s_uvalid[u - lo];
+      const int r = static_cast<int>(u / p.k), s = static_cast<int>(u % p.k);
+      if (r != cur_r) {
+        flush();
+        cur_r = r;
+        cur_nr = s_un[u - lo];
+        seg_cnt = 0;
+      }
+      const int slot = wg;
+      const uint32_t ph_slot = (n >> 1) & 1;
+      // ---- S^T ready: the warpgroup decides together whether to go on
+      if (!mbar_wait(&bar_sfull[slot], ph_slot, abort_flag, p.dev_err)) s_fail[wg] = 1;
+      named_bar_sync(bar_id, 128);
+      if (s_fail[wg]) break;
       tc_fence_after();
       uint32_t sv[8];
       tmem_ld8(tmem + lane_addr + slot * 32, sv);
       tmem_ld_wait();
-      const int valid = (s == p.n[r] - 1) ? p.last_len[r] : kBk;
       float z[kMaxG];
       float mx[kMaxG];
 #pragma unroll
@@ -216,13 +309,13 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
       }
       if (lane == 0) {
 #pragma unroll
-        for (int h = 0; h < kMaxG; ++h) s_red[q][h] = mx[h];
+        for (int h = 0; h < kMaxG; ++h) s_red[wg][q][h] = mx[h];
       }
-      named_bar_sync(1, 128);
+      named_bar_sync(bar_id, 128);
       float l[kMaxG];
 #pragma unroll
       for (int h = 0; h < kMaxG; ++h) {
-        mx[h] = fmaxf(fmaxf(s_red[0][h], s_red[1][h]), fmaxf(s_red[2][h], s_red[3][h]));
+        mx[h] = fmaxf(fmaxf(s_red[wg][0][h], s_red[wg][1][h]), fmaxf(s_red[wg][2][h], s_red[wg][3][h]));
         const float e = (t < valid) ? exp2f(z[h] - mx[h]) : 0.f;
         z[h] = e;
         float v = e;
@@ -230,10 +323,10 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
         l[h] = v;
       }
-      named_bar_sync(1, 128);           // everyone has read the maxima
+      named_bar_sync(bar_id, 128);           // everyone has read the maxima
       if (lane == 0) {
 #pragma unroll
-        for (int h = 0; h < kMaxG; ++h) s_red[q][h] = l[h];
+        for (int h = 0; h < kMaxG; ++h) s_red[wg][q][h] = l[h];
       }
       // P^T[h][t] into the K-major B tile of this slot
       uint8_t* pt_tile = s_p + slot * kPTile + (t >> 6) * kQHalf;
@@ -249,13 +342,13 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_pready[slot]);
-      named_bar_sync(1, 128);
+      named_bar_sync(bar_id, 128);
 #pragma unroll
-      for (int h = 0; h < kMaxG; ++h) l[h] = s_red[0][h] + s_red[1][h] + s_red[2][h] + s_red[3][h];
+      for (int h = 0; h < kMaxG; ++h) l[h] = s_red[wg][0][h] + s_red[wg][1][h] + s_red[wg][2][h] + s_red[wg][3][h];
       // ---- O^T ready
-      if (!mbar_wait(&bar_ofull[slot], ph_slot, abort_flag, p.dev_err)) s_fail = 1;
-      named_bar_sync(1, 128);
-      if (s_fail) break;
+      if (!mbar_wait(&bar_ofull[slot], ph_slot, abort_flag, p.dev_err)) s_fail[wg] = 1;
+      named_bar_sync(bar_id, 128);
+      if (s_fail[wg]) break;
       tc_fence_after();
       uint32_t ov[8];
       tmem_ld8(tmem + lane_addr + slot * 32 + 16, ov);
@@ -263,7 +356,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_sfree[slot]);
-      const int64_t page = p.pt[static_cast<int64_t>(r) * p.k + s];
+      const int64_t page = s_upage[u - lo];
       const bool bad = page < 0 || page >= p.num_pages;
       if (bad && t == 0) report(p.dev_err, MSA_DEVERR_BAD_PAGE);
 #pragma unroll
@@ -274,8 +367,9 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
           if (t == h) p.lse_part[row] = bad ? -INFINITY : (mx[h] + log2f(l[h])) * kLn2;
         }
       }
-      ++n;
+      ++seg_cnt;
     }
+    if (!s_fail[wg]) flush();
   }
 
   tc_fence_before();
@@ -288,7 +382,8 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
 
 }  // namespace
 
-msa_status launch_attn_decode(const msa_decode_args& a, float* o_part, float* lse_part, cudaStream_t stream) {
+msa_status launch_attn_decode(const msa_decode_args& a, float* o_part, float* lse_part, int32_t* counter,
+                              cudaStream_t stream) {
   DeviceInfo dev;
   if (msa_status st = current_device(&dev); st != MSA_OK) return st;
   CUtensorMap kmap, vmap, qmap;
@@ -319,6 +414,9 @@ msa_status launch_attn_decode(const msa_decode_args& a, float* o_part, float* ls
   p.scale_log2 = scale * kLog2e;
   p.num_pages = a.num_pages; p.pt = a.pt; p.n = a.n; p.last_len = a.last_len;
   p.o_part = o_part; p.lse_part = lse_part; p.dev_err = a.dev_err;
+  p.counter = counter;
+  p.O = static_cast<__nv_bfloat16*>(a.O);
+  p.LSE = a.LSE;
 
   const size_t smem = 1024 + static_cast<size_t>(kStages) * kStageBytes + kSlots * kPTile;
   if (smem > dev.max_smem_optin) return fail(MSA_ERR_UNSUPPORTED, "decode attention: not enough shared memory");
@@ -326,7 +424,10 @@ msa_status launch_attn_decode(const msa_decode_args& a, float* o_part, float* ls
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attn_decode)");
   const int64_t units = static_cast<int64_t>(a.B) * a.Hkv * a.k;
-  const int grid = static_cast<int>(std::min<int64_t>(dev.num_sms, std::max<int64_t>(units, 1)));
+  const int64_t grid64 = std::max<int64_t>(std::min<int64_t>(dev.num_sms, units), (units + kMaxUnits - 1) / kMaxUnits);
+  const int grid = static_cast<int>(std::max<int64_t>(grid64, 1));
+  e = cudaMemsetAsync(counter, 0, static_cast<size_t>(a.B) * a.Hkv * sizeof(int32_t), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(decode row counters)");
   attn_decode_kernel<<<grid, kThreads, smem, stream>>>(kmap, vmap, qmap, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "attn_decode_kernel launch");

@@ -13,9 +13,9 @@
 // The array is kNoallocScratchBytes large and stays resident on every device
 // that loads the library until the process exits.  All calls share it: two
 // calls whose kernels overlap on the GPU (different streams, or several host
-// threads) race on it and must be serialised by the caller.  Every partial that
-// the merge reads is written by the same call first, so nothing has to be
-// cleared between calls.
+// threads) race on it and must be serialised by the caller.  Each call clears
+// the per-row counters it uses (cudaMemsetAsync) and writes every partial that
+// the merge reads before reading it.
 #include <cstdio>
 #include <mutex>
 
@@ -63,7 +63,7 @@ extern "C" msa_status msa_sparse_attn_decode_noalloc(const msa_decode_args* a, m
   if (need > kNoallocScratchBytes) {
     char buf[256];
     std::snprintf(buf, sizeof(buf),
-                  "decode needs %zu bytes of scratch (B*Hq*k*(D+1)*4 + 256) but the built-in array holds %zu; "
+                  "decode needs %zu bytes of scratch (B*Hq*k*(D+1)*4 + B*Hkv*4 + 256) but the built-in array holds %zu; "
                   "use msa_sparse_attn_decode with a workspace",
                   need, kNoallocScratchBytes);
     return fail(MSA_ERR_WORKSPACE, buf);

@@ -12,23 +12,28 @@
 // once.  A persistent CTA per SM walks a contiguous range of the flattened
 // (b, g, j) items:
 //   warp 0    TMA producer: one 4-D tiled load (128 tokens x 64 dims, 128-byte
-//             swizzle) per block into an 8-deep shared-memory ring;
+//             swizzle) per block into a 12-deep shared-memory ring, page ids
+//             fetched 32 at a time by the whole warp;
 //   warp 1    tcgen05 issuer: D[t, h] = k_idx_t . q_idx_h as one M=128 (tokens)
 //             x N=16 (index heads, zero-padded) x K=64 contraction (4 MMAs)
-//             into one of 8 TMEM slots; it also stages q_idx of the current
+//             into one of 16 TMEM slots; it also stages q_idx of the current
 //             (b, g) as the B operand (double-buffered);
 //   warps 2-5 epilogue: thread = token; w-weighted ReLU sum over heads, max
 //             over the block's 128 tokens, one fp32 store per block.
 #include "msa_internal.h"
 #include "msa_ptx.cuh"
+#include "select_warp.cuh"
 
 namespace msa {
 namespace {
 
-constexpr int kStages = 12;
-constexpr int kSlots = 16;
+// Two CTAs per SM: one tcgen05 issue stream per CTA serialises on MMA latency,
+// two overlap and keep the stream at the HBM rate.
+constexpr int kCtasPerSm = 2;
+constexpr int kStages = 6;
+constexpr int kSlots = 8;
 constexpr int kSlotCols = 16;
-constexpr int kTmemCols = 256;
+constexpr int kTmemCols = 128;
 constexpr int kStageBytes = kBk * kDI * 2;   // 16 KiB
 constexpr int kQTileBytes = 16 * kDI * 2;    // 2 KiB: 16 rows (HI used) x 64
 constexpr int kThreads = 192;
@@ -51,6 +56,14 @@ struct Params {
   int64_t cs0, cs1;
   int nb_stride;
   int32_t* dev_err;
+  // optional fused selection (a2) and page table (a3)
+  int k;
+  int32_t* sel;
+  int32_t* count;
+  int32_t* pt;
+  int32_t* n_out;
+  int32_t* last_len;
+  int32_t* counter;
 };
 
 struct Walker {  // position in the flattened (b, g, j) item space
@@ -81,7 +94,91 @@ __device__ __forceinline__ void walk_next(Walker& w, const int* own, int B, int 
   do { ++w.b; } while (w.b < B && own[w.b] == 0);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// Block-wide maximum of a uint64 over the kThreads threads of the CTA.
+__device__ __forceinline__ uint64_t block_max_u64(uint64_t v, uint64_t* s_w) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  v = warp_max_u64(v);
+  if (lane == 0) s_w[wid] = v;
+  __syncthreads();
+  if (wid == 0) {
+    uint64_t x = lane < kThreads / 32 ? s_w[lane] : 0ull;
+    x = warp_max_u64(x);
+    if (lane == 0) s_w[kThreads / 32] = x;
+  }
+  __syncthreads();
+  const uint64_t r = s_w[kThreads / 32];
+  __syncthreads();
+  return r;
+}
+
+// Writes the selection (a2) and, if requested, the page-table row (a3) of
+// decode row (b, g): own block + the k-1 best earlier blocks by (score desc,
+// index asc), ascending, -1 padded.  `valid` is false for a sequence whose
+// length failed the checks (count 0).  All threads of the CTA call this.
+__device__ void emit_row(const Params& p, int b, int g, int own, bool valid, const int* picks, int m_picked) {
+  const int r = b * p.Hkv + g;
+  const int tid = threadIdx.x;
+  const int cnt = valid ? m_picked + 1 : 0;
+  // entries from m_picked on: the own block, then -1 padding
+  for (int x = m_picked + tid; x < p.k; x += kThreads) {
+    const int j = (x == m_picked && valid) ? own : -1;
+    p.sel[static_cast<int64_t>(r) * p.k + x] = j;
+    if (p.pt != nullptr) p.pt[static_cast<int64_t>(r) * p.k + x] = j >= 0 ? p.seq_pt[b * p.max_pages + j] : -1;
+  }
+  // the picks, each placed at its rank in ascending order
+  for (int t = tid; t < m_picked; t += kThreads) {
+    const int jt = picks[t];
+    int pos = 0;
+    for (int y = 0; y < m_picked; ++y) pos += picks[y] < jt;
+    p.sel[static_cast<int64_t>(r) * p.k + pos] = jt;
+    if (p.pt != nullptr) p.pt[static_cast<int64_t>(r) * p.k + pos] = p.seq_pt[b * p.max_pages + jt];
+  }
+  if (tid == 0) {
+    p.count[r] = cnt;
+    if (p.pt != nullptr) {
+      p.n_out[r] = cnt;
+      const int L = p.seq_len[b];
+      p.last_len[r] = valid ? L - p.Bk * own : 0;
+    }
+  }
+}
+
+// Exact top-(k-1) of the own_b earlier blocks of row (b, g), by m rounds of a
+// block-wide arg-max below the previous pick; candidate keys are staged in
+// shared memory when they fit, else re-read from C (L2) every round.
+__device__ void select_row(const Params& p, int b, int g, int own, uint64_t* s_keys, int key_cap, uint64_t* s_w,
+                           int* s_picks) {
+  const int m = p.k - 1;
+  if (own <= m) {
+    for (int x = threadIdx.x; x < own; x += kThreads) s_picks[x] = x;
+    __syncthreads();
+    emit_row(p, b, g, own, true, s_picks, own);
+    __syncthreads();
+    return;
+  }
+  const float* crow = p.C + b * p.cs0 + g * p.cs1;
+  const bool staged = own <= key_cap;
+  if (staged) {
+    for (int j = threadIdx.x; j < own; j += kThreads) s_keys[j] = select_key(__ldcg(crow + j), j);
+    __syncthreads();
+  }
+  uint64_t prev = ~0ull;
+  for (int t = 0; t < m; ++t) {
+    uint64_t best = 0;
+    for (int j = threadIdx.x; j < own; j += kThreads) {
+      const uint64_t key = staged ? s_keys[j] : select_key(__ldcg(crow + j), j);
+      if (key < prev && key > best) best = key;
+    }
+    best = block_max_u64(best, s_w);
+    prev = best;
+    if (threadIdx.x == 0) s_picks[t] = select_key_index(best);
+  }
+  __syncthreads();
+  emit_row(p, b, g, own, true, s_picks, m);
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
 index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -154,6 +251,25 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
       if (j >= s_own[b]) p.C[b * p.cs0 + g * p.cs1 + j] = -INFINITY;
     }
   }
+  if (p.sel != nullptr && blockIdx.x == 0) {
+    // rows with nothing to score: own block only (or nothing for a bad length)
+    for (int r = tid; r < p.B * p.Hkv; r += kThreads) {
+      const int b = r / p.Hkv;
+      if (s_own[b] != 0) continue;
+      const int L = p.seq_len[b];
+      const bool valid = L >= 1 && static_cast<int64_t>(L) <= p.max_pages * p.Bk && (L - 1) / p.Bk < p.nb_stride;
+      for (int x = 0; x < p.k; ++x) {
+        const int j = (valid && x == 0) ? 0 : -1;
+        p.sel[static_cast<int64_t>(r) * p.k + x] = j;
+        if (p.pt != nullptr) p.pt[static_cast<int64_t>(r) * p.k + x] = j >= 0 ? p.seq_pt[b * p.max_pages] : -1;
+      }
+      p.count[r] = valid ? 1 : 0;
+      if (p.pt != nullptr) {
+        p.n_out[r] = valid ? 1 : 0;
+        p.last_len[r] = valid ? L : 0;
+      }
+    }
+  }
 
   const int64_t total_items = s_pre[p.B];
   const int64_t per_cta = (total_items + gridDim.x - 1) / gridDim.x;
@@ -163,30 +279,44 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
 
   if (warp == 0) {
     // ===================== TMA producer =====================
-    if (lane == 0 && count > 0) {
-      Walker it;
-      walk_init(it, lo, s_pre, s_own, p.B, p.Hkv);
-      int issued = 0;
-      for (int n = 0; n < count; ++n) {
-        const int st = n % kStages;
-        const uint32_t ph = (n / kStages) & 1;
-        if (!mbar_wait(&bar_empty[st], ph ^ 1, abort_flag, p.dev_err)) break;
-        const int64_t page = p.seq_pt[it.b * p.max_pages + it.j];
-        if (page < 0 || page >= p.num_pages) {
-          mbar_arrive(&bar_full[st]);   // nothing to load; the epilogue reports the bad page
-        } else {
-          mbar_arrive_expect_tx(&bar_full[st], kStageBytes);
-          tma_load_4d(s_stage + st * kStageBytes, &kmap, &bar_full[st], 0, 0, it.g, static_cast<int>(page));
-        }
-        ++issued;
-        walk_next(it, s_own, p.B, p.Hkv);
+    // The page ids of the next 32 items are loaded by the 32 lanes at once, so
+    // the TMA issue loop of lane 0 never waits on a global load.
+    int issued = 0;
+    bool ok = true;
+    for (int base = 0; base < count && ok; base += 32) {
+      const int nb = min(32, count - base);
+      Walker w;
+      int64_t page = -1;
+      if (lane < nb) {
+        walk_init(w, lo + base + lane, s_pre, s_own, p.B, p.Hkv);
+        page = p.seq_pt[w.b * p.max_pages + w.j];
       }
-      if (*abort_flag) {  // drain loads still in flight before the CTA exits
-        for (int n = max(0, issued - kStages); n < issued; ++n) {
-          uint64_t t0 = global_timer_ns();
-          while (!mbar_try_wait(&bar_full[n % kStages], (n / kStages) & 1) &&
-                 global_timer_ns() - t0 < MSA_WAIT_LIMIT_NS) {
+      for (int i = 0; i < nb; ++i) {
+        const int64_t pg = __shfl_sync(0xffffffffu, page, i);
+        const int g = __shfl_sync(0xffffffffu, w.g, i);
+        if (lane == 0) {
+          const int n = base + i;
+          const int st = n % kStages;
+          ok = mbar_wait(&bar_empty[st], ((n / kStages) & 1) ^ 1, abort_flag, p.dev_err);
+          if (ok) {
+            if (pg < 0 || pg >= p.num_pages) {
+              mbar_arrive(&bar_full[st]);   // nothing to load; the epilogue reports the bad page
+            } else {
+              mbar_arrive_expect_tx(&bar_full[st], kStageBytes);
+              tma_load_4d(s_stage + st * kStageBytes, &kmap, &bar_full[st], 0, 0, g, static_cast<int>(pg));
+            }
+            ++issued;
           }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+      }
+    }
+    if (lane == 0 && *abort_flag) {  // drain loads still in flight before the CTA exits
+      for (int n = max(0, issued - kStages); n < issued; ++n) {
+        uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(&bar_full[n % kStages], (n / kStages) & 1) &&
+               global_timer_ns() - t0 < MSA_WAIT_LIMIT_NS) {
         }
       }
     }
@@ -316,6 +446,81 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+
+  // ---- fused selection: the CTA whose scores complete a (b, g) row selects it ----
+  if (p.sel != nullptr && !*abort_flag && count > 0) {
+    __shared__ int s_rows[kThreads], s_long[kThreads];
+    __shared__ int s_nrows, s_nlong;
+    __shared__ uint64_t s_w[kThreads / 32 + 1];
+    __shared__ int s_picks[kThreads / 32][kMaxK];
+    __shared__ int s_out[kThreads / 32][kMaxK];
+    uint8_t* ring = s_stage;                          // the TMA ring is idle now
+    uint64_t* s_surv = reinterpret_cast<uint64_t*>(ring);                  // [warps][kSelCap]
+    uint64_t* s_keys = reinterpret_cast<uint64_t*>(ring + (kThreads / 32) * kSelCap * 8);
+    const int key_cap = (kStages * kStageBytes - (kThreads / 32) * kSelCap * 8) / 8;
+    const int m = p.k - 1;
+    __threadfence();                                   // this CTA's scores, device-wide
+    // this CTA's items cover the contiguous rows r_first .. r_last
+    Walker wf, wl;
+    walk_init(wf, lo, s_pre, s_own, p.B, p.Hkv);
+    walk_init(wl, hi - 1, s_pre, s_own, p.B, p.Hkv);
+    const int r_first = wf.b * p.Hkv + wf.g, r_last = wl.b * p.Hkv + wl.g;
+    for (int base = r_first; base <= r_last; base += kThreads) {
+      if (tid == 0) { s_nrows = 0; s_nlong = 0; }
+      __syncthreads();
+      const int r = base + tid;
+      if (r <= r_last) {
+        const int b = r / p.Hkv, g = r % p.Hkv;
+        const int own = s_own[b];
+        const int64_t row_start = s_pre[b] + static_cast<int64_t>(g) * own;
+        const int64_t mine64 = min(row_start + own, hi) - max(row_start, lo);
+        if (own > 0 && mine64 > 0) {
+          const int mine = static_cast<int>(mine64);
+          if (atomicAdd(&p.counter[r], mine) + mine == own) {   // this CTA completed row r
+            if (own <= 2048 || own <= m) s_rows[atomicAdd(&s_nrows, 1)] = r;
+            else s_long[atomicAdd(&s_nlong, 1)] = r;
+          }
+        }
+      }
+      __syncthreads();
+      __threadfence();                                 // scores written by other CTAs
+      // short rows: one warp per row
+      for (int x = warp; x < s_nrows; x += kThreads / 32) {
+        const int rr = s_rows[x];
+        const int b = rr / p.Hkv, g = rr % p.Hkv;
+        const int own = s_own[b];
+        const float* crow = p.C + b * p.cs0 + g * p.cs1;
+        int* out = s_out[warp];
+        int npick = own;
+        if (own <= m) {
+          for (int y = lane; y < own; y += 32) out[y] = y;
+        } else {
+          warp_select_any(crow, own, m, s_surv + warp * kSelCap, s_picks[warp], out);
+          npick = m;
+        }
+        __syncwarp();
+        for (int y = lane; y < p.k; y += 32) {
+          const int j = y < npick ? out[y] : (y == npick ? own : -1);
+          p.sel[static_cast<int64_t>(rr) * p.k + y] = j;
+          if (p.pt != nullptr) p.pt[static_cast<int64_t>(rr) * p.k + y] = j >= 0 ? p.seq_pt[b * p.max_pages + j] : -1;
+        }
+        if (lane == 0) {
+          p.count[rr] = npick + 1;
+          if (p.pt != nullptr) {
+            p.n_out[rr] = npick + 1;
+            p.last_len[rr] = p.seq_len[b] - p.Bk * own;
+          }
+        }
+        __syncwarp();
+      }
+      // long rows: the whole CTA
+      for (int x = 0; x < s_nlong; ++x) {
+        const int rr = s_long[x];
+        select_row(p, rr / p.Hkv, rr % p.Hkv, s_own[rr / p.Hkv], s_keys, key_cap, s_w, s_picks[0]);
+      }
+      __syncthreads();
+    }
+  }
 }
 
 }  // namespace
@@ -343,13 +548,19 @@ msa_status launch_index_decode(const msa_index_args& a, cudaStream_t stream) {
   p.num_pages = a.num_pages; p.seq_pt = a.seq_pt; p.max_pages = a.max_pages; p.seq_len = a.seq_len;
   p.C = a.C; p.cs0 = a.C_stride[0]; p.cs1 = a.C_stride[1]; p.nb_stride = a.nb_stride;
   p.dev_err = a.dev_err;
+  p.k = a.k; p.sel = a.sel; p.count = a.count; p.pt = a.pt; p.n_out = a.n; p.last_len = a.last_len;
+  p.counter = a.row_scratch;
 
   const size_t smem = 1024 + kStages * kStageBytes + 2 * kQTileBytes + (2 * static_cast<size_t>(a.B) + 1) * 4;
   if (smem > dev.max_smem_optin) return fail(MSA_ERR_UNSUPPORTED, "decode index score: batch too large for shared memory");
   cudaError_t e = cudaFuncSetAttribute(index_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(index_decode)");
-  const int grid = dev.num_sms;
+  if (p.sel != nullptr) {
+    e = cudaMemsetAsync(p.counter, 0, static_cast<size_t>(a.B) * a.Hkv * sizeof(int32_t), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(index row counters)");
+  }
+  const int grid = dev.num_sms * kCtasPerSm;
   index_decode_kernel<<<grid, kThreads, smem, stream>>>(kmap, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "index_decode_kernel launch");

@@ -39,7 +39,8 @@ msa_status launch_page_table(const int32_t* sel, const int32_t* count, const int
                              int64_t max_pages, const int32_t* seq_len, int B, int Hkv, int k, int Bk,
                              int32_t* pt, int32_t* n, int32_t* last_len, int32_t* dev_err,
                              cudaStream_t stream);
-msa_status launch_attn_decode(const msa_decode_args& a, float* o_part, float* lse_part, cudaStream_t stream);
+msa_status launch_attn_decode(const msa_decode_args& a, float* o_part, float* lse_part, int32_t* counter,
+                              cudaStream_t stream);
 msa_status launch_lse_merge(const float* o_part, const float* lse_part, int64_t rows, int parts, int D,
                             void* O, float* LSE, int32_t* dev_err, cudaStream_t stream);
 msa_status launch_lse_merge_bf16(const __nv_bfloat16* o_part, const float* lse_part, int64_t rows, int parts, int D,

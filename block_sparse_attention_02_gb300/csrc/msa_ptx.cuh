@@ -209,6 +209,27 @@ __device__ __forceinline__ uint32_t float_order_key(float f) {
 __device__ __forceinline__ float float_from_order_key(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
+// Selection keys: score desc, then block index asc, as one uint64 (larger =
+// better).  NaN ranks below every number and -0 equals +0.
+__device__ __forceinline__ uint32_t score_order_key(float f) {
+  if (f != f) return 0u;
+  return float_order_key(f);
+}
+__device__ __forceinline__ uint64_t select_key(float score, int j) {
+  return (static_cast<uint64_t>(score_order_key(score)) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(j));
+}
+__device__ __forceinline__ int select_key_index(uint64_t key) {
+  return static_cast<int>(~static_cast<uint32_t>(key & 0xffffffffu));
+}
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t x = __shfl_xor_sync(0xffffffffu, v, o);
+    v = x > v ? x : v;
+  }
+  return v;
+}
+
 // Warp-wide maximum of a uint32 in one instruction.
 __device__ __forceinline__ uint32_t redux_max_u32(uint32_t v) {
   uint32_t r;

@@ -11,46 +11,24 @@
 // the composite key (key << 32 | ~j) makes every candidate distinct, so the
 // selected set is unique.
 //
-// Short rows (<= 32 * NPL candidates, all prefill rows and short decode rows):
-// one warp per row, candidates in registers.  A threshold T0 = the m-th largest
-// of the 32 lane maxima (m = k-1 <= 32) is a lower bound of the m-th largest
-// key, so every selected candidate has key >= T0.  The survivors (usually a
-// few dozen) are compacted in index order into shared memory and ranked
-// exactly; more than kCap survivors (massive ties) take an exact successive
-// arg-max over the registers instead.
+// Short rows (<= 2048 candidates: all prefill rows and short decode rows): one
+// warp per row, the register algorithm of select_warp.cuh.
 // Long decode rows: one 256-thread CTA per row, successive block-wide arg-max.
 #include "msa_internal.h"
 #include "msa_ptx.cuh"
+#include "select_warp.cuh"
 
 namespace msa {
 namespace {
 
 constexpr int kWarpsPerCta = 8;
-constexpr int kCap = 128;          // survivors ranked in shared memory per warp
 constexpr int kCtaThreads = 256;
 
-__device__ __forceinline__ uint32_t order_key(float f) {
-  if (f != f) return 0u;           // NaN below everything
-  f = f + 0.0f;                    // -0 -> +0
-  uint32_t u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
+__device__ __forceinline__ uint32_t order_key(float f) { return score_order_key(f); }
 __device__ __forceinline__ uint64_t comp_key(uint32_t u, int j) {
   return (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(j));
 }
-__device__ __forceinline__ int comp_index(uint64_t K) {
-  return static_cast<int>(~static_cast<uint32_t>(K & 0xffffffffu));
-}
-
-__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    uint64_t x = __shfl_xor_sync(0xffffffffu, v, o);
-    v = x > v ? x : v;
-  }
-  return v;
-}
+__device__ __forceinline__ int comp_index(uint64_t K) { return select_key_index(K); }
 
 struct RowInfo {
   const float* c;     // score row
@@ -89,8 +67,9 @@ __device__ __forceinline__ void write_all(const RowInfo& r, int k, int lane_or_t
 template <int NPL>
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
 topk_warp_kernel(const msa_topk_args a, int64_t rows) {
-  __shared__ uint64_t s_surv[kWarpsPerCta][kCap];
+  __shared__ uint64_t s_surv[kWarpsPerCta][kSelCap];
   __shared__ int s_pick[kWarpsPerCta][kMaxK];
+  __shared__ int s_out[kWarpsPerCta][kMaxK];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + wid;
   if (row >= rows) return;
@@ -102,93 +81,9 @@ topk_warp_kernel(const msa_topk_args a, int64_t rows) {
     write_all(r, a.k, lane, 32);
     return;
   }
-  uint32_t u[NPL];
-  uint32_t lmax = 0;
-#pragma unroll
-  for (int i = 0; i < NPL; ++i) {
-    const int j = lane + 32 * i;
-    u[i] = (j < n) ? order_key(r.c[j]) : 0u;
-    lmax = max(lmax, u[i]);
-  }
-  // T0 = m-th largest lane maximum (bitonic sort, descending over lanes)
-  uint32_t T0 = 0;
-  if (m <= 32) {
-    uint32_t v = lmax;
-#pragma unroll
-    for (int kk = 2; kk <= 32; kk <<= 1) {
-#pragma unroll
-      for (int jj = kk >> 1; jj > 0; jj >>= 1) {
-        const uint32_t o = __shfl_xor_sync(0xffffffffu, v, jj);
-        const bool desc = (lane & kk) == 0;
-        const bool lower = (lane & jj) == 0;
-        v = (lower == desc) ? max(v, o) : min(v, o);
-      }
-    }
-    T0 = __shfl_sync(0xffffffffu, v, m - 1);
-  }
-  // compact survivors (key >= T0) in index order
-  int c = 0;
-#pragma unroll
-  for (int i = 0; i < NPL; ++i) {
-    const int j = lane + 32 * i;
-    const bool f = (j < n) && u[i] >= T0;
-    const uint32_t mask = __ballot_sync(0xffffffffu, f);
-    const int pos = c + __popc(mask & ((1u << lane) - 1u));
-    if (f && pos < kCap) s_surv[wid][pos] = comp_key(u[i], j);
-    c += __popc(mask);
-  }
-  __syncwarp();
-  int out = 0;
-  if (c <= kCap) {
-    // exact rank of every survivor; the m best have rank < m
-    for (int base = 0; base < c; base += 32) {
-      const int x = base + lane;
-      bool pick = false;
-      int jx = 0;
-      if (x < c) {
-        const uint64_t Kx = s_surv[wid][x];
-        int rank = 0;
-        for (int y = 0; y < c; ++y) rank += s_surv[wid][y] > Kx;
-        pick = rank < m;
-        jx = comp_index(Kx);
-      }
-      const uint32_t mask = __ballot_sync(0xffffffffu, pick);
-      if (pick) r.sel[out + __popc(mask & ((1u << lane) - 1u))] = jx;
-      out += __popc(mask);
-    }
-  } else {
-    // exact fallback: m rounds of arg-max below the previous pick
-    uint64_t prev = ~0ull;
-    for (int t = 0; t < m; ++t) {
-      uint64_t best = 0;
-#pragma unroll
-      for (int i = 0; i < NPL; ++i) {
-        const int j = lane + 32 * i;
-        if (j < n) {
-          const uint64_t K = comp_key(u[i], j);
-          if (K < prev && K > best) best = K;
-        }
-      }
-      best = warp_max_u64(best);
-      prev = best;
-      if (lane == 0) s_pick[wid][t] = comp_index(best);
-    }
-    __syncwarp();
-    // ascending order by counting
-    for (int t = lane; t < m; t += 32) {
-      const int jt = s_pick[wid][t];
-      int pos = 0;
-      for (int y = 0; y < m; ++y) pos += s_pick[wid][y] < jt;
-      r.sel[pos] = jt;
-    }
-    out = m;
-  }
-  if (lane == 0) {
-    r.sel[m] = n;          // own block, the largest selected index
-    *r.cnt = m + 1;
-  }
-  for (int x = m + 1 + lane; x < a.k; x += 32) r.sel[x] = -1;
-  (void)out;
+  warp_select<NPL>(r.c, n, m, s_surv[wid], s_pick[wid], s_out[wid]);
+  for (int x = lane; x < a.k; x += 32) r.sel[x] = x < m ? s_out[wid][x] : (x == m ? n : -1);
+  if (lane == 0) *r.cnt = m + 1;
 }
 
 // One CTA per long row: m rounds of block-wide arg-max below the previous pick.

@@ -115,6 +115,13 @@ const char *msa_status_string(msa_status s);
  *   MSA_DEVERR_BAD_PAGE is raised.  A sequence whose length is outside
  *   [1, max_pages * Bk], or whose own block is not below nb_stride, is not
  *   scored (its row stays -inf) and raises MSA_DEVERR_BAD_LEN.
+ * DECODE, fused selection (optional): when `sel` is non-NULL the same kernel
+ *   also performs a2 (exactly what msa_topk_blocks computes with this k) on
+ *   each (b, g) row as soon as the row's scores are complete, and when `pt` is
+ *   also non-NULL a3 (exactly what msa_build_page_table computes).  This saves
+ *   two launches per decode step.  `row_scratch` is then required: B*Hkv int32
+ *   of caller scratch, cleared by the call.  Outputs are those of a2 / a3:
+ *   sel [B,Hkv,k], count [B,Hkv], pt [B*Hkv,k], n and last_len [B*Hkv].
  * ------------------------------------------------------------------------ */
 typedef struct msa_index_args {
     msa_mode mode;
@@ -133,6 +140,14 @@ typedef struct msa_index_args {
     int64_t C_stride[3];
     int nb_stride;
     int32_t *dev_err;
+    /* decode, optional fused a2/a3 outputs (NULL = scores only) */
+    int k;
+    int32_t *sel;
+    int32_t *count;
+    int32_t *pt;
+    int32_t *n;
+    int32_t *last_len;
+    int32_t *row_scratch;
 } msa_index_args;
 
 msa_status msa_index_score(const msa_index_args *args, msa_stream_t stream);
@@ -236,13 +251,15 @@ msa_status msa_sparse_attn_prefill(const msa_prefill_args *args, void *ws, size_
  * heads of group g attend to the first n[r] pages, the last of which holds
  * last_len[r] valid tokens ([serving], "MSA con paged attention").  Each
  * (row, page) pair is an independent split of the softmax; the partials go to
- * the workspace and are combined by the log-sum-exp merge.
+ * the workspace and the CTA that finishes a row's last split combines them with
+ * the log-sum-exp merge.
  *     Q [B, Hq, D] bf16 strides (b, h); K_pool, V_pool [num_pages, Hkv, Bk, D]
  *     bf16 with common strides kv_stride = (page, g, t);
  *     pt [B*Hkv, k], n [B*Hkv], last_len [B*Hkv] int32;
  *     O [B, Hq, D] bf16 (dense), LSE [B, Hq] fp32 (dense).
  * Workspace: msa_sparse_attn_decode_workspace_size(args) bytes (fp32 partial
- * outputs and LSEs, B*Hq*k*(D+1)*4 bytes).  Page ids outside [0, num_pages)
+ * outputs and LSEs and one counter per row: B*Hq*k*(D+1)*4 + B*Hkv*4 + 256
+ * bytes); the call clears the counters itself.  Page ids outside [0, num_pages)
  * are skipped (MSA_DEVERR_BAD_PAGE).  softmax_scale <= 0 selects 1/sqrt(D).
  * ------------------------------------------------------------------------ */
 typedef struct msa_decode_args {
@@ -278,15 +295,15 @@ msa_status msa_sparse_attn_decode(const msa_decode_args *args, void *ws, size_t 
  * MSA_NOALLOC_SCRATCH_BYTES that is part of the library's device image and
  * stays resident on every device that loads the library until the process
  * exits.  It allocates nothing and frees nothing.
- *   - Sizes whose scratch, B*Hq*k*(D+1)*4 + 256 bytes, exceeds the array are
+ *   - Sizes whose scratch, B*Hq*k*(D+1)*4 + B*Hkv*4 + 256 bytes, exceeds the array are
  *     rejected with MSA_ERR_WORKSPACE and a message; use msa_sparse_attn_decode
  *     with a workspace for those.
  *   - The first call on a device looks up the array's device address with that
  *     device current; make that first call before any stream capture.
  *   - All calls share the array, which keeps the last call's contents.  Calls
  *     whose kernels overlap on the GPU (other streams, other host threads)
- *     race on it: serialise them.  Nothing needs clearing between calls, since
- *     every value the merge reads is written by the same call first.
+ *     race on it: serialise them.  Each call clears the per-row counters it
+ *     needs and writes every partial the merge reads before reading it.
  * ------------------------------------------------------------------------ */
 #define MSA_NOALLOC_SCRATCH_BYTES (32u << 20)
 

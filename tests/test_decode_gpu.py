@@ -30,8 +30,8 @@ def msa():
     return m
 
 
-def run_gpu(msa, inp, k):
-    bufs = msa.decode_step(inp, k)
+def run_gpu(msa, inp, k, fused=True):
+    bufs = msa.decode_step(inp, k, fused=fused)
     torch.cuda.synchronize()
     assert int(bufs["dev_err"].item()) == 0, f"device error word {int(bufs['dev_err'].item()):#x}"
     return {n: t.cpu() for n, t in bufs.items() if n != "ws"}
@@ -172,3 +172,23 @@ def test_standalone_lse_merge(msa):
     np.testing.assert_allclose(O.float().cpu().numpy(), Oo, atol=1e-2, rtol=1e-2)
     np.testing.assert_allclose(L.cpu().numpy()[fin], Lo[fin], atol=1e-4)
     assert torch.all(O[7] == 0)
+
+
+@pytest.mark.parametrize("wl", SMALL[:3] + [workload("decode_b8_l60001")], ids=lambda w: w.name)
+def test_fused_selection_equals_standalone_entry_points(msa, wl):
+    """a2/a3 fused into the index-score call give the same bits as msa_topk_blocks + msa_build_page_table."""
+    inp = decode_inputs(wl, device="cuda")
+    f = run_gpu(msa, inp, wl.shape.k, fused=True)
+    u = run_gpu(msa, inp, wl.shape.k, fused=False)
+    for n in ("C", "sel", "count", "pt", "n", "last_len", "O", "LSE"):
+        assert torch.equal(f[n], u[n]), n
+
+
+def test_decode_b1_l1048576_unfused(msa):
+    """The standalone top-k (CTA per long row) and page table at 1M tokens."""
+    wl = workload("decode_b1_l1048576")
+    inp = decode_inputs(wl, device="cuda")
+    f = run_gpu(msa, inp, wl.shape.k, fused=True)
+    u = run_gpu(msa, inp, wl.shape.k, fused=False)
+    for n in ("sel", "count", "pt", "n", "last_len"):
+        assert torch.equal(f[n], u[n]), n
