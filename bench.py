@@ -474,7 +474,7 @@ def main():
     ap.add_argument("--workload", default="decode_b8_l60001")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
-    ap.add_argument("--prefill-chunk", type=int, default=16384)
+    ap.add_argument("--prefill-chunk", type=int, default=8192)
     ap.add_argument("--seq", type=int, default=None, help="override the prefill sequence length (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -29,7 +29,8 @@
 namespace msa {
 namespace {
 
-constexpr int kAttnThreads = 288;     // w0-3 Q gather + K/V TMA, w4-7 softmax/epilogue, w8 MMA
+constexpr int kAttnThreads = 352;     // w0-1 Q gather + K/V TMA, w2-5 and w6-9 softmax/epilogue, w10 MMA
+constexpr int kMmaWarp = 10;
 constexpr int kHalf = 128 * 64 * 2;   // 16 KiB
 constexpr int kQStage = 2 * kHalf;    // 32 KiB: 128 rows x 128 (Q, then P)
 constexpr int kKV = 4 * kHalf;        // 64 KiB: K (2 halves) + V (2 halves)
@@ -183,6 +184,40 @@ __device__ __forceinline__ int64_t find_item(const AttnParams& p, int64_t t) {
   return lo;
 }
 
+// packed fp32 helpers and the hardware base-2 exponential
+__device__ __forceinline__ uint64_t pack2f(float x, float y) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+  return r;
+}
+__device__ __forceinline__ void unpack2f(uint64_t v, float& x, float& y) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(v));
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h2 = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h2);
+}
+
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool full) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(full ? 16 : 0)
                : "memory");
@@ -205,24 +240,25 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   __shared__ __align__(8) uint64_t bar_sfull[2], bar_pready[2], bar_ofull[2], bar_tfree[2], bar_drain;
   __shared__ TileInfo s_info[2];
   __shared__ const __nv_bfloat16* s_rowsrc[2][128];
+  __shared__ int2 s_rinfo[2][128];         // per tile row: query position i, partial row (-1: padding)
   __shared__ uint32_t s_tmem;
-  __shared__ int s_abort, s_fail, s_gfail[2];
+  __shared__ int s_abort, s_fail[2], s_gfail[2];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar_qfull[i], 64); mbar_init(&bar_qempty[i], 1);
+      mbar_init(&bar_qfull[i], 32); mbar_init(&bar_qempty[i], 1);
       mbar_init(&bar_kvfull[i], 1); mbar_init(&bar_kvempty[i], 1);
       mbar_init(&bar_sfull[i], 1); mbar_init(&bar_pready[i], 4);
       mbar_init(&bar_ofull[i], 1); mbar_init(&bar_tfree[i], 4);
     }
     mbar_init(&bar_drain, 1);
     s_abort = 0;
-    s_fail = 0;
+    s_fail[0] = s_fail[1] = 0;
     s_gfail[0] = s_gfail[1] = 0;
     fence_mbar_init();
   }
-  if (warp == 8) tmem_alloc(&s_tmem, kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(&s_tmem, kTmemCols);
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
@@ -234,16 +270,14 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   const int64_t t1 = min(total_tiles, t0 + per);
   const int ntiles = static_cast<int>(t1 - t0);
 
-  if (warp < 4) {
-    // ===================== producers: group gi owns Q stage gi (tiles n = gi mod 2) =====================
-    // Each group gathers its tile, waits for its own copies, fences them for the
-    // tensor core and releases the stage; the two groups keep two gathers in flight.
-    const int gi = warp >> 1;
-    const int l64 = tid - gi * 64;
-    const bool leader = l64 == 0;
+  if (warp < 2) {
+    // ===================== producers: warp gi owns Q stage gi (tiles n = gi mod 2) =====================
+    // Each warp resolves its tile's rows (query, head, slot), gathers the Q rows,
+    // waits for its own copies, fences them for the tensor core and releases the
+    // stage; the two warps keep two gathers in flight.
+    const int gi = warp;
     int64_t prev_item = -1;
-    int kvn = 0, last_kv = -1;   // last K/V load issued by this group's leader
-    bool ok = true;
+    int kvn = 0, last_kv = -1;   // last K/V load issued by this warp
     // tiles of this CTA are contiguous: walk their items forward instead of searching
     int64_t item = ntiles > 0 ? find_item(p, t0) : 0;
     for (int n = 0; n < ntiles; ++n) {
@@ -262,7 +296,27 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       const int row0 = static_cast<int>(t - p.tile_off[item]) * 128;
       const int nrows = min(128, rows_item - row0);
       const int kvb = (kvn - 1) & 1;
-      if (leader) {
+      // rows of this tile (4 per lane), resolved before waiting for the stage
+      const __nv_bfloat16* src[4];
+      int2 ri[4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const int rr = lane + 32 * x;
+        src[x] = nullptr;
+        ri[x] = make_int2(0, -1);
+        if (rr < nrows) {
+          const int rho = row0 + rr;
+          const int ent = p.list[ebase + rho / p.G];
+          const int qi = ent >> 6;
+          const int hq = g * p.G + rho % p.G;
+          const int i = static_cast<int>((p.q0 + qi) % p.S);
+          src[x] = p.Q + static_cast<int64_t>(b) * p.qs0 + static_cast<int64_t>(i) * p.qs1 +
+                   static_cast<int64_t>(hq) * p.qs2;
+          ri[x] = make_int2(i, (qi * p.Hq + hq) * p.k + (ent & 63));
+        }
+      }
+      bool ok = true;
+      if (lane == 0) {
         const bool release = (n + 1 == ntiles) || p.tile_off[item + 1] <= t + 1;
         ok = mbar_wait(&bar_qempty[st], ((n >> 1) & 1) ^ 1, abort_flag, p.dev_err);
         if (ok && kv_new) {
@@ -279,45 +333,37 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         }
         s_info[st] = TileInfo{static_cast<int>(item), b, g, j, row0, nrows, kvb, kv_new ? 1 : 0, release ? 1 : 0,
                               ebase};
-        if (!ok) s_gfail[gi] = 1;
       }
-      // source row pointers of this tile (2 rows per lane of the group)
-      for (int rr = l64; rr < 128; rr += 64) {
-        const __nv_bfloat16* src = nullptr;
-        if (rr < nrows) {
-          const int rho = row0 + rr;
-          const int ent = p.list[ebase + rho / p.G];
-          const int64_t bs = p.q0 + (ent >> 6);
-          const int i = static_cast<int>(bs % p.S);
-          src = p.Q + static_cast<int64_t>(b) * p.qs0 + static_cast<int64_t>(i) * p.qs1 +
-                static_cast<int64_t>(g * p.G + rho % p.G) * p.qs2;
-        }
-        s_rowsrc[st][rr] = src;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;                      // the warp stops together
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        s_rowsrc[st][lane + 32 * x] = src[x];
+        s_rinfo[st][lane + 32 * x] = ri[x];
       }
-      named_bar_sync(2 + gi, 64);
-      if (s_gfail[gi]) break;     // the whole group stops together
+      __syncwarp();
       const uint32_t qbase = smem_u32(s_q + st * kQStage);
-#pragma unroll 4
-      for (int u = 0; u < 32; ++u) {
-        const int idx = l64 + 64 * u;     // 2048 chunks of 16 B
+#pragma unroll 8
+      for (int u = 0; u < 64; ++u) {
+        const int idx = lane + 32 * u;     // 2048 chunks of 16 B
         const int rr = idx >> 4, c = idx & 15;
-        const __nv_bfloat16* src = s_rowsrc[st][rr];
+        const __nv_bfloat16* sp = s_rowsrc[st][rr];
         const uint32_t dst = qbase + (c >> 3) * kHalf + sw128_offset(rr, c & 7);
-        cp_async16(dst, src ? static_cast<const void*>(src + c * 8) : static_cast<const void*>(p.Q), src != nullptr);
+        cp_async16(dst, sp ? static_cast<const void*>(sp + c * 8) : static_cast<const void*>(p.Q), sp != nullptr);
       }
       cp_async_commit();
       cp_async_wait<0>();
       fence_proxy_async_smem();
       mbar_arrive(&bar_qfull[st]);
-      named_bar_sync(2 + gi, 64);   // s_rowsrc[st] is rewritten two tiles later
+      __syncwarp();                        // s_rowsrc[st] is rewritten two tiles later
     }
-    if (*abort_flag && leader && last_kv >= 0) {   // let this group's last K/V load land
+    if (*abort_flag && lane == 0 && last_kv >= 0) {   // let this warp's last K/V load land
       uint64_t tt = global_timer_ns();
       while (!mbar_try_wait(&bar_kvfull[last_kv & 1], (last_kv >> 1) & 1) &&
              global_timer_ns() - tt < MSA_WAIT_LIMIT_NS) {
       }
     }
-  } else if (warp == 8) {
+  } else if (warp == kMmaWarp) {
     // ===================== tcgen05 issuer =====================
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
@@ -374,78 +420,123 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     }
     __syncwarp();
   } else {
-    // ===================== softmax + epilogue (warps 4-7), thread = tile row =====================
+    // ===================== softmax + epilogue: warpgroup wg (warps 2-5 / 6-9) owns tiles n = wg mod 2 =====
+    const int wg = (warp - 2) >> 2;
+    const int bar_id = 1 + wg;
     const int q = warp & 3;
-    const int r = q * 32 + lane;
+    const int r = q * 32 + lane;                     // tile row = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
-    for (int n = 0; n < ntiles; ++n) {
-      const int st = n & 1, slot = n & 1;
+    const int st = wg, slot = wg;
+    for (int n = wg; n < ntiles; n += 2) {
       const uint32_t ph = (n >> 1) & 1;
-      if (!mbar_wait(&bar_qfull[st], ph, abort_flag, p.dev_err)) s_fail = 1;
-      named_bar_sync(1, 128);
-      if (s_fail) break;
-      const TileInfo inf = s_info[st];
-      const bool valid = r < inf.nrows;
-      int qi = 0, slot_sel = 0, hq = 0, i = 0;
-      if (valid) {
-        const int rho = inf.row0 + r;
-        const int ent = p.list[inf.ebase + rho / p.G];
-        qi = ent >> 6;
-        slot_sel = ent & 63;
-        hq = inf.g * p.G + rho % p.G;
-        i = static_cast<int>((p.q0 + qi) % p.S);
-      }
+      if (!mbar_wait(&bar_qfull[st], ph, abort_flag, p.dev_err)) s_fail[wg] = 1;
+      named_bar_sync(bar_id, 128);
+      if (s_fail[wg]) break;
+      const int j = s_info[st].j;
+      const int2 ri = s_rinfo[st][r];
+      const bool valid = ri.y >= 0;
       // keys of this block visible to the row: t <= i
-      const int nvis = valid ? min(kBk, i - inf.j * kBk + 1) : kBk;
-      if (!mbar_wait(&bar_sfull[slot], ph, abort_flag, p.dev_err)) s_fail = 1;
-      named_bar_sync(1, 128);
-      if (s_fail) break;
+      const int nvis = valid ? min(kBk, ri.x - j * kBk + 1) : kBk;
+      if (!mbar_wait(&bar_sfull[slot], ph, abort_flag, p.dev_err)) s_fail[wg] = 1;
+      named_bar_sync(bar_id, 128);
+      if (s_fail[wg]) break;
       tc_fence_after();
       const uint32_t sbase = tmem + lane_addr + slot * 256;
-      float m = -INFINITY;
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t v[32];
-        tmem_ld32(sbase + cc * 32, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (cc * 32 + e < nvis) m = fmaxf(m, __uint_as_float(v[e]) * p.scale_log2);
-      }
-      float l = 0.f;
       uint8_t* prow = s_q + st * kQStage;
+      const float sc = p.scale_log2;
+      float m = -INFINITY, l = 0.f;
+      // the branch must be warp-uniform: the TMEM loads inside are warp-collective
+      if (__all_sync(0xffffffffu, nvis == kBk)) {
+        // whole block visible to every row of the warp: no masking
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t v[32];
-        tmem_ld32(sbase + cc * 32, v);
-        tmem_ld_wait();
-        uint32_t pk[16];
+        for (int half = 0; half < 2; ++half) {
+          uint32_t v[2][32];
+          tmem_ld32(sbase + half * 64, v[0]);
+          tmem_ld32(sbase + half * 64 + 32, v[1]);
+          tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float p0 = (cc * 32 + e < nvis) ? exp2f(__uint_as_float(v[e]) * p.scale_log2 - m) : 0.f;
-          const float p1 = (cc * 32 + e + 1 < nvis) ? exp2f(__uint_as_float(v[e + 1]) * p.scale_log2 - m) : 0.f;
-          l += p0 + p1;
-          __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-          pk[e >> 1] = *reinterpret_cast<uint32_t*>(&h2);
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) m = max3f(m, __uint_as_float(v[c][e]), __uint_as_float(v[c][e + 1]));
         }
-        // keys cc*32 .. cc*32+31 are chunks 4cc .. 4cc+3 of the 16-chunk row
+        m *= sc;   // scale > 0: max of scaled scores
+        uint64_t l2 = 0ull;
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const int c = cc * 4 + x;
-          *reinterpret_cast<uint4*>(prow + (c >> 3) * kHalf + sw128_offset(r, c & 7)) =
-              make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
+        for (int half = 0; half < 2; ++half) {
+          uint32_t v[2][32];
+          tmem_ld32(sbase + half * 64, v[0]);
+          tmem_ld32(sbase + half * 64 + 32, v[1]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const float p0 = fast_exp2(fmaf(__uint_as_float(v[c][e]), sc, -m));
+              const float p1 = fast_exp2(fmaf(__uint_as_float(v[c][e + 1]), sc, -m));
+              l2 = add2(l2, pack2f(p0, p1));
+              pk[e >> 1] = pack_bf16x2(p0, p1);
+            }
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              const int ch = (half * 2 + c) * 4 + x;
+              *reinterpret_cast<uint4*>(prow + (ch >> 3) * kHalf + sw128_offset(r, ch & 7)) =
+                  make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
+            }
+          }
         }
+        float la, lb;
+        unpack2f(l2, la, lb);
+        l = la + lb;
+      } else {
+        // some row of the warp sees only part of the block (its own block): keys t <= i
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t v[32];
+          tmem_ld32(sbase + cc * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (cc * 32 + e < nvis) m = fmaxf(m, __uint_as_float(v[e]));
+        }
+        m *= sc;
+        // same pairwise accumulation order as the unmasked path, so a fully
+        // visible row gets identical bits whichever path its warp takes
+        uint64_t l2 = 0ull;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t v[32];
+          tmem_ld32(sbase + cc * 32, v);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float p0 = (cc * 32 + e < nvis) ? fast_exp2(fmaf(__uint_as_float(v[e]), sc, -m)) : 0.f;
+            const float p1 = (cc * 32 + e + 1 < nvis) ? fast_exp2(fmaf(__uint_as_float(v[e + 1]), sc, -m)) : 0.f;
+            l2 = add2(l2, pack2f(p0, p1));
+            pk[e >> 1] = pack_bf16x2(p0, p1);
+          }
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const int ch = cc * 4 + x;
+            *reinterpret_cast<uint4*>(prow + (ch >> 3) * kHalf + sw128_offset(r, ch & 7)) =
+                make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
+          }
+        }
+        float la, lb;
+        unpack2f(l2, la, lb);
+        l = la + lb;
       }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_pready[slot]);
-      if (!mbar_wait(&bar_ofull[slot], ph, abort_flag, p.dev_err)) s_fail = 1;
-      named_bar_sync(1, 128);
-      if (s_fail) break;
+      if (!mbar_wait(&bar_ofull[slot], ph, abort_flag, p.dev_err)) s_fail[wg] = 1;
+      named_bar_sync(bar_id, 128);
+      if (s_fail[wg]) break;
       tc_fence_after();
       const float inv = 1.0f / l;
-      __nv_bfloat16* orow = p.o_part + ((static_cast<int64_t>(qi) * p.Hq + hq) * p.k + slot_sel) * kD;
+      __nv_bfloat16* orow = p.o_part + static_cast<int64_t>(valid ? ri.y : 0) * kD;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t v[32];
@@ -453,19 +544,20 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         tmem_ld_wait();
         if (valid) {
 #pragma unroll
+          const uint64_t inv2 = pack2f(inv, inv);
           for (int e = 0; e < 32; e += 8) {
             uint32_t w[4];
 #pragma unroll
             for (int x = 0; x < 4; ++x) {
-              __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[e + 2 * x]) * inv,
-                                                        __uint_as_float(v[e + 2 * x + 1]) * inv);
-              w[x] = *reinterpret_cast<uint32_t*>(&h2);
+              float a, b;
+              unpack2f(mul2(pack2f(__uint_as_float(v[e + 2 * x]), __uint_as_float(v[e + 2 * x + 1])), inv2), a, b);
+              w[x] = pack_bf16x2(a, b);
             }
             *reinterpret_cast<uint4*>(orow + cc * 32 + e) = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
       }
-      if (valid) p.lse_part[(static_cast<int64_t>(qi) * p.Hq + hq) * p.k + slot_sel] = (m + log2f(l)) * kLn2;
+      if (valid) p.lse_part[ri.y] = (m + log2f(l)) * kLn2;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_tfree[slot]);
@@ -474,7 +566,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -521,7 +613,7 @@ msa_status launch_attn_prefill(const msa_prefill_args& a, void* ws, size_t ws_by
   const WsLayout L = ws_layout(a, cq);
   const int64_t nb = (a.S + kBk - 1) / kBk;
   const int64_t n_items = static_cast<int64_t>(a.B) * a.Hkv * nb;
-  if (cq * 64 >= (int64_t(1) << 31) || n_items >= (int64_t(1) << 31))
+  if (cq * 64 >= (int64_t(1) << 31) || cq * a.Hq * a.k >= (int64_t(1) << 31) || n_items >= (int64_t(1) << 31))
     return fail(MSA_ERR_UNSUPPORTED, "prefill attention: problem too large for 32-bit lists");
   uint8_t* w = static_cast<uint8_t*>(ws);
 

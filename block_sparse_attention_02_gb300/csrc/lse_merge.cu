@@ -73,6 +73,53 @@ lse_merge_kernel(const TP* __restrict__ o_part, const float* __restrict__ lse_pa
   if (lane == 0 && LSE != nullptr) LSE[row] = lse;
 }
 
+// bf16 partials, at most 16 parts, D = 128: one warp per row, every partial load
+// of the row issued before any is used.
+__global__ void __launch_bounds__(kWarps * 32)
+lse_merge_bf16_k16_kernel(const __nv_bfloat16* __restrict__ o_part, const float* __restrict__ lse_part, int64_t rows,
+                          int parts, __nv_bfloat16* __restrict__ O, float* __restrict__ LSE) {
+  constexpr int D = 128;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const float lv = lane < parts ? lse_part[row * parts + lane] : -INFINITY;
+  const __nv_bfloat16* op = o_part + row * static_cast<int64_t>(parts) * D + lane * 4;
+  uint2 raw[16];
+#pragma unroll
+  for (int pi = 0; pi < 16; ++pi) raw[pi] = pi < parts ? *reinterpret_cast<const uint2*>(op + pi * D) : make_uint2(0, 0);
+  float m = lv;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __nv_bfloat16* orow = O + row * D + lane * 4;
+  if (m == -INFINITY) {
+    *reinterpret_cast<uint2*>(orow) = make_uint2(0, 0);
+    if (lane == 0 && LSE != nullptr) LSE[row] = -INFINITY;
+    return;
+  }
+  const float e = lv == -INFINITY ? 0.f : __expf(lv - m);
+  float sum = e;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float wgt = e / sum;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int pi = 0; pi < 16; ++pi) {
+    const float wp = __shfl_sync(0xffffffffu, wgt, pi);
+    if (pi < parts && wp != 0.f) {
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[pi].x));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[pi].y));
+      acc.x = fmaf(wp, a.x, acc.x);
+      acc.y = fmaf(wp, a.y, acc.y);
+      acc.z = fmaf(wp, b.x, acc.z);
+      acc.w = fmaf(wp, b.y, acc.w);
+    }
+  }
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+  *reinterpret_cast<uint2*>(orow) = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+  if (lane == 0 && LSE != nullptr) LSE[row] = m + __logf(sum);
+}
+
 }  // namespace
 
 msa_status launch_lse_merge(const float* o_part, const float* lse_part, int64_t rows, int parts, int D, void* O,
@@ -91,8 +138,12 @@ msa_status launch_lse_merge_bf16(const __nv_bfloat16* o_part, const float* lse_p
                                  __nv_bfloat16* O, float* LSE, cudaStream_t stream) {
   if (rows == 0) return MSA_OK;
   const int64_t grid = (rows + kWarps - 1) / kWarps;
-  lse_merge_kernel<__nv_bfloat16><<<static_cast<unsigned>(grid), kWarps * 32, 0, stream>>>(o_part, lse_part, rows,
-                                                                                          parts, D, O, LSE);
+  if (parts <= 16 && D == 128)
+    lse_merge_bf16_k16_kernel<<<static_cast<unsigned>(grid), kWarps * 32, 0, stream>>>(o_part, lse_part, rows, parts,
+                                                                                      O, LSE);
+  else
+    lse_merge_kernel<__nv_bfloat16><<<static_cast<unsigned>(grid), kWarps * 32, 0, stream>>>(o_part, lse_part, rows,
+                                                                                            parts, D, O, LSE);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "lse_merge_kernel<bf16> launch");
   return MSA_OK;
