@@ -5,38 +5,52 @@
 // again and again, the outer loop walks KV blocks and the inner loop the
 // queries that selected them; per-block partial outputs are recombined by a
 // final log-sum-exp reduction ("MiniMax M3 preparado para inferencia en
-// produccion", paragraph "KV-Block-Major").  Per query chunk:
-//   1. count    how many (query, slot) pairs of the chunk selected each
-//               (b, g, block j); empty slots get LSE_part = -inf;
-//   2. scan     exclusive scan of the counts (CSR offsets) and of the number of
-//               128-row tiles per block (rows = selecting queries x G heads);
-//   3. fill     the CSR lists: entry = (query within chunk) * 64 + slot;
-//   4. attend   persistent tcgen05 kernel over the tiles.  Per tile of 128
-//               (query, head) rows of one (b, g, j): K_j and V_j are staged by
-//               TMA once per block (double-buffered), the Q rows are gathered
-//               with cp.async into a 128-byte-swizzled tile, then
+// produccion", paragraph "KV-Block-Major").  An item is one (b, g, block j);
+// its entries are the queries that selected it.  A tile holds 16 entries of one
+// item; entry e owns tile rows 8e .. 8e+7, of which the first G are its G query
+// heads of group g (the rest are padding).  In shared memory entry e is one
+// 2 KiB block: its 8 rows of columns 0-63, then of columns 64-127, each an
+// 8-row 128-byte-swizzled atom, loaded by a single TMA box.  Per query chunk:
+//   1. count    how many (query, slot) pairs of the chunk selected each item;
+//               empty slots are marked in the slot map;
+//   2. scan     CSR offsets, the number of tiles per item, and one descriptor
+//               per tile (item, entries, ordinal of the item, first/last flags);
+//   3. fill     the entry table in tile order (flattened query b*S+i of every
+//               tile entry) and the slot map (query, g, slot) -> first row;
+//   4. attend   persistent tcgen05 kernel over the tiles.  Per tile: K_j and
+//               V_j are staged by TMA once per item (double-buffered), each
+//               entry's query rows by one TMA box (three Q stages), then
 //                 S = Q K_j^T                (M=128, N=128, K=D; TMEM)
-//                 P = exp(S - rowmax), masked t <= i      (one thread per row)
-//                 O = P V_j                  (V as the MN-major operand)
-//               and each row writes its normalised partial O and
-//               LSE = m + ln l for its (query, head, slot);
-//   5. merge    the log-sum-exp merge kernel combines the k partials per
-//               (query, head) into O (bf16) and LSE.
+//                 P = exp(S - rowmax), masked t <= i, written back to TMEM
+//                 O = P V_j                  (P from TMEM, V as MN-major B)
+//               and each valid row writes its normalised partial O (bf16) and
+//               LSE = m + ln l at its tile row;
+//   5. merge    per (query, head): the log-sum-exp merge of its k partials,
+//               found through the slot map.
 // Keys of block j seen by query i are t in [j*Bk, (j+1)*Bk) with t <= i.
+#include <algorithm>
+
 #include "msa_internal.h"
 #include "msa_ptx.cuh"
 
 namespace msa {
 namespace {
 
-constexpr int kAttnThreads = 352;     // w0-1 Q gather + K/V TMA, w2-5 and w6-9 softmax/epilogue, w10 MMA
-constexpr int kMmaWarp = 10;
-constexpr int kHalf = 128 * 64 * 2;   // 16 KiB
-constexpr int kQStage = 2 * kHalf;    // 32 KiB: 128 rows x 128 (Q, then P)
+constexpr int kProducerWarp = 0;      // w0: Q and K/V TMA
+constexpr int kMmaWarp = 1;           // w1: tcgen05 issuer
+constexpr int kSoftmax0 = 2;          // w2-5 and w6-9: softmax/epilogue warpgroups
+constexpr int kAttnThreads = 10 * 32;
+constexpr int kQStages = 3;
+constexpr int kEntries = 16;          // queries (entries) per tile, 8 rows each
+constexpr int kHalf = 128 * 64 * 2;   // 16 KiB: 128 rows x 64 bf16, 128-byte swizzled
+constexpr int kQStage = 2 * kHalf;    // 32 KiB: 128 rows x 128
 constexpr int kKV = 4 * kHalf;        // 64 KiB: K (2 halves) + V (2 halves)
-constexpr int kTmemCols = 512;        // 2 slots x (S 128 + O 128)
+constexpr int kTmemCols = 512;        // 2 slots x (S/P 128 + O 128)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+
+constexpr int kTileFirst = 1;         // tile_info.w: first tile of its item
+constexpr int kTileLast = 2;          //              last tile of its item
 
 struct CsrParams {
   int S, Hkv, Hq, G, k, nb;
@@ -48,8 +62,9 @@ struct CsrParams {
   int32_t* cursor;      // [n_items]
   int32_t* off;         // [n_items + 1]
   int32_t* tile_off;    // [n_items + 1]
-  int32_t* list;
-  float* lse_part;
+  int4* tile_info;      // [tiles]: item, entries, ordinal of the item, first/last flags
+  int32_t* tile_q;      // [tiles * 16]: flattened query b*S+i of each tile entry
+  int32_t* where;       // [nq, Hkv, k]: first tile row of the (query, g, slot) entry, -1 if empty
   int32_t* dev_err;
 };
 
@@ -75,64 +90,77 @@ __global__ void csr_count_kernel(const CsrParams p) {
         live = true;
       }
     }
-    if (!live) {
-      for (int h = 0; h < p.G; ++h)
-        p.lse_part[(static_cast<int64_t>(qi) * p.Hq + g * p.G + h) * p.k + s] = -INFINITY;
-    }
+    if (!live) p.where[e] = -1;
   }
 }
 
-// single CTA: exclusive scans of counts and of tiles per item
+__device__ __forceinline__ int tiles_of(int c) { return (c + kEntries - 1) / kEntries; }
+
+// single CTA: exclusive scans of entries, tiles and non-empty items; then the
+// per-item offsets and one descriptor per tile
 __global__ void __launch_bounds__(1024) csr_scan_kernel(const CsrParams p, int64_t n_items) {
-  __shared__ int64_t s_sum[32][2];
+  __shared__ int64_t s_sum[32][3];
   const int tid = threadIdx.x;
   const int64_t per = (n_items + 1023) / 1024;
-  const int64_t i0 = tid * per, i1 = min(n_items, i0 + per);
-  int64_t c = 0, t = 0;
+  const int64_t i0 = min(n_items, tid * per), i1 = min(n_items, i0 + per);
+  int64_t c = 0, t = 0, z = 0;
   for (int64_t x = i0; x < i1; ++x) {
     const int v = p.cnt[x];
     c += v;
-    t += (static_cast<int64_t>(v) * p.G + 127) / 128;
+    t += tiles_of(v);
+    z += v > 0;
   }
   // inclusive warp scans, then a scan of the 32 warp totals
   const int lane = tid & 31, wid = tid >> 5;
-  int64_t ic = c, it = t;
+  int64_t ic = c, it = t, iz = z;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int64_t xc = __shfl_up_sync(0xffffffffu, ic, o);
     const int64_t xt = __shfl_up_sync(0xffffffffu, it, o);
-    if (lane >= o) { ic += xc; it += xt; }
+    const int64_t xz = __shfl_up_sync(0xffffffffu, iz, o);
+    if (lane >= o) { ic += xc; it += xt; iz += xz; }
   }
-  if (lane == 31) { s_sum[wid][0] = ic; s_sum[wid][1] = it; }
+  if (lane == 31) { s_sum[wid][0] = ic; s_sum[wid][1] = it; s_sum[wid][2] = iz; }
   __syncthreads();
   if (wid == 0) {
-    int64_t wc = s_sum[lane][0], wt = s_sum[lane][1];
+    int64_t wc = s_sum[lane][0], wt = s_sum[lane][1], wz = s_sum[lane][2];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int64_t xc = __shfl_up_sync(0xffffffffu, wc, o);
       const int64_t xt = __shfl_up_sync(0xffffffffu, wt, o);
-      if (lane >= o) { wc += xc; wt += xt; }
+      const int64_t xz = __shfl_up_sync(0xffffffffu, wz, o);
+      if (lane >= o) { wc += xc; wt += xt; wz += xz; }
     }
     s_sum[lane][0] = wc;   // inclusive over warps
     s_sum[lane][1] = wt;
+    s_sum[lane][2] = wz;
     if (lane == 31) {
       p.off[n_items] = static_cast<int32_t>(wc);
       p.tile_off[n_items] = static_cast<int32_t>(wt);
     }
   }
   __syncthreads();
-  c = ic - c + (wid > 0 ? s_sum[wid - 1][0] : 0);   // exclusive prefix of this thread
+  c = ic - c + (wid > 0 ? s_sum[wid - 1][0] : 0);   // exclusive prefixes of this thread
   t = it - t + (wid > 0 ? s_sum[wid - 1][1] : 0);
+  z = iz - z + (wid > 0 ? s_sum[wid - 1][2] : 0);
   for (int64_t x = i0; x < i1; ++x) {
     const int v = p.cnt[x];
     p.off[x] = static_cast<int32_t>(c);
     p.cursor[x] = static_cast<int32_t>(c);
     p.tile_off[x] = static_cast<int32_t>(t);
+    const int nt = tiles_of(v);
+    for (int u = 0; u < nt; ++u) {
+      const int flags = (u == 0 ? kTileFirst : 0) | (u == nt - 1 ? kTileLast : 0);
+      p.tile_info[t + u] = make_int4(static_cast<int>(x), min(kEntries, v - kEntries * u), static_cast<int>(z), flags);
+    }
     c += v;
-    t += (static_cast<int64_t>(v) * p.G + 127) / 128;
+    t += nt;
+    z += v > 0;
   }
 }
 
+// one thread per (query in chunk, group, slot): claims the entry's place in its
+// item and writes the entry table and the slot map
 __global__ void csr_fill_kernel(const CsrParams p) {
   const int64_t total = static_cast<int64_t>(p.nq) * p.Hkv * p.k;
   for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
@@ -147,8 +175,12 @@ __global__ void csr_fill_kernel(const CsrParams p) {
     if (s >= c) continue;
     const int j = p.sel[(bs * p.Hkv + g) * p.k + s];
     if (j < 0 || j > i / kBk) continue;
-    const int pos = atomicAdd(&p.cursor[(static_cast<int64_t>(b) * p.Hkv + g) * p.nb + j], 1);
-    p.list[pos] = qi * 64 + s;
+    const int64_t item = (static_cast<int64_t>(b) * p.Hkv + g) * p.nb + j;
+    const int pos = atomicAdd(&p.cursor[item], 1);
+    const int es = p.tile_off[item] * kEntries + (pos - p.off[item]);   // entry slot in tile order
+    p.tile_q[es] = static_cast<int>(bs);
+    p.where[e] = es * 8;                                                // tile row of head 0
+
   }
 }
 
@@ -157,32 +189,16 @@ __global__ void csr_fill_kernel(const CsrParams p) {
 // ---------------------------------------------------------------------------
 
 struct AttnParams {
-  int S, Hq, Hkv, G, k, nb;
-  int64_t q0;
+  int S, Hkv, G, nb;
   int64_t n_items;
   float scale_log2;
-  const __nv_bfloat16* Q;
-  int64_t qs0, qs1, qs2;
-  const int32_t* off;
-  const int32_t* tile_off;
-  const int32_t* list;
-  __nv_bfloat16* o_part;
-  float* lse_part;
+  const int32_t* tile_off;   // tile_off[n_items] = number of tiles
+  const int4* tile_info;
+  const int32_t* tile_q;
+  __nv_bfloat16* o_part;     // [tiles * 128, D] bf16, tile order
+  float* lse_part;           // [tiles * 128]
   int32_t* dev_err;
 };
-
-struct TileInfo {
-  int item, b, g, j, row0, nrows, kvb, kv_new, kv_release, ebase;
-};
-
-__device__ __forceinline__ int64_t find_item(const AttnParams& p, int64_t t) {
-  int64_t lo = 0, hi = p.n_items - 1;
-  while (lo < hi) {
-    const int64_t mid = (lo + hi + 1) >> 1;
-    if (p.tile_off[mid] <= t) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
 
 // packed fp32 helpers and the hardware base-2 exponential
 __device__ __forceinline__ uint64_t pack2f(float x, float y) {
@@ -218,44 +234,43 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h2);
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool full) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(full ? 16 : 0)
+// streaming store (evict-first): the partials are read once, by the merge
+__device__ __forceinline__ void st_cs_v4(void* ptr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.global.cs.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __global__ void __launch_bounds__(kAttnThreads, 1)
-attn_prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                    const AttnParams p) {
+attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                    const __grid_constant__ CUtensorMap vmap, const AttnParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* s_kv = smem;                    // [2] x (K0 K1 V0 V1)
-  uint8_t* s_q = smem + 2 * kKV;           // [2] x (Q then P), 128 rows x 128
+  uint8_t* s_q = smem + 2 * kKV;           // [kQStages] x Q tile
 
-  __shared__ __align__(8) uint64_t bar_qfull[2], bar_qempty[2], bar_kvfull[2], bar_kvempty[2];
+  __shared__ __align__(8) uint64_t bar_qfull[kQStages], bar_qempty[kQStages], bar_kvfull[2], bar_kvempty[2];
   __shared__ __align__(8) uint64_t bar_sfull[2], bar_pready[2], bar_ofull[2], bar_tfree[2], bar_drain;
-  __shared__ TileInfo s_info[2];
-  __shared__ const __nv_bfloat16* s_rowsrc[2][128];
-  __shared__ int2 s_rinfo[2][128];         // per tile row: query position i, partial row (-1: padding)
+  __shared__ int s_kvinfo[kQStages];       // per Q stage: K/V buffer, new, release, phase (producer -> MMA)
   __shared__ uint32_t s_tmem;
-  __shared__ int s_abort, s_fail[2], s_gfail[2];
+  __shared__ int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // padding rows of a tile (no query) keep whatever the stage held; start from zeros
+  for (int x = tid; x < kQStages * kQStage / 16; x += kAttnThreads)
+    reinterpret_cast<uint4*>(s_q)[x] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
   if (tid == 0) {
+    for (int i = 0; i < kQStages; ++i) {
+      mbar_init(&bar_qfull[i], 1);
+      mbar_init(&bar_qempty[i], 1);
+    }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar_qfull[i], 32); mbar_init(&bar_qempty[i], 1);
       mbar_init(&bar_kvfull[i], 1); mbar_init(&bar_kvempty[i], 1);
       mbar_init(&bar_sfull[i], 1); mbar_init(&bar_pready[i], 4);
       mbar_init(&bar_ofull[i], 1); mbar_init(&bar_tfree[i], 4);
     }
     mbar_init(&bar_drain, 1);
     s_abort = 0;
-    s_fail[0] = s_fail[1] = 0;
-    s_gfail[0] = s_gfail[1] = 0;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) tmem_alloc(&s_tmem, kTmemCols);
@@ -270,182 +285,197 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   const int64_t t1 = min(total_tiles, t0 + per);
   const int ntiles = static_cast<int>(t1 - t0);
 
-  if (warp < 2) {
-    // ===================== producers: warp gi owns Q stage gi (tiles n = gi mod 2) =====================
-    // Each warp resolves its tile's rows (query, head, slot), gathers the Q rows,
-    // waits for its own copies, fences them for the tensor core and releases the
-    // stage; the two warps keep two gathers in flight.
-    const int gi = warp;
-    int64_t prev_item = -1;
-    int kvn = 0, last_kv = -1;   // last K/V load issued by this warp
-    // tiles of this CTA are contiguous: walk their items forward instead of searching
-    int64_t item = ntiles > 0 ? find_item(p, t0) : 0;
-    for (int n = 0; n < ntiles; ++n) {
-      const int64_t t = t0 + n;
-      while (p.tile_off[item + 1] <= t) ++item;
-      const bool kv_new = item != prev_item;
-      prev_item = item;
-      if (kv_new) ++kvn;
-      if ((n & 1) != gi) continue;
-      const int st = gi;
-      const int b = static_cast<int>(item / (static_cast<int64_t>(p.Hkv) * p.nb));
-      const int g = static_cast<int>((item / p.nb) % p.Hkv);
-      const int j = static_cast<int>(item % p.nb);
-      const int ebase = p.off[item];
-      const int rows_item = (p.off[item + 1] - ebase) * p.G;
-      const int row0 = static_cast<int>(t - p.tile_off[item]) * 128;
-      const int nrows = min(128, rows_item - row0);
-      const int kvb = (kvn - 1) & 1;
-      // rows of this tile (4 per lane), resolved before waiting for the stage
-      const __nv_bfloat16* src[4];
-      int2 ri[4];
+  if (warp == kProducerWarp) {
+    // ===================== producer: Q boxes and K/V blocks by TMA =====================
+    // Lane e loads the query rows of tile entry e (heads g*G .. g*G+7, both
+    // column halves) into bytes 2048e.. of the stage; lane 0 also loads K_j, V_j
+    // for the first tile of each item (in this CTA).
+    const int ord0 = ntiles > 0 ? p.tile_info[t0].z : 0;
+    constexpr uint32_t kQBytesPerEntry = 2048;   // full box, out-of-range heads included (zero-filled)
+    int last_kv = -1, last_q = -1;
+    // tile descriptors and entry queries, kPf tiles ahead (a ring in registers)
+    constexpr int kPf = 4;
+    int4 rti[kPf];
+    int rbs[kPf];
 #pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const int rr = lane + 32 * x;
-        src[x] = nullptr;
-        ri[x] = make_int2(0, -1);
-        if (rr < nrows) {
-          const int rho = row0 + rr;
-          const int ent = p.list[ebase + rho / p.G];
-          const int qi = ent >> 6;
-          const int hq = g * p.G + rho % p.G;
-          const int i = static_cast<int>((p.q0 + qi) % p.S);
-          src[x] = p.Q + static_cast<int64_t>(b) * p.qs0 + static_cast<int64_t>(i) * p.qs1 +
-                   static_cast<int64_t>(hq) * p.qs2;
-          ri[x] = make_int2(i, (qi * p.Hq + hq) * p.k + (ent & 63));
-        }
+    for (int x = 0; x < kPf; ++x) {
+      rti[x] = make_int4(0, 0, 0, 0);
+      rbs[x] = 0;
+      if (x < ntiles) {
+        rti[x] = p.tile_info[t0 + x];
+        rbs[x] = lane < kEntries ? p.tile_q[(t0 + x) * kEntries + lane] : 0;   // entries past ti.y unused
       }
-      bool ok = true;
-      if (lane == 0) {
-        const bool release = (n + 1 == ntiles) || p.tile_off[item + 1] <= t + 1;
-        ok = mbar_wait(&bar_qempty[st], ((n >> 1) & 1) ^ 1, abort_flag, p.dev_err);
-        if (ok && kv_new) {
-          ok = mbar_wait(&bar_kvempty[kvb], (((kvn - 1) >> 1) & 1) ^ 1, abort_flag, p.dev_err);
+    }
+    bool stop = false;
+    for (int n0 = 0; n0 < ntiles && !stop; n0 += kPf) {
+#pragma unroll
+      for (int x = 0; x < kPf; ++x) {
+        const int n = n0 + x;
+        if (stop || n >= ntiles) break;
+        const int4 ti = rti[x];
+        const int bs = rbs[x];
+        if (n + kPf < ntiles) {
+          rti[x] = p.tile_info[t0 + n + kPf];
+          rbs[x] = lane < kEntries ? p.tile_q[(t0 + n + kPf) * kEntries + lane] : 0;
+        }
+        const int item = ti.x, ne = ti.y, rel = ti.z - ord0;
+        const int kvb = rel & 1;
+        const bool kv_new = n == 0 || (ti.w & kTileFirst);
+        const bool kv_rel = n + 1 == ntiles || (ti.w & kTileLast);
+        const int b = static_cast<int>(item / (static_cast<int64_t>(p.Hkv) * p.nb));
+        const int g = static_cast<int>((item / p.nb) % p.Hkv);
+        const int j = static_cast<int>(item % p.nb);
+        const int st = n % kQStages;
+        bool ok = true;
+        if (lane == 0) {
+          ok = mbar_wait(&bar_qempty[st], ((n / kQStages) & 1) ^ 1, abort_flag, p.dev_err);
+          if (ok && kv_new) {
+            ok = mbar_wait(&bar_kvempty[kvb], ((rel >> 1) & 1) ^ 1, abort_flag, p.dev_err);
+            if (ok) {
+              uint8_t* kvbuf = s_kv + kvb * kKV;
+              mbar_arrive_expect_tx(&bar_kvfull[kvb], kKV);
+              tma_load_4d(kvbuf + 0 * kHalf, &kmap, &bar_kvfull[kvb], 0, g, j * kBk, b);
+              tma_load_4d(kvbuf + 1 * kHalf, &kmap, &bar_kvfull[kvb], 64, g, j * kBk, b);
+              tma_load_4d(kvbuf + 2 * kHalf, &vmap, &bar_kvfull[kvb], 0, g, j * kBk, b);
+              tma_load_4d(kvbuf + 3 * kHalf, &vmap, &bar_kvfull[kvb], 64, g, j * kBk, b);
+              last_kv = rel;
+            }
+          }
           if (ok) {
-            uint8_t* kvbuf = s_kv + kvb * kKV;
-            mbar_arrive_expect_tx(&bar_kvfull[kvb], kKV);
-            tma_load_4d(kvbuf + 0 * kHalf, &kmap, &bar_kvfull[kvb], 0, g, j * kBk, b);
-            tma_load_4d(kvbuf + 1 * kHalf, &kmap, &bar_kvfull[kvb], 64, g, j * kBk, b);
-            tma_load_4d(kvbuf + 2 * kHalf, &vmap, &bar_kvfull[kvb], 0, g, j * kBk, b);
-            tma_load_4d(kvbuf + 3 * kHalf, &vmap, &bar_kvfull[kvb], 64, g, j * kBk, b);
-            last_kv = kvn - 1;
+            s_kvinfo[st] = kvb | (kv_new ? 2 : 0) | (kv_rel ? 4 : 0) | (((rel >> 1) & 1) << 3);
+            mbar_arrive_expect_tx(&bar_qfull[st], static_cast<uint32_t>(ne) * kQBytesPerEntry);
+            last_q = n;
           }
         }
-        s_info[st] = TileInfo{static_cast<int>(item), b, g, j, row0, nrows, kvb, kv_new ? 1 : 0, release ? 1 : 0,
-                              ebase};
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;                      // the warp stops together
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        s_rowsrc[st][lane + 32 * x] = src[x];
-        s_rinfo[st][lane + 32 * x] = ri[x];
-      }
-      __syncwarp();
-      const uint32_t qbase = smem_u32(s_q + st * kQStage);
-#pragma unroll 8
-      for (int u = 0; u < 64; ++u) {
-        const int idx = lane + 32 * u;     // 2048 chunks of 16 B
-        const int rr = idx >> 4, c = idx & 15;
-        const __nv_bfloat16* sp = s_rowsrc[st][rr];
-        const uint32_t dst = qbase + (c >> 3) * kHalf + sw128_offset(rr, c & 7);
-        cp_async16(dst, sp ? static_cast<const void*>(sp + c * 8) : static_cast<const void*>(p.Q), sp != nullptr);
-      }
-      cp_async_commit();
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      mbar_arrive(&bar_qfull[st]);
-      __syncwarp();                        // s_rowsrc[st] is rewritten two tiles later
-    }
-    if (*abort_flag && lane == 0 && last_kv >= 0) {   // let this warp's last K/V load land
-      uint64_t tt = global_timer_ns();
-      while (!mbar_try_wait(&bar_kvfull[last_kv & 1], (last_kv >> 1) & 1) &&
-             global_timer_ns() - tt < MSA_WAIT_LIMIT_NS) {
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {                         // the warp stops together
+          stop = true;
+          break;
+        }
+        if (lane < ne) {
+          const int qb_ = bs / p.S, qi_ = bs - qb_ * p.S;
+          tma_load_5d(s_q + st * kQStage + lane * 2048, &qmap, &bar_qfull[st], 0, g * p.G, 0, qi_, qb_);
+        }
+        __syncwarp();
       }
     }
+    if (*abort_flag && lane == 0) {        // let this warp's last loads land before the CTA exits
+      const uint64_t tt = global_timer_ns();
+      if (last_kv >= 0)
+        while (!mbar_try_wait(&bar_kvfull[last_kv & 1], (last_kv >> 1) & 1) &&
+               global_timer_ns() - tt < MSA_WAIT_LIMIT_NS) {
+        }
+      if (last_q >= 0)
+        while (!mbar_try_wait(&bar_qfull[last_q % kQStages], (last_q / kQStages) & 1) &&
+               global_timer_ns() - tt < MSA_WAIT_LIMIT_NS) {
+        }
+    }
+    __syncwarp();
   } else if (warp == kMmaWarp) {
     // ===================== tcgen05 issuer =====================
-    if (lane == 0) {
+    // S(n) and O(n) are issued as soon as their inputs are ready, in either
+    // order: S(n+1) never waits for P(n), O(n) never waits for Q(n+1).
+    if (lane == 0 && ntiles > 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_o = idesc_bf16(128, 128, false, true);
-      int kvn = 0;
-      bool ok = true;
-      auto issue_s = [&](int n) -> bool {
-        const int st = n & 1, slot = n & 1;
-        if (!mbar_wait(&bar_qfull[st], (n >> 1) & 1, abort_flag, p.dev_err)) return false;
-        const TileInfo inf = s_info[st];
-        if (inf.kv_new) {
-          ++kvn;
-          if (!mbar_wait(&bar_kvfull[inf.kvb], ((kvn - 1) >> 1) & 1, abort_flag, p.dev_err)) return false;
-        }
-        if (!mbar_wait(&bar_tfree[slot], ((n >> 1) & 1) ^ 1, abort_flag, p.dev_err)) return false;
-        tc_fence_after();
-        const uint32_t qb = smem_u32(s_q + st * kQStage);
-        const uint32_t kb = smem_u32(s_kv + inf.kvb * kKV);
+      int ns = 0, no = 0;
+      int kvinfo[2] = {0, 0};
+      uint64_t idle_since = global_timer_ns();
+      uint32_t spins = 0;
+      while (no < ntiles) {
+        bool progress = false;
+        if (ns < ntiles && ns < no + 2) {
+          const int st = ns % kQStages, slot = ns & 1;
+          if (mbar_test_wait(&bar_qfull[st], (ns / kQStages) & 1)) {
+            const int kv = s_kvinfo[st];
+            bool ready = !(kv & 2) || mbar_test_wait(&bar_kvfull[kv & 1], (kv >> 3) & 1);
+            ready = ready && mbar_test_wait(&bar_tfree[slot], ((ns >> 1) & 1) ^ 1);
+            if (ready) {
+              tc_fence_after();
+              const uint32_t qb = smem_u32(s_q + st * kQStage);
+              const uint32_t kb = smem_u32(s_kv + (kv & 1) * kKV);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t o = (kk >> 2) * kHalf + 32 * (kk & 3);
-          umma_bf16(tmem + slot * 256, sdesc_sw128(qb + o, 16, 1024), sdesc_sw128(kb + o, 16, 1024), idesc_s, kk > 0);
+              for (int kk = 0; kk < 8; ++kk) {
+                // Q: 8-row atoms 2048 B apart, column half at +1024; K: halves 16 KiB apart
+                umma_bf16(tmem + slot * 256, sdesc_sw128(qb + (kk >> 2) * 1024 + 32 * (kk & 3), 16, 2048),
+                          sdesc_sw128(kb + (kk >> 2) * kHalf + 32 * (kk & 3), 16, 1024), idesc_s, kk > 0);
+              }
+              umma_commit(&bar_sfull[slot]);
+              umma_commit(&bar_qempty[st]);
+              kvinfo[slot] = kv;
+              ++ns;
+              progress = true;
+            }
+          }
         }
-        umma_commit(&bar_sfull[slot]);
-        return true;
-      };
-      auto issue_o = [&](int n) -> bool {
-        const int st = n & 1, slot = n & 1;
-        if (!mbar_wait(&bar_pready[slot], (n >> 1) & 1, abort_flag, p.dev_err)) return false;
-        tc_fence_after();
-        const TileInfo inf = s_info[st];
-        const uint32_t pb = smem_u32(s_q + st * kQStage);
-        const uint32_t vb = smem_u32(s_kv + inf.kvb * kKV + 2 * kHalf);
+        if (no < ns) {
+          const int slot = no & 1;
+          if (mbar_test_wait(&bar_pready[slot], (no >> 1) & 1)) {
+            tc_fence_after();
+            const int kv = kvinfo[slot];
+            const uint32_t vb = smem_u32(s_kv + (kv & 1) * kKV + 2 * kHalf);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t po = (kk >> 2) * kHalf + 32 * (kk & 3);
-          umma_bf16(tmem + slot * 256 + 128, sdesc_sw128(pb + po, 16, 1024), sdesc_sw128(vb + kk * 2048, kHalf, 1024),
-                    idesc_o, kk > 0);
+            for (int kk = 0; kk < 8; ++kk)
+              umma_bf16_ts(tmem + slot * 256 + 128, tmem + slot * 256 + kk * 8,
+                           sdesc_sw128(vb + kk * 2048, kHalf, 1024), idesc_o, kk > 0);
+            umma_commit(&bar_ofull[slot]);
+            if (kv & 4) umma_commit(&bar_kvempty[kv & 1]);
+            ++no;
+            progress = true;
+          }
         }
-        umma_commit(&bar_ofull[slot]);
-        umma_commit(&bar_qempty[st]);
-        if (inf.kv_release) umma_commit(&bar_kvempty[inf.kvb]);
-        return true;
-      };
-      if (ntiles > 0) ok = issue_s(0);
-      for (int n = 0; n < ntiles && ok; ++n) {
-        if (n + 1 < ntiles) ok = issue_s(n + 1);
-        if (ok) ok = issue_o(n);
+        if (progress) {
+          spins = 0;
+        } else if ((++spins & 63u) == 0) {
+          const uint64_t now = global_timer_ns();
+          if (spins == 64) idle_since = now;
+          if (*abort_flag) break;
+          if (now - idle_since > MSA_WAIT_LIMIT_NS) {
+            *abort_flag = 1;
+            report(p.dev_err, MSA_DEVERR_TIMEOUT);
+            break;
+          }
+        }
       }
       umma_commit(&bar_drain);
-      uint64_t tt = global_timer_ns();
+      const uint64_t tt = global_timer_ns();
       while (!mbar_try_wait(&bar_drain, 0) && global_timer_ns() - tt < MSA_WAIT_LIMIT_NS) {
       }
     }
     __syncwarp();
   } else {
-    // ===================== softmax + epilogue: warpgroup wg (warps 2-5 / 6-9) owns tiles n = wg mod 2 =====
-    const int wg = (warp - 2) >> 2;
-    const int bar_id = 1 + wg;
+    // ===================== softmax + epilogue: warpgroup wg owns TMEM slot wg (tiles n = wg mod 2) =====
+    const int wg = (warp - kSoftmax0) >> 2;
     const int q = warp & 3;
     const int r = q * 32 + lane;                     // tile row = TMEM lane
+    const int e = r >> 3, h = r & 7;                 // entry of the row, head within the group
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
-    const int st = wg, slot = wg;
+    const int slot = wg;
+    const uint32_t sbase = tmem + lane_addr + slot * 256;   // S, then P (bf16 pairs) in its first 64 columns
+    const float sc = p.scale_log2;
+    int4 nti = make_int4(0, 0, 0, 0);
+    int nbs = 0;
+    if (wg < ntiles) {
+      nti = p.tile_info[t0 + wg];
+      nbs = p.tile_q[(t0 + wg) * kEntries + e];
+    }
     for (int n = wg; n < ntiles; n += 2) {
+      const int4 ti = nti;
+      const int bs = nbs;
+      if (n + 2 < ntiles) {
+        nti = p.tile_info[t0 + n + 2];
+        nbs = p.tile_q[(t0 + n + 2) * kEntries + e];
+      }
       const uint32_t ph = (n >> 1) & 1;
-      if (!mbar_wait(&bar_qfull[st], ph, abort_flag, p.dev_err)) s_fail[wg] = 1;
-      named_bar_sync(bar_id, 128);
-      if (s_fail[wg]) break;
-      const int j = s_info[st].j;
-      const int2 ri = s_rinfo[st][r];
-      const bool valid = ri.y >= 0;
+      const int j = static_cast<int>(ti.x % p.nb);
+      const bool valid = h < p.G && e < ti.y;
       // keys of this block visible to the row: t <= i
-      const int nvis = valid ? min(kBk, ri.x - j * kBk + 1) : kBk;
-      if (!mbar_wait(&bar_sfull[slot], ph, abort_flag, p.dev_err)) s_fail[wg] = 1;
-      named_bar_sync(bar_id, 128);
-      if (s_fail[wg]) break;
+      const int nvis = valid ? min(kBk, bs % p.S - j * kBk + 1) : kBk;
+      const bool ok_s = mbar_wait(&bar_sfull[slot], ph, abort_flag, p.dev_err);
+      if (!__all_sync(0xffffffffu, ok_s)) break;     // warp-uniform exit
       tc_fence_after();
-      const uint32_t sbase = tmem + lane_addr + slot * 256;
-      uint8_t* prow = s_q + st * kQStage;
-      const float sc = p.scale_log2;
       float m = -INFINITY, l = 0.f;
-      // the branch must be warp-uniform: the TMEM loads inside are warp-collective
+      // the branch must be warp-uniform: the TMEM loads and stores inside are warp-collective
       if (__all_sync(0xffffffffu, nvis == kBk)) {
         // whole block visible to every row of the warp: no masking
 #pragma unroll
@@ -467,23 +497,19 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
           tmem_ld32(sbase + half * 64, v[0]);
           tmem_ld32(sbase + half * 64 + 32, v[1]);
           tmem_ld_wait();
+          uint32_t pw[32];
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
-            uint32_t pk[16];
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
               const float p0 = fast_exp2(fmaf(__uint_as_float(v[c][e]), sc, -m));
               const float p1 = fast_exp2(fmaf(__uint_as_float(v[c][e + 1]), sc, -m));
               l2 = add2(l2, pack2f(p0, p1));
-              pk[e >> 1] = pack_bf16x2(p0, p1);
-            }
-#pragma unroll
-            for (int x = 0; x < 4; ++x) {
-              const int ch = (half * 2 + c) * 4 + x;
-              *reinterpret_cast<uint4*>(prow + (ch >> 3) * kHalf + sw128_offset(r, ch & 7)) =
-                  make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
+              pw[16 * c + (e >> 1)] = pack_bf16x2(p0, p1);
             }
           }
+          // P columns 32*half.. hold keys 64*half..: S columns already read
+          tmem_st32(sbase + half * 32, pw);
         }
         float la, lb;
         unpack2f(l2, la, lb);
@@ -508,59 +534,61 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
           uint32_t v[32];
           tmem_ld32(sbase + cc * 32, v);
           tmem_ld_wait();
-          uint32_t pk[16];
+          uint32_t pw[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const float p0 = (cc * 32 + e < nvis) ? fast_exp2(fmaf(__uint_as_float(v[e]), sc, -m)) : 0.f;
             const float p1 = (cc * 32 + e + 1 < nvis) ? fast_exp2(fmaf(__uint_as_float(v[e + 1]), sc, -m)) : 0.f;
             l2 = add2(l2, pack2f(p0, p1));
-            pk[e >> 1] = pack_bf16x2(p0, p1);
+            pw[e >> 1] = pack_bf16x2(p0, p1);
           }
-#pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            const int ch = cc * 4 + x;
-            *reinterpret_cast<uint4*>(prow + (ch >> 3) * kHalf + sw128_offset(r, ch & 7)) =
-                make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
-          }
+          tmem_st16(sbase + cc * 16, pw);
         }
         float la, lb;
         unpack2f(l2, la, lb);
         l = la + lb;
       }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_pready[slot]);
-      if (!mbar_wait(&bar_ofull[slot], ph, abort_flag, p.dev_err)) s_fail[wg] = 1;
-      named_bar_sync(bar_id, 128);
-      if (s_fail[wg]) break;
+      const bool ok_o = mbar_wait(&bar_ofull[slot], ph, abort_flag, p.dev_err);
+      if (!__all_sync(0xffffffffu, ok_o)) break;
       tc_fence_after();
       const float inv = 1.0f / l;
-      __nv_bfloat16* orow = p.o_part + static_cast<int64_t>(valid ? ri.y : 0) * kD;
+      const uint64_t inv2 = pack2f(inv, inv);
+      const int64_t prow = (t0 + n) * 128 + r;
+      __nv_bfloat16* orow = p.o_part + prow * kD;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t v[32];
-        tmem_ld32(sbase + 128 + cc * 32, v);
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t v[2][32];
+        tmem_ld32(sbase + 128 + hh * 64, v[0]);
+        tmem_ld32(sbase + 128 + hh * 64 + 32, v[1]);
         tmem_ld_wait();
+        if (hh == 1) {                               // O is in registers: the slot may be reused
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar_tfree[slot]);
+        }
         if (valid) {
 #pragma unroll
-          const uint64_t inv2 = pack2f(inv, inv);
-          for (int e = 0; e < 32; e += 8) {
-            uint32_t w[4];
+          for (int c = 0; c < 2; ++c) {
 #pragma unroll
-            for (int x = 0; x < 4; ++x) {
-              float a, b;
-              unpack2f(mul2(pack2f(__uint_as_float(v[e + 2 * x]), __uint_as_float(v[e + 2 * x + 1])), inv2), a, b);
-              w[x] = pack_bf16x2(a, b);
+            for (int e8 = 0; e8 < 32; e8 += 8) {
+              uint32_t w4[4];
+#pragma unroll
+              for (int x = 0; x < 4; ++x) {
+                float a0, a1;
+                unpack2f(mul2(pack2f(__uint_as_float(v[c][e8 + 2 * x]), __uint_as_float(v[c][e8 + 2 * x + 1])), inv2),
+                         a0, a1);
+                w4[x] = pack_bf16x2(a0, a1);
+              }
+              st_cs_v4(orow + hh * 64 + c * 32 + e8, w4[0], w4[1], w4[2], w4[3]);
             }
-            *reinterpret_cast<uint4*>(orow + cc * 32 + e) = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
       }
-      if (valid) p.lse_part[ri.y] = (m + log2f(l)) * kLn2;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_tfree[slot]);
+      if (valid) __stcs(p.lse_part + prow, (m + log2f(l)) * kLn2);
     }
   }
 
@@ -572,23 +600,113 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   }
 }
 
-struct WsLayout {
-  size_t cnt, cursor, off, tile_off, list, o_part, lse_part, total;
+// ---------------------------------------------------------------------------
+// merge: O = sum_s e^{LSE_s - LSE} O_s, LSE = ln sum_s e^{LSE_s} over the k
+// slots of each (query, head); one warp per (query, head)
+// ---------------------------------------------------------------------------
+
+constexpr int kMergeWarps = 8;
+
+struct MergeParams {
+  int nq, Hq, Hkv, G, k;
+  const __nv_bfloat16* o_part;
+  const float* lse_part;
+  const int32_t* where;
+  __nv_bfloat16* O;      // chunk's first output row
+  float* LSE;            // chunk's first LSE (or null)
 };
 
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+}
+
+// KMAX = 16: every partial load of the row in flight at once (k <= 16);
+// KMAX = 64: a loop over the slots, two per lane.
+template <int KMAX>
+__global__ void __launch_bounds__(kMergeWarps * 32) prefill_merge_kernel(const MergeParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
+  if (row >= static_cast<int64_t>(p.nq) * p.Hq) return;
+  const int qi = static_cast<int>(row / p.Hq), hq = static_cast<int>(row % p.Hq);
+  const int g = hq / p.G, h = hq - g * p.G;
+  const int32_t* wp = p.where + (static_cast<int64_t>(qi) * p.Hkv + g) * p.k;
+  const int base0 = lane < p.k ? wp[lane] : -1;
+  const int base1 = (KMAX > 32 && lane + 32 < p.k) ? wp[lane + 32] : -1;
+  const float l0 = base0 >= 0 ? __ldcs(p.lse_part + base0 + h) : -INFINITY;
+  const float l1 = base1 >= 0 ? __ldcs(p.lse_part + base1 + h) : -INFINITY;
+  __nv_bfloat16* orow = p.O + row * kD + lane * 4;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float m = fmaxf(l0, l1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (m == -INFINITY) {
+    *reinterpret_cast<uint2*>(orow) = make_uint2(0, 0);
+    if (lane == 0 && p.LSE != nullptr) p.LSE[row] = -INFINITY;
+    return;
+  }
+  const float e0 = l0 == -INFINITY ? 0.f : __expf(l0 - m);
+  const float e1 = l1 == -INFINITY ? 0.f : __expf(l1 - m);
+  float sum = e0 + e1;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float w0 = e0 / sum, w1 = e1 / sum;
+  auto fma4 = [&](float wgt, uint2 raw) {
+    const float2 a = bf2_to_f2(raw.x), b = bf2_to_f2(raw.y);
+    acc.x = fmaf(wgt, a.x, acc.x);
+    acc.y = fmaf(wgt, a.y, acc.y);
+    acc.z = fmaf(wgt, b.x, acc.z);
+    acc.w = fmaf(wgt, b.y, acc.w);
+  };
+  if (KMAX <= 16) {
+    uint2 raw[16];
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+      const int bs = __shfl_sync(0xffffffffu, base0, s);
+      raw[s] = bs >= 0 ? __ldcs(reinterpret_cast<const uint2*>(p.o_part + static_cast<int64_t>(bs + h) * kD) + lane)
+                       : make_uint2(0, 0);
+    }
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+      const float ws = __shfl_sync(0xffffffffu, w0, s);
+      if (ws != 0.f) fma4(ws, raw[s]);
+    }
+  } else {
+    for (int s = 0; s < p.k; ++s) {
+      const int bs = __shfl_sync(0xffffffffu, s < 32 ? base0 : base1, s & 31);
+      const float ws = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
+      if (bs >= 0 && ws != 0.f)
+        fma4(ws, __ldcs(reinterpret_cast<const uint2*>(p.o_part + static_cast<int64_t>(bs + h) * kD) + lane));
+    }
+  }
+  *reinterpret_cast<uint2*>(orow) = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+  if (lane == 0 && p.LSE != nullptr) p.LSE[row] = m + __logf(sum);
+}
+
+struct WsLayout {
+  size_t cnt, cursor, off, tile_off, tile_info, tile_q, where, o_part, lse_part, total;
+  int64_t max_tiles;
+};
+
+// Tiles of a chunk: sum over items of ceil(entries / 16)
+//   <= entries / 16 + (non-empty items) + 1.
 WsLayout ws_layout(const msa_prefill_args& a, int64_t cq) {
   const int64_t nb = (a.S + kBk - 1) / kBk;
   const int64_t n_items = static_cast<int64_t>(a.B) * a.Hkv * nb;
+  const int64_t entries = cq * a.Hkv * a.k;
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   WsLayout L;
+  L.max_tiles = (entries + kEntries - 1) / kEntries + std::min(n_items, entries) + 1;
+  const size_t rows = static_cast<size_t>(L.max_tiles) * 128;
   size_t o = 0;
   L.cnt = o; o = al(o + n_items * 4);
   L.cursor = o; o = al(o + n_items * 4);
   L.off = o; o = al(o + (n_items + 1) * 4);
   L.tile_off = o; o = al(o + (n_items + 1) * 4);
-  L.list = o; o = al(o + static_cast<size_t>(cq) * a.Hkv * a.k * 4);
-  L.o_part = o; o = al(o + static_cast<size_t>(cq) * a.Hq * a.k * kD * 2);   // bf16 partials
-  L.lse_part = o; o = al(o + static_cast<size_t>(cq) * a.Hq * a.k * 4);
+  L.tile_info = o; o = al(o + static_cast<size_t>(L.max_tiles) * 16);
+  L.tile_q = o; o = al(o + static_cast<size_t>(L.max_tiles) * kEntries * 4);
+  L.where = o; o = al(o + static_cast<size_t>(entries) * 4);
+  L.o_part = o; o = al(o + rows * kD * 2);   // bf16 partials
+  L.lse_part = o; o = al(o + rows * 4);
   L.total = o + 256;
   return L;
 }
@@ -613,11 +731,26 @@ msa_status launch_attn_prefill(const msa_prefill_args& a, void* ws, size_t ws_by
   const WsLayout L = ws_layout(a, cq);
   const int64_t nb = (a.S + kBk - 1) / kBk;
   const int64_t n_items = static_cast<int64_t>(a.B) * a.Hkv * nb;
-  if (cq * 64 >= (int64_t(1) << 31) || cq * a.Hq * a.k >= (int64_t(1) << 31) || n_items >= (int64_t(1) << 31))
-    return fail(MSA_ERR_UNSUPPORTED, "prefill attention: problem too large for 32-bit lists");
+  const int G = a.Hq / a.Hkv;
+  if (L.max_tiles * 128 >= (int64_t(1) << 31) || cq * a.Hkv * a.k >= (int64_t(1) << 31) ||
+      n_items >= (int64_t(1) << 31) || total_q >= (int64_t(1) << 31))
+    return fail(MSA_ERR_UNSUPPORTED, "prefill attention: problem too large for 32-bit tile rows");
   uint8_t* w = static_cast<uint8_t*>(ws);
 
-  CUtensorMap kmap, vmap;
+  CUtensorMap qmap, kmap, vmap;
+  {
+    // Q [B, S, Hq, D] seen as (64 columns, head, column half, i, b): one box =
+    // 8 heads from g*G, both halves -> [half][head][64] in shared memory
+    const uint64_t qdims[5] = {64, static_cast<uint64_t>(a.Hq), 2, static_cast<uint64_t>(a.S),
+                               static_cast<uint64_t>(a.B)};
+    const uint64_t qstrides[4] = {static_cast<uint64_t>(a.Q_stride[2]) * 2, 128,
+                                  static_cast<uint64_t>(a.Q_stride[1]) * 2, static_cast<uint64_t>(a.Q_stride[0]) * 2};
+    const uint32_t qbox[5] = {64, 8, 2, 1, 1};
+    if (msa_status st = encode_tiled_map(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, a.Q, qdims, qstrides, qbox,
+                                         CU_TENSOR_MAP_SWIZZLE_128B, "Q");
+        st != MSA_OK)
+      return st;
+  }
   const uint64_t dims[4] = {static_cast<uint64_t>(a.D), static_cast<uint64_t>(a.Hkv), static_cast<uint64_t>(a.S),
                             static_cast<uint64_t>(a.B)};
   const uint32_t box[4] = {64, 1, 128, 1};
@@ -637,13 +770,12 @@ msa_status launch_attn_prefill(const msa_prefill_args& a, void* ws, size_t ws_by
         st != MSA_OK)
       return st;
   }
-  const size_t smem = 1024 + 2 * static_cast<size_t>(kKV) + 2 * static_cast<size_t>(kQStage);
+  const size_t smem = 1024 + 2 * static_cast<size_t>(kKV) + kQStages * static_cast<size_t>(kQStage);
   if (smem > dev.max_smem_optin) return fail(MSA_ERR_UNSUPPORTED, "prefill attention: not enough shared memory");
   cudaError_t e = cudaFuncSetAttribute(attn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attn_prefill)");
 
-  const int G = a.Hq / a.Hkv;
   const float scale = a.softmax_scale > 0.f ? a.softmax_scale : 1.0f / sqrtf(static_cast<float>(a.D));
   for (int64_t q0 = 0; q0 < total_q; q0 += cq) {
     const int nq = static_cast<int>(std::min<int64_t>(cq, total_q - q0));
@@ -655,8 +787,9 @@ msa_status launch_attn_prefill(const msa_prefill_args& a, void* ws, size_t ws_by
     c.cursor = reinterpret_cast<int32_t*>(w + L.cursor);
     c.off = reinterpret_cast<int32_t*>(w + L.off);
     c.tile_off = reinterpret_cast<int32_t*>(w + L.tile_off);
-    c.list = reinterpret_cast<int32_t*>(w + L.list);
-    c.lse_part = reinterpret_cast<float*>(w + L.lse_part);
+    c.tile_info = reinterpret_cast<int4*>(w + L.tile_info);
+    c.tile_q = reinterpret_cast<int32_t*>(w + L.tile_q);
+    c.where = reinterpret_cast<int32_t*>(w + L.where);
     c.dev_err = a.dev_err;
     e = cudaMemsetAsync(c.cnt, 0, n_items * 4, stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(prefill counts)");
@@ -667,22 +800,29 @@ msa_status launch_attn_prefill(const msa_prefill_args& a, void* ws, size_t ws_by
     csr_fill_kernel<<<grid_w, 256, 0, stream>>>(c);
 
     AttnParams p;
-    p.S = a.S; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = G; p.k = a.k; p.nb = static_cast<int>(nb);
-    p.q0 = q0; p.n_items = n_items;
+    p.S = a.S; p.Hkv = a.Hkv; p.G = G; p.nb = static_cast<int>(nb);
+    p.n_items = n_items;
     p.scale_log2 = scale * kLog2e;
-    p.Q = static_cast<const __nv_bfloat16*>(a.Q);
-    p.qs0 = a.Q_stride[0]; p.qs1 = a.Q_stride[1]; p.qs2 = a.Q_stride[2];
-    p.off = c.off; p.tile_off = c.tile_off; p.list = c.list;
+    p.tile_off = c.tile_off; p.tile_info = c.tile_info; p.tile_q = c.tile_q;
     p.o_part = reinterpret_cast<__nv_bfloat16*>(w + L.o_part);
-    p.lse_part = c.lse_part;
+    p.lse_part = reinterpret_cast<float*>(w + L.lse_part);
     p.dev_err = a.dev_err;
-    attn_prefill_kernel<<<dev.num_sms, kAttnThreads, smem, stream>>>(kmap, vmap, p);
+    attn_prefill_kernel<<<dev.num_sms, kAttnThreads, smem, stream>>>(qmap, kmap, vmap, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
-    msa_status st = launch_lse_merge_bf16(p.o_part, p.lse_part, static_cast<int64_t>(nq) * a.Hq, a.k, kD,
-                                          static_cast<__nv_bfloat16*>(a.O) + q0 * a.Hq * kD,
-                                          a.LSE != nullptr ? a.LSE + q0 * a.Hq : nullptr, stream);
-    if (st != MSA_OK) return st;
+
+    MergeParams mp;
+    mp.nq = nq; mp.Hq = a.Hq; mp.Hkv = a.Hkv; mp.G = G; mp.k = a.k;
+    mp.o_part = p.o_part; mp.lse_part = p.lse_part; mp.where = c.where;
+    mp.O = static_cast<__nv_bfloat16*>(a.O) + q0 * a.Hq * kD;
+    mp.LSE = a.LSE != nullptr ? a.LSE + q0 * a.Hq : nullptr;
+    const int64_t mgrid = (static_cast<int64_t>(nq) * a.Hq + kMergeWarps - 1) / kMergeWarps;
+    if (a.k <= 16)
+      prefill_merge_kernel<16><<<static_cast<unsigned>(mgrid), kMergeWarps * 32, 0, stream>>>(mp);
+    else
+      prefill_merge_kernel<64><<<static_cast<unsigned>(mgrid), kMergeWarps * 32, 0, stream>>>(mp);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "prefill merge launch");
   }
   return MSA_OK;
 }
