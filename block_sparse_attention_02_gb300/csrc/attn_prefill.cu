@@ -62,6 +62,7 @@ struct CsrParams {
   int32_t* cursor;      // [n_items]
   int32_t* off;         // [n_items + 1]
   int32_t* tile_off;    // [n_items + 1]
+  int32_t* ord;         // [n_items]: ordinal of the item among the non-empty ones
   int4* tile_info;      // [tiles]: item, entries, ordinal of the item, first/last flags
   int32_t* tile_q;      // [tiles * 16]: flattened query b*S+i of each tile entry
   int32_t* where;       // [nq, Hkv, k]: first tile row of the (query, g, slot) entry, -1 if empty
@@ -96,8 +97,7 @@ __global__ void csr_count_kernel(const CsrParams p) {
 
 __device__ __forceinline__ int tiles_of(int c) { return (c + kEntries - 1) / kEntries; }
 
-// single CTA: exclusive scans of entries, tiles and non-empty items; then the
-// per-item offsets and one descriptor per tile
+// single CTA: exclusive scans of entries, tiles and non-empty items
 __global__ void __launch_bounds__(1024) csr_scan_kernel(const CsrParams p, int64_t n_items) {
   __shared__ int64_t s_sum[32][3];
   const int tid = threadIdx.x;
@@ -148,19 +148,16 @@ __global__ void __launch_bounds__(1024) csr_scan_kernel(const CsrParams p, int64
     p.off[x] = static_cast<int32_t>(c);
     p.cursor[x] = static_cast<int32_t>(c);
     p.tile_off[x] = static_cast<int32_t>(t);
-    const int nt = tiles_of(v);
-    for (int u = 0; u < nt; ++u) {
-      const int flags = (u == 0 ? kTileFirst : 0) | (u == nt - 1 ? kTileLast : 0);
-      p.tile_info[t + u] = make_int4(static_cast<int>(x), min(kEntries, v - kEntries * u), static_cast<int>(z), flags);
-    }
+    p.ord[x] = static_cast<int32_t>(z);
     c += v;
-    t += nt;
+    t += tiles_of(v);
     z += v > 0;
   }
 }
 
 // one thread per (query in chunk, group, slot): claims the entry's place in its
-// item and writes the entry table and the slot map
+// item and writes the entry table and the slot map; the first entry of each
+// tile writes the tile's descriptor
 __global__ void csr_fill_kernel(const CsrParams p) {
   const int64_t total = static_cast<int64_t>(p.nq) * p.Hkv * p.k;
   for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
@@ -177,9 +174,15 @@ __global__ void csr_fill_kernel(const CsrParams p) {
     if (j < 0 || j > i / kBk) continue;
     const int64_t item = (static_cast<int64_t>(b) * p.Hkv + g) * p.nb + j;
     const int pos = atomicAdd(&p.cursor[item], 1);
-    const int es = p.tile_off[item] * kEntries + (pos - p.off[item]);   // entry slot in tile order
+    const int idx = pos - p.off[item];                                  // entry index within the item
+    const int es = p.tile_off[item] * kEntries + idx;                   // entry slot in tile order
     p.tile_q[es] = static_cast<int>(bs);
     p.where[e] = es * 8;                                                // tile row of head 0
+    if (idx % kEntries == 0) {
+      const int c = p.off[item + 1] - p.off[item], u = idx / kEntries, nt = tiles_of(c);
+      const int flags = (u == 0 ? kTileFirst : 0) | (u == nt - 1 ? kTileLast : 0);
+      p.tile_info[es / kEntries] = make_int4(static_cast<int>(item), min(kEntries, c - idx), p.ord[item], flags);
+    }
 
   }
 }
@@ -195,7 +198,7 @@ struct AttnParams {
   const int32_t* tile_off;   // tile_off[n_items] = number of tiles
   const int4* tile_info;
   const int32_t* tile_q;
-  __nv_bfloat16* o_part;     // [tiles * 128, D] bf16, tile order
+  __nv_bfloat16* o_part;     // [tiles][16 column chunks][128 rows][8] bf16
   float* lse_part;           // [tiles * 128]
   int32_t* dev_err;
 };
@@ -249,7 +252,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
   uint8_t* s_q = smem + 2 * kKV;           // [kQStages] x Q tile
 
   __shared__ __align__(8) uint64_t bar_qfull[kQStages], bar_qempty[kQStages], bar_kvfull[2], bar_kvempty[2];
-  __shared__ __align__(8) uint64_t bar_sfull[2], bar_pready[2], bar_ofull[2], bar_tfree[2], bar_drain;
+  __shared__ __align__(8) uint64_t bar_sfull[2], bar_pready[2], bar_ofull[2], bar_drain;
   __shared__ int s_kvinfo[kQStages];       // per Q stage: K/V buffer, new, release, phase (producer -> MMA)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -267,7 +270,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_kvfull[i], 1); mbar_init(&bar_kvempty[i], 1);
       mbar_init(&bar_sfull[i], 1); mbar_init(&bar_pready[i], 4);
-      mbar_init(&bar_ofull[i], 1); mbar_init(&bar_tfree[i], 4);
+      mbar_init(&bar_ofull[i], 1);
     }
     mbar_init(&bar_drain, 1);
     s_abort = 0;
@@ -373,8 +376,12 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ===================== tcgen05 issuer =====================
-    // S(n) and O(n) are issued as soon as their inputs are ready, in either
-    // order: S(n+1) never waits for P(n), O(n) never waits for Q(n+1).
+    // S(n) and O(n) are issued as soon as their inputs are ready, O first:
+    //   O(n) needs P(n) (pready); the warpgroup that arrives there has already
+    //   read O(n-2) out of the slot's accumulator;
+    //   S(n) needs Q(n), K_j, and O(n-2) complete: it overwrites the slot's S/P
+    //   columns, from which O(n-2) reads P (issue order alone does not order a
+    //   later MMA's TMEM writes after an earlier MMA's TMEM operand reads).
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_o = idesc_bf16(128, 128, false, true);
@@ -384,13 +391,28 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
       uint32_t spins = 0;
       while (no < ntiles) {
         bool progress = false;
+        if (no < ns) {
+          const int slot = no & 1;
+          if (mbar_test_wait(&bar_pready[slot], (no >> 1) & 1)) {
+            tc_fence_after();
+            const int kv = kvinfo[slot];
+            const uint32_t vb = smem_u32(s_kv + (kv & 1) * kKV + 2 * kHalf);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              umma_bf16_ts(tmem + slot * 256 + 128, tmem + slot * 256 + kk * 8,
+                           sdesc_sw128(vb + kk * 2048, kHalf, 1024), idesc_o, kk > 0);
+            umma_commit(&bar_ofull[slot]);
+            if (kv & 4) umma_commit(&bar_kvempty[kv & 1]);
+            ++no;
+            progress = true;
+          }
+        }
         if (ns < ntiles && ns < no + 2) {
           const int st = ns % kQStages, slot = ns & 1;
-          if (mbar_test_wait(&bar_qfull[st], (ns / kQStages) & 1)) {
+          if ((ns < 2 || mbar_test_wait(&bar_ofull[slot], ((ns - 2) >> 1) & 1)) &&
+              mbar_test_wait(&bar_qfull[st], (ns / kQStages) & 1)) {
             const int kv = s_kvinfo[st];
-            bool ready = !(kv & 2) || mbar_test_wait(&bar_kvfull[kv & 1], (kv >> 3) & 1);
-            ready = ready && mbar_test_wait(&bar_tfree[slot], ((ns >> 1) & 1) ^ 1);
-            if (ready) {
+            if (!(kv & 2) || mbar_test_wait(&bar_kvfull[kv & 1], (kv >> 3) & 1)) {
               tc_fence_after();
               const uint32_t qb = smem_u32(s_q + st * kQStage);
               const uint32_t kb = smem_u32(s_kv + (kv & 1) * kKV);
@@ -406,22 +428,6 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
               ++ns;
               progress = true;
             }
-          }
-        }
-        if (no < ns) {
-          const int slot = no & 1;
-          if (mbar_test_wait(&bar_pready[slot], (no >> 1) & 1)) {
-            tc_fence_after();
-            const int kv = kvinfo[slot];
-            const uint32_t vb = smem_u32(s_kv + (kv & 1) * kKV + 2 * kHalf);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              umma_bf16_ts(tmem + slot * 256 + 128, tmem + slot * 256 + kk * 8,
-                           sdesc_sw128(vb + kk * 2048, kHalf, 1024), idesc_o, kk > 0);
-            umma_commit(&bar_ofull[slot]);
-            if (kv & 4) umma_commit(&bar_kvempty[kv & 1]);
-            ++no;
-            progress = true;
           }
         }
         if (progress) {
@@ -558,18 +564,15 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
       const float inv = 1.0f / l;
       const uint64_t inv2 = pack2f(inv, inv);
       const int64_t prow = (t0 + n) * 128 + r;
-      __nv_bfloat16* orow = p.o_part + prow * kD;
+      // partial layout inside a tile: [16-byte column chunk][row]: each store
+      // of a warp covers 32 consecutive rows of one chunk, 512 contiguous bytes
+      __nv_bfloat16* obase = p.o_part + ((t0 + n) * 16 * 128 + r) * 8;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t v[2][32];
         tmem_ld32(sbase + 128 + hh * 64, v[0]);
         tmem_ld32(sbase + 128 + hh * 64 + 32, v[1]);
         tmem_ld_wait();
-        if (hh == 1) {                               // O is in registers: the slot may be reused
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bar_tfree[slot]);
-        }
         if (valid) {
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
@@ -583,11 +586,15 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
                          a0, a1);
                 w4[x] = pack_bf16x2(a0, a1);
               }
-              st_cs_v4(orow + hh * 64 + c * 32 + e8, w4[0], w4[1], w4[2], w4[3]);
+              const int chunk = hh * 8 + c * 4 + (e8 >> 3);
+              st_cs_v4(obase + chunk * 128 * 8, w4[0], w4[1], w4[2], w4[3]);
             }
           }
         }
       }
+      // the loads above are complete (wait::ld): ordered before this
+      // warpgroup's next pready arrive, which gates O(n+2) into this slot
+      tc_fence_before();
       if (valid) __stcs(p.lse_part + prow, (m + log2f(l)) * kLn2);
     }
   }
@@ -602,7 +609,9 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
 
 // ---------------------------------------------------------------------------
 // merge: O = sum_s e^{LSE_s - LSE} O_s, LSE = ln sum_s e^{LSE_s} over the k
-// slots of each (query, head); one warp per (query, head)
+// slots of each (query, head).  One warp per (query, group): lane L owns head
+// h = L % 8 (idle if h >= G) and the column chunks c = L / 8 + 4x, x = 0..3,
+// so that for each part the 8 lanes of a chunk read its 8 contiguous rows.
 // ---------------------------------------------------------------------------
 
 constexpr int kMergeWarps = 8;
@@ -616,74 +625,99 @@ struct MergeParams {
   float* LSE;            // chunk's first LSE (or null)
 };
 
-__device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
-  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+__device__ __forceinline__ void fma8(float (&acc)[8], float w, uint4 raw) {
+  const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[i]));
+    acc[2 * i] = fmaf(w, f.x, acc[2 * i]);
+    acc[2 * i + 1] = fmaf(w, f.y, acc[2 * i + 1]);
+  }
 }
 
-// KMAX = 16: every partial load of the row in flight at once (k <= 16);
-// KMAX = 64: a loop over the slots, two per lane.
+// KMAX = 16 or 64 (k <= KMAX): lane (c0, h) also owns slots s = c0 + 4y.
 template <int KMAX>
-__global__ void __launch_bounds__(kMergeWarps * 32) prefill_merge_kernel(const MergeParams p) {
+__global__ void __launch_bounds__(kMergeWarps * 32, 2) prefill_merge_kernel(const MergeParams p) {
+  constexpr int SPL = KMAX / 4;              // slots per lane
   const int lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
-  if (row >= static_cast<int64_t>(p.nq) * p.Hq) return;
-  const int qi = static_cast<int>(row / p.Hq), hq = static_cast<int>(row % p.Hq);
-  const int g = hq / p.G, h = hq - g * p.G;
-  const int32_t* wp = p.where + (static_cast<int64_t>(qi) * p.Hkv + g) * p.k;
-  const int base0 = lane < p.k ? wp[lane] : -1;
-  const int base1 = (KMAX > 32 && lane + 32 < p.k) ? wp[lane + 32] : -1;
-  const float l0 = base0 >= 0 ? __ldcs(p.lse_part + base0 + h) : -INFINITY;
-  const float l1 = base1 >= 0 ? __ldcs(p.lse_part + base1 + h) : -INFINITY;
-  __nv_bfloat16* orow = p.O + row * kD + lane * 4;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float m = fmaxf(l0, l1);
+  const int64_t wq = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
+  if (wq >= static_cast<int64_t>(p.nq) * p.Hkv) return;
+  const int qi = static_cast<int>(wq / p.Hkv), g = static_cast<int>(wq % p.Hkv);
+  const int h = lane & 7, c0 = lane >> 3;
+  const bool live = h < p.G;
+  const int32_t* wp = p.where + wq * p.k;
+  int base[SPL];
+  float wgt[SPL];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if (m == -INFINITY) {
-    *reinterpret_cast<uint2*>(orow) = make_uint2(0, 0);
-    if (lane == 0 && p.LSE != nullptr) p.LSE[row] = -INFINITY;
-    return;
+  for (int y = 0; y < SPL; ++y) base[y] = c0 + 4 * y < p.k ? wp[c0 + 4 * y] : -1;
+#pragma unroll
+  for (int y = 0; y < SPL; ++y) wgt[y] = live && base[y] >= 0 ? __ldcs(p.lse_part + base[y] + h) : -INFINITY;
+  // this head's maximum and sum over its slots (the 4 lanes of head h)
+  float m = -INFINITY;
+#pragma unroll
+  for (int y = 0; y < SPL; ++y) m = fmaxf(m, wgt[y]);
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+  float sum = 0.f;
+#pragma unroll
+  for (int y = 0; y < SPL; ++y) {
+    wgt[y] = wgt[y] == -INFINITY ? 0.f : __expf(wgt[y] - m);
+    sum += wgt[y];
   }
-  const float e0 = l0 == -INFINITY ? 0.f : __expf(l0 - m);
-  const float e1 = l1 == -INFINITY ? 0.f : __expf(l1 - m);
-  float sum = e0 + e1;
+  sum += __shfl_xor_sync(0xffffffffu, sum, 8);
+  sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+  // a head with no visible key (impossible for a valid selection) gets zeros, LSE = -inf
+  const float inv = sum > 0.f ? 1.0f / sum : 0.f;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  const float w0 = e0 / sum, w1 = e1 / sum;
-  auto fma4 = [&](float wgt, uint2 raw) {
-    const float2 a = bf2_to_f2(raw.x), b = bf2_to_f2(raw.y);
-    acc.x = fmaf(wgt, a.x, acc.x);
-    acc.y = fmaf(wgt, a.y, acc.y);
-    acc.z = fmaf(wgt, b.x, acc.z);
-    acc.w = fmaf(wgt, b.y, acc.w);
-  };
-  if (KMAX <= 16) {
-    uint2 raw[16];
+  for (int y = 0; y < SPL; ++y) wgt[y] *= inv;
+  float acc[4][8];
 #pragma unroll
-    for (int s = 0; s < 16; ++s) {
-      const int bs = __shfl_sync(0xffffffffu, base0, s);
-      raw[s] = bs >= 0 ? __ldcs(reinterpret_cast<const uint2*>(p.o_part + static_cast<int64_t>(bs + h) * kD) + lane)
-                       : make_uint2(0, 0);
+  for (int x = 0; x < 4; ++x)
+#pragma unroll
+    for (int z = 0; z < 8; ++z) acc[x][z] = 0.f;
+  // slots 4y .. 4y+3 together: 16 loads of 16 B in flight per lane
+#pragma unroll
+  for (int y = 0; y < SPL; ++y) {
+    if (4 * y >= p.k) break;
+    uint4 raw[4][4];
+    float w4[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int src_lane = u * 8 + h;        // lane (c0 = u, h) owns slot 4y + u
+      w4[u] = __shfl_sync(0xffffffffu, wgt[y], src_lane);
+      const int b = __shfl_sync(0xffffffffu, base[y], src_lane);
+      if (live && b >= 0 && w4[u] != 0.f) {
+        const int64_t t = b >> 7, r = (b & 127) + h;
+        const __nv_bfloat16* src = p.o_part + ((t * 16 + c0) * 128 + r) * 8;
+#pragma unroll
+        for (int x = 0; x < 4; ++x) raw[u][x] = __ldcs(reinterpret_cast<const uint4*>(src + x * 4 * 128 * 8));
+      } else {
+        w4[u] = 0.f;
+      }
     }
 #pragma unroll
-    for (int s = 0; s < 16; ++s) {
-      const float ws = __shfl_sync(0xffffffffu, w0, s);
-      if (ws != 0.f) fma4(ws, raw[s]);
-    }
-  } else {
-    for (int s = 0; s < p.k; ++s) {
-      const int bs = __shfl_sync(0xffffffffu, s < 32 ? base0 : base1, s & 31);
-      const float ws = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
-      if (bs >= 0 && ws != 0.f)
-        fma4(ws, __ldcs(reinterpret_cast<const uint2*>(p.o_part + static_cast<int64_t>(bs + h) * kD) + lane));
-    }
+    for (int u = 0; u < 4; ++u)
+      if (w4[u] != 0.f)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) fma8(acc[x], w4[u], raw[u][x]);
   }
-  *reinterpret_cast<uint2*>(orow) = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
-  if (lane == 0 && p.LSE != nullptr) p.LSE[row] = m + __logf(sum);
+  if (live) {
+    const int64_t orow = (static_cast<int64_t>(qi) * p.Hq + g * p.G + h) * kD;
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      uint4 o;
+      o.x = pack_bf16x2(acc[x][0], acc[x][1]);
+      o.y = pack_bf16x2(acc[x][2], acc[x][3]);
+      o.z = pack_bf16x2(acc[x][4], acc[x][5]);
+      o.w = pack_bf16x2(acc[x][6], acc[x][7]);
+      *reinterpret_cast<uint4*>(p.O + orow + (c0 + 4 * x) * 8) = o;
+    }
+    if (c0 == 0 && p.LSE != nullptr) p.LSE[qi * p.Hq + g * p.G + h] = sum > 0.f ? m + __logf(sum) : -INFINITY;
+  }
 }
 
 struct WsLayout {
-  size_t cnt, cursor, off, tile_off, tile_info, tile_q, where, o_part, lse_part, total;
+  size_t cnt, cursor, off, tile_off, ord, tile_info, tile_q, where, o_part, lse_part, total;
   int64_t max_tiles;
 };
 
@@ -702,6 +736,7 @@ WsLayout ws_layout(const msa_prefill_args& a, int64_t cq) {
   L.cursor = o; o = al(o + n_items * 4);
   L.off = o; o = al(o + (n_items + 1) * 4);
   L.tile_off = o; o = al(o + (n_items + 1) * 4);
+  L.ord = o; o = al(o + n_items * 4);
   L.tile_info = o; o = al(o + static_cast<size_t>(L.max_tiles) * 16);
   L.tile_q = o; o = al(o + static_cast<size_t>(L.max_tiles) * kEntries * 4);
   L.where = o; o = al(o + static_cast<size_t>(entries) * 4);
@@ -787,6 +822,7 @@ msa_status launch_attn_prefill(const msa_prefill_args& a, void* ws, size_t ws_by
     c.cursor = reinterpret_cast<int32_t*>(w + L.cursor);
     c.off = reinterpret_cast<int32_t*>(w + L.off);
     c.tile_off = reinterpret_cast<int32_t*>(w + L.tile_off);
+    c.ord = reinterpret_cast<int32_t*>(w + L.ord);
     c.tile_info = reinterpret_cast<int4*>(w + L.tile_info);
     c.tile_q = reinterpret_cast<int32_t*>(w + L.tile_q);
     c.where = reinterpret_cast<int32_t*>(w + L.where);
@@ -816,7 +852,7 @@ msa_status launch_attn_prefill(const msa_prefill_args& a, void* ws, size_t ws_by
     mp.o_part = p.o_part; mp.lse_part = p.lse_part; mp.where = c.where;
     mp.O = static_cast<__nv_bfloat16*>(a.O) + q0 * a.Hq * kD;
     mp.LSE = a.LSE != nullptr ? a.LSE + q0 * a.Hq : nullptr;
-    const int64_t mgrid = (static_cast<int64_t>(nq) * a.Hq + kMergeWarps - 1) / kMergeWarps;
+    const int64_t mgrid = (static_cast<int64_t>(nq) * a.Hkv + kMergeWarps - 1) / kMergeWarps;
     if (a.k <= 16)
       prefill_merge_kernel<16><<<static_cast<unsigned>(mgrid), kMergeWarps * 32, 0, stream>>>(mp);
     else
