@@ -14,12 +14,14 @@
 //   warp 0    TMA: the HI q_idx tiles of the item (128 queries x 64, one per
 //             index head, double-buffered across items) and a 4-deep ring of
 //             k_idx blocks (128 tokens x 64), all 128-byte swizzled;
-//   warp 1    tcgen05: per key block and half (64 tokens), one MMA chain per
-//             head, D_h[query, token] = q_idx_h . k_idx  (M=128, N=64, K=64)
-//             into a 256-column TMEM buffer (4 heads x 64); two buffers;
+//   warp 1    tcgen05: per key block, passes of two index heads:
+//             D_h[query, token] = q_idx_h . k_idx  (M=128, N=128, K=64) for
+//             both heads into a 256-column TMEM buffer, the two MMA chains
+//             interleaved step by step (a single accumulation chain leaves the
+//             tensor core waiting on its own results); two buffers;
 //   warps 2-5 epilogue, thread = query: acc_t = sum_h w_h ReLU(D_h[t]) with
-//             packed fp32 FMAs, running max over the block's 128 tokens, one
-//             store per (query, block).
+//             packed fp32 FMAs, carried across the passes in registers, then
+//             the max over the block's 128 tokens, one store per (query, block).
 #include "msa_internal.h"
 #include "msa_ptx.cuh"
 
@@ -30,7 +32,7 @@ constexpr int kThreads = 192;
 constexpr int kTile = 128 * 64 * 2;            // 16 KiB: 128 rows x 64 bf16
 constexpr int kKStages = 4;
 constexpr int kTmemCols = 512;
-constexpr int kBufCols = 256;                  // one TMEM buffer: 4 heads x 64 tokens
+constexpr int kBufCols = 256;                  // one TMEM buffer: 2 heads x 128 tokens
 
 struct Params {
   int B, S, Hkv, HI, nbq, nb_stride;
@@ -152,7 +154,8 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
   } else if (warp == 1) {
     // ===================== tcgen05 issuer =====================
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(128, 64, false, false);
+      constexpr uint32_t idesc = idesc_bf16(128, 128, false, false);
+      const int npass = (p.HI + 1) / 2;
       int na = 0, nk = 0, nt = 0;
       bool ok = true;
       for (int64_t pr = blockIdx.x; pr < npairs && ok; pr += gridDim.x) {
@@ -168,16 +171,16 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
             const int st = nk % kKStages;
             if (!(ok = mbar_wait(&bar_kfull[st], (nk / kKStages) & 1, abort_flag, p.dev_err))) break;
             const uint32_t kbase = smem_u32(s_k + st * kTile);
-            for (int hf = 0; hf < 2; ++hf) {
+            for (int ps = 0; ps < npass; ++ps) {
               const int buf = nt & 1;
               if (!(ok = mbar_wait(&bar_tempty[buf], ((nt >> 1) & 1) ^ 1, abort_flag, p.dev_err))) break;
               tc_fence_after();
-              for (int h = 0; h < p.HI; ++h) {
+              const int h0 = 2 * ps, nh = min(2, p.HI - h0);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                  umma_bf16(tmem + buf * kBufCols + h * 64, sdesc_sw128(abase + h * kTile + 32 * kk, 16, 1024),
-                            sdesc_sw128(kbase + hf * 8192 + 32 * kk, 16, 1024), idesc, kk > 0);
-              }
+              for (int kk = 0; kk < 4; ++kk)
+                for (int hh = 0; hh < nh; ++hh)
+                  umma_bf16(tmem + buf * kBufCols + hh * 128, sdesc_sw128(abase + (h0 + hh) * kTile + 32 * kk, 16, 1024),
+                            sdesc_sw128(kbase + 32 * kk, 16, 1024), idesc, kk > 0);
               umma_commit(&bar_tfull[buf]);
               ++nt;
             }
@@ -226,43 +229,37 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
           }
           __syncwarp();
         };
+        const int npass = (p.HI + 1) / 2;
         for (int j = 0; j < it.qb; ++j) {
-          float m = -INFINITY;
-          for (int hf = 0; hf < 2; ++hf) {
+          // acc[t/2] = sum over heads of w_h ReLU(D_h[query, t]) for t = 2e, 2e+1 (packed)
+          uint64_t acc[64];
+#pragma unroll
+          for (int e = 0; e < 64; ++e) acc[e] = 0ull;
+#pragma unroll
+          for (int ps = 0; ps < (kMaxHI + 1) / 2; ++ps) {
+            if (ps >= npass) break;
             const int buf = nt & 1;
             // warp-uniform decision: the TMEM loads below are warp-collective
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar_tfull[buf], (nt >> 1) & 1, abort_flag, p.dev_err))))
               break;
             tc_fence_after();
             const uint32_t base = tmem + lane_addr + buf * kBufCols;
+            const bool two = 2 * ps + 1 < p.HI;
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-              uint64_t acc[16];
-#pragma unroll
-              for (int e = 0; e < 16; ++e) acc[e] = 0ull;
-              // issue the loads of every head, then wait once
-              uint32_t v[kMaxHI][32];
-#pragma unroll
-              for (int h = 0; h < kMaxHI; ++h)
-                if (h < p.HI) tmem_ld32(base + h * 64 + cc * 32, v[h]);
+            for (int cc = 0; cc < 4; ++cc) {
+              uint32_t v[2][32];
+              tmem_ld32(base + cc * 32, v[0]);
+              if (two) tmem_ld32(base + 128 + cc * 32, v[1]);
               tmem_ld_wait();
 #pragma unroll
-              for (int h = 0; h < kMaxHI; ++h) {
-                if (h < p.HI) {
+              for (int hh = 0; hh < 2; ++hh) {
+                if (hh == 1 && !two) break;
 #pragma unroll
-                  for (int e = 0; e < 16; ++e) {
-                    const uint64_t rl = pack2(fmaxf(__uint_as_float(v[h][2 * e]), 0.f),
-                                              fmaxf(__uint_as_float(v[h][2 * e + 1]), 0.f));
-                    acc[e] = fma2(w2[h], rl, acc[e]);
-                  }
+                for (int e = 0; e < 16; ++e) {
+                  const uint64_t rl = pack2(fmaxf(__uint_as_float(v[hh][2 * e]), 0.f),
+                                            fmaxf(__uint_as_float(v[hh][2 * e + 1]), 0.f));
+                  acc[cc * 16 + e] = fma2(w2[2 * ps + hh], rl, acc[cc * 16 + e]);
                 }
-              }
-#pragma unroll
-              for (int e = 0; e < 16; e += 2) {
-                float a0, a1, b0, b1;
-                unpack2(acc[e], a0, a1);
-                unpack2(acc[e + 1], b0, b1);
-                m = max3(m, max3(a0, a1, b0), b1);
               }
             }
             tc_fence_before();
@@ -271,6 +268,14 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
             ++nt;
           }
           if (!ok) break;
+          float m = -INFINITY;
+#pragma unroll
+          for (int e = 0; e < 64; e += 2) {
+            float a0, a1, b0, b1;
+            unpack2(acc[e], a0, a1);
+            unpack2(acc[e + 1], b0, b1);
+            m = max3(m, max3(a0, a1, b0), b1);
+          }
           s_cst[r][j & 31] = m;
           if ((j & 31) == 31 || j == it.qb - 1) flush(j & ~31, (j & 31) + 1);
         }
