@@ -128,35 +128,6 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const void* map, uint64_t
       : "memory");
 }
 
-// The same loads with an L2 eviction policy (from createpolicy).
-__device__ __forceinline__ void tma_load_4d_hint(void* dst, const void* map, uint64_t* bar, int c0, int c1, int c2,
-                                                 int c3, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_5d_hint(void* dst, const void* map, uint64_t* bar, int c0, int c1, int c2,
-                                                 int c3, int c4, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
-      "l"(policy)
-      : "memory");
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-
 // ---------------------------------------------------------------------------
 // tcgen05 / TMEM (cta_group::1)
 // ---------------------------------------------------------------------------
