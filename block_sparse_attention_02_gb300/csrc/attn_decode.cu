@@ -22,7 +22,9 @@
 //                                          V is the MN-major A operand
 //   epilogue: one thread per d, coalesced fp32 partial rows.
 // Warp 0 streams K, V (64 KiB) and the row's 16 Q rows by TMA into a 3-deep
-// ring; warp 1 issues the MMAs; warps 2-5 run softmax, epilogue and merge.
+// ring; warp 1 issues the MMAs (S of the next unit before O of this one);
+// warps 2-5 and 6-9 are two softmax/epilogue warpgroups taking alternate
+// units, each with its own TMEM slot, and merge the rows they complete.
 // Each CTA first copies its units' page ids and valid lengths into shared
 // memory, so no role waits on a global load per unit.
 #include "msa_internal.h"

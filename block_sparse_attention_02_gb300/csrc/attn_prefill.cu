@@ -380,8 +380,9 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
     //   O(n) needs P(n) (pready); the warpgroup that arrives there has already
     //   read O(n-2) out of the slot's accumulator;
     //   S(n) needs Q(n), K_j, and O(n-2) complete: it overwrites the slot's S/P
-    //   columns, from which O(n-2) reads P (issue order alone does not order a
-    //   later MMA's TMEM writes after an earlier MMA's TMEM operand reads).
+    //   columns, from which O(n-2) reads P (waiting for the completion barrier
+    //   rather than relying on issue order between an MMA's TMEM operand read
+    //   and a later MMA's TMEM write).
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_o = idesc_bf16(128, 128, false, true);

@@ -9,17 +9,20 @@
 // in blocks; the formula is this library's, the pages give none.)
 //
 // This is an HBM stream: each (page, group) block of k_idx is 16 KiB, read
-// once.  A persistent CTA per SM walks a contiguous range of the flattened
-// (b, g, j) items:
+// once.  Two persistent CTAs per SM each walk a contiguous range of the
+// flattened (b, g, j) items:
 //   warp 0    TMA producer: one 4-D tiled load (128 tokens x 64 dims, 128-byte
-//             swizzle) per block into a 12-deep shared-memory ring, page ids
+//             swizzle) per block into a 6-deep shared-memory ring, page ids
 //             fetched 32 at a time by the whole warp;
 //   warp 1    tcgen05 issuer: D[t, h] = k_idx_t . q_idx_h as one M=128 (tokens)
 //             x N=16 (index heads, zero-padded) x K=64 contraction (4 MMAs)
-//             into one of 16 TMEM slots; it also stages q_idx of the current
+//             into one of 8 TMEM slots; it also stages q_idx of the current
 //             (b, g) as the B operand (double-buffered);
 //   warps 2-5 epilogue: thread = token; w-weighted ReLU sum over heads, max
 //             over the block's 128 tokens, one fp32 store per block.
+// With the optional fused selection, the CTA that completes a (b, g) row
+// (per-row completion counter) then selects its top-k blocks and writes the
+// row's page table, using the idle ring as scratch.
 #include "msa_internal.h"
 #include "msa_ptx.cuh"
 #include "select_warp.cuh"
