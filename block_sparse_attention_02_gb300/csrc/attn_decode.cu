@@ -78,8 +78,6 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
   __shared__ int s_uvalid[kMaxUnits];   // valid tokens of the page; 0 = no such split
   __shared__ int s_un[kMaxUnits];       // selected pages of the unit's row
   __shared__ int s_last[2], s_fail[2];
-  __shared__ float s_mlse[2][kMaxG][kMaxK];   // merge: LSE of each (head, split) of the row
-  __shared__ float s_mm[2][kMaxG], s_minv[2][kMaxG];
   __shared__ short s_live[kMaxUnits];         // offsets of the live units of this CTA, in order
   __shared__ int s_nlive;
 
@@ -248,36 +246,56 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
       if (!s_last[wg]) return;
       __threadfence();
       const int r = cur_r, nr = cur_nr;
-      for (int e = t; e < G * nr; e += 128) {
-        const int h = e / nr, x = e % nr;
-        s_mlse[wg][h][x] = __ldcg(p.lse_part + (static_cast<int64_t>(r) * G + h) * p.k + x);
-      }
-      named_bar_sync(bar_id, 128);
-      if (t < G) {
-        float m = -INFINITY;
-        for (int x = 0; x < nr; ++x) m = fmaxf(m, s_mlse[wg][t][x]);
-        float sum = 0.f;
-        if (m != -INFINITY)
-          for (int x = 0; x < nr; ++x) sum += s_mlse[wg][t][x] == -INFINITY ? 0.f : __expf(s_mlse[wg][t][x] - m);
-        s_mm[wg][t] = m;
-        s_minv[wg][t] = m == -INFINITY ? 0.f : 1.0f / sum;
-        if (p.LSE != nullptr) p.LSE[static_cast<int64_t>(r) * G + t] = m == -INFINITY ? -INFINITY : m + __logf(sum);
-      }
-      named_bar_sync(bar_id, 128);
-      for (int h = 0; h < G; ++h) {           // thread = d; all partial loads independent
+      // warp q merges heads q and q+4 (G <= 8); lane l owns d = 4l .. 4l+3.
+      // A head's split LSEs (one per lane) and its first 16 partial rows
+      // (float4 per lane) are loaded together; max, sum and weights by shuffles.
+      const int lq = t >> 5, ll = t & 31;
+#pragma unroll
+      for (int hi = 0; hi < 2; ++hi) {
+        const int h = lq + 4 * hi;
+        if (h >= G) break;                     // warp-uniform
         const int64_t row = static_cast<int64_t>(r) * G + h;
-        const float m = s_mm[wg][h], inv = s_minv[wg][h];
-        float acc = 0.f;
-#pragma unroll 8
-        for (int x = 0; x < nr; ++x) {
-          const float lx = s_mlse[wg][h][x];
-          const float wgt = (lx == -INFINITY) ? 0.f : __expf(lx - m) * inv;
-          acc = fmaf(wgt, __ldcg(p.o_part + (row * p.k + x) * kD + t), acc);
+        const float* lrow = p.lse_part + row * p.k;
+        const float* orow = p.o_part + row * p.k * kD;
+        const float l0 = ll < nr ? __ldcg(lrow + ll) : -INFINITY;
+        const float l1 = ll + 32 < nr ? __ldcg(lrow + ll + 32) : -INFINITY;
+        float4 v[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x)
+          v[x] = __ldcg(reinterpret_cast<const float4*>(orow + static_cast<int64_t>(min(x, nr - 1)) * kD) + ll);
+        float m = fmaxf(l0, l1);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const float e0 = l0 == -INFINITY ? 0.f : __expf(l0 - m);
+        const float e1 = l1 == -INFINITY ? 0.f : __expf(l1 - m);
+        float sum = e0 + e1;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        const float inv = sum > 0.f ? 1.0f / sum : 0.f;
+        const float w0 = e0 * inv, w1 = e1 * inv;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+          const float wgt = __shfl_sync(0xffffffffu, w0, x);   // 0 for x >= nr
+          acc.x = fmaf(wgt, v[x].x, acc.x);
+          acc.y = fmaf(wgt, v[x].y, acc.y);
+          acc.z = fmaf(wgt, v[x].z, acc.z);
+          acc.w = fmaf(wgt, v[x].w, acc.w);
         }
-        p.O[row * kD + t] = __float2bfloat16_rn(acc);
+        for (int x = 16; x < nr; ++x) {        // k > 16
+          const float wgt = __shfl_sync(0xffffffffu, x < 32 ? w0 : w1, x & 31);
+          const float4 u = __ldcg(reinterpret_cast<const float4*>(orow + static_cast<int64_t>(x) * kD) + ll);
+          acc.x = fmaf(wgt, u.x, acc.x);
+          acc.y = fmaf(wgt, u.y, acc.y);
+          acc.z = fmaf(wgt, u.z, acc.z);
+          acc.w = fmaf(wgt, u.w, acc.w);
+        }
+        __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x, acc.y), hi2 = __floats2bfloat162_rn(acc.z, acc.w);
+        *reinterpret_cast<uint2*>(p.O + row * kD + 4 * ll) =
+            make_uint2(*reinterpret_cast<uint32_t*>(&lo2), *reinterpret_cast<uint32_t*>(&hi2));
+        if (ll == 0 && p.LSE != nullptr) p.LSE[row] = sum > 0.f ? m + __logf(sum) : -INFINITY;
       }
       if (t == 0) p.counter[r] = 0;           // ready for the next call
-      named_bar_sync(bar_id, 128);            // s_mlse / s_mm are reused
     };
     for (int n = wg; n < nlive; n += 2) {
       const int64_t u = lo + s_live[n];
