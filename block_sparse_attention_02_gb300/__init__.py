@@ -69,7 +69,8 @@ def msa_index_score(mode: int, q_idx: torch.Tensor, w: torch.Tensor, k_idx: torc
                     dev_err: Optional[torch.Tensor] = None, stream=None, k: int = 0,
                     sel: Optional[torch.Tensor] = None, count: Optional[torch.Tensor] = None,
                     pt: Optional[torch.Tensor] = None, n: Optional[torch.Tensor] = None,
-                    last_len: Optional[torch.Tensor] = None, row_scratch: Optional[torch.Tensor] = None) -> None:
+                    last_len: Optional[torch.Tensor] = None, row_scratch: Optional[torch.Tensor] = None,
+                    scratch_zeroed: bool = False) -> None:
     """Block scores of the Index Branch into ``C_out`` (see msa.h, a1).
 
     PREFILL: q_idx [B,S,Hkv,HI,dI], w [B,S,Hkv,HI], k_idx [B,S,Hkv,dI], C_out [B,S,Hkv,nb_stride].
@@ -77,7 +78,8 @@ def msa_index_score(mode: int, q_idx: torch.Tensor, w: torch.Tensor, k_idx: torc
              seq_pt [B,max_pages] int32 (contiguous rows), seq_len [B] int32.
     DECODE with ``sel`` given: the same call also selects (a2) into sel/count and,
     with ``pt`` given, builds the page table (a3) into pt/n/last_len; ``row_scratch``
-    is B*Hkv int32 of scratch.
+    is B*Hkv int32 of scratch, cleared by the call unless ``scratch_zeroed`` says
+    it is already zero (every error-free call leaves it zero).
     """
     for t, nm in ((q_idx, "q_idx"), (w, "w"), (k_idx, "k_idx"), (C_out, "C")):
         _inner_contig(t, nm)
@@ -109,6 +111,7 @@ def msa_index_score(mode: int, q_idx: torch.Tensor, w: torch.Tensor, k_idx: torc
                 if t is None or not t.is_contiguous():
                     raise ValueError(f"fused selection: {nm} must be a contiguous tensor")
             a.k, a.sel, a.count, a.row_scratch = k, _ptr(sel), _ptr(count), _ptr(row_scratch)
+            a.scratch_zeroed = int(bool(scratch_zeroed))
             if pt is not None:
                 a.pt, a.n, a.last_len = _ptr(pt), _ptr(n), _ptr(last_len)
     _abi.check(lib().msa_index_score(C.byref(a), _stream(stream)), "msa_index_score")
@@ -229,11 +232,16 @@ def msa_sparse_attn_decode_workspace_size(B: int, Hq: int, Hkv: int, k: int, D_:
 
 
 def msa_sparse_attn_decode(Q, K_pool, V_pool, pt, n, last_len, O, LSE, ws: torch.Tensor, *,
-                           softmax_scale: float = 0.0, dev_err=None, stream=None) -> None:
-    """Paged sparse attention of one decode step over the flattened page table (see msa.h, a5-a6)."""
+                           softmax_scale: float = 0.0, dev_err=None, stream=None,
+                           scratch_zeroed: bool = False) -> None:
+    """Paged sparse attention of one decode step over the flattened page table (see msa.h, a5-a6).
+
+    The workspace's row counters are cleared by the call unless ``scratch_zeroed``
+    says they are already zero (every error-free call leaves them zero)."""
     if not (pt.is_contiguous() and n.is_contiguous() and last_len.is_contiguous() and O.is_contiguous()):
         raise ValueError("pt, n, last_len and O must be contiguous")
     a = _decode_args(Q, K_pool, V_pool, pt, n, last_len, O, LSE, softmax_scale, dev_err)
+    a.scratch_zeroed = int(bool(scratch_zeroed))
     _abi.check(lib().msa_sparse_attn_decode(C.byref(a), _ptr(ws), ws.numel() * ws.element_size(),
                                             _stream(stream)), "msa_sparse_attn_decode")
 
@@ -265,7 +273,10 @@ def msa_lse_merge(O_part: torch.Tensor, LSE_part: torch.Tensor, O: torch.Tensor,
 # ---------------------------------------------------------------------------
 
 def decode_buffers(B: int, Hq: int, Hkv: int, k: int, nb_stride: int, device) -> Dict[str, torch.Tensor]:
-    """Output and scratch buffers of one decode step (allocated by torch, owned by the caller)."""
+    """Output and scratch buffers of one decode step (allocated by torch, owned by the caller).
+
+    The scratch (``ws``, ``row_scratch``) is zero-filled, so calls may pass
+    ``scratch_zeroed=True`` from the first one on."""
     dev = torch.device(device)
     return {
         "C": torch.empty(B, Hkv, nb_stride, dtype=torch.float32, device=dev),
@@ -276,20 +287,23 @@ def decode_buffers(B: int, Hq: int, Hkv: int, k: int, nb_stride: int, device) ->
         "last_len": torch.empty(B * Hkv, dtype=torch.int32, device=dev),
         "O": torch.empty(B, Hq, D, dtype=torch.bfloat16, device=dev),
         "LSE": torch.empty(B, Hq, dtype=torch.float32, device=dev),
-        "ws": torch.empty(msa_sparse_attn_decode_workspace_size(B, Hq, Hkv, k) // 4 + 64, dtype=torch.float32,
+        "ws": torch.zeros(msa_sparse_attn_decode_workspace_size(B, Hq, Hkv, k) // 4 + 64, dtype=torch.float32,
                           device=dev),
-        "row_scratch": torch.empty(B * Hkv, dtype=torch.int32, device=dev),
+        "row_scratch": torch.zeros(B * Hkv, dtype=torch.int32, device=dev),
         "dev_err": torch.zeros(1, dtype=torch.int32, device=dev),
     }
 
 
 def decode_step(inp: Dict[str, torch.Tensor], k: int, bufs: Optional[Dict[str, torch.Tensor]] = None,
-                softmax_scale: float = 0.0, stream=None, fused: bool = True) -> Dict[str, torch.Tensor]:
+                softmax_scale: float = 0.0, stream=None, fused: bool = True,
+                scratch_zeroed: bool = False) -> Dict[str, torch.Tensor]:
     """One MSA decode step: a1 index score -> a2 top-k -> a3 page table -> a5/a6 attention.
 
     ``inp`` holds Q, q_idx, w, kidx_pool, K_pool, V_pool, seq_pt, seq_len (device tensors).
     With ``fused`` (default) a1-a3 run in one index-score call; otherwise the
-    four entry points are called one by one.
+    four entry points are called one by one.  ``scratch_zeroed`` skips the
+    counter clears (valid with ``decode_buffers`` scratch that every previous
+    call left zero, i.e. no device error was raised).
     """
     B, Hq, _ = inp["Q"].shape
     Hkv = inp["K_pool"].shape[1]
@@ -300,7 +314,7 @@ def decode_step(inp: Dict[str, torch.Tensor], k: int, bufs: Optional[Dict[str, t
         msa_index_score(MSA_MODE_DECODE, inp["q_idx"], inp["w"], inp["kidx_pool"], bufs["C"], seq_pt=inp["seq_pt"],
                         seq_len=inp["seq_len"], dev_err=e, stream=stream, k=k, sel=bufs["sel"],
                         count=bufs["count"], pt=bufs["pt"], n=bufs["n"], last_len=bufs["last_len"],
-                        row_scratch=bufs["row_scratch"])
+                        row_scratch=bufs["row_scratch"], scratch_zeroed=scratch_zeroed)
     else:
         msa_index_score(MSA_MODE_DECODE, inp["q_idx"], inp["w"], inp["kidx_pool"], bufs["C"], seq_pt=inp["seq_pt"],
                         seq_len=inp["seq_len"], dev_err=e, stream=stream)
@@ -310,7 +324,7 @@ def decode_step(inp: Dict[str, torch.Tensor], k: int, bufs: Optional[Dict[str, t
                              bufs["last_len"], dev_err=e, stream=stream)
     msa_sparse_attn_decode(inp["Q"], inp["K_pool"], inp["V_pool"], bufs["pt"], bufs["n"], bufs["last_len"],
                            bufs["O"], bufs["LSE"], bufs["ws"], softmax_scale=softmax_scale, dev_err=e,
-                           stream=stream)
+                           stream=stream, scratch_zeroed=scratch_zeroed)
     return bufs
 
 

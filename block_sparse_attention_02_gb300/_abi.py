@@ -45,7 +45,7 @@ class IndexArgs(C.Structure):
         ("C", _p), ("C_stride", _i64x3), ("nb_stride", C.c_int),
         ("dev_err", _p),
         ("k", C.c_int), ("sel", _p), ("count", _p), ("pt", _p), ("n", _p), ("last_len", _p),
-        ("row_scratch", _p),
+        ("row_scratch", _p), ("scratch_zeroed", C.c_int),
     ]
 
 
@@ -72,7 +72,7 @@ class DecodeArgs(C.Structure):
         ("softmax_scale", C.c_float),
         ("Q", _p), ("Q_stride", _i64x2), ("K_pool", _p), ("V_pool", _p), ("kv_stride", _i64x3),
         ("num_pages", C.c_int64), ("pt", _p), ("n", _p), ("last_len", _p),
-        ("O", _p), ("LSE", _p), ("dev_err", _p),
+        ("O", _p), ("LSE", _p), ("dev_err", _p), ("scratch_zeroed", C.c_int),
     ]
 
 

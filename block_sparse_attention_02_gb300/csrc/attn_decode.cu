@@ -446,8 +446,10 @@ msa_status launch_attn_decode(const msa_decode_args& a, float* o_part, float* ls
   const int64_t units = static_cast<int64_t>(a.B) * a.Hkv * a.k;
   const int64_t grid64 = std::max<int64_t>(std::min<int64_t>(dev.num_sms, units), (units + kMaxUnits - 1) / kMaxUnits);
   const int grid = static_cast<int>(std::max<int64_t>(grid64, 1));
-  e = cudaMemsetAsync(counter, 0, static_cast<size_t>(a.B) * a.Hkv * sizeof(int32_t), stream);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(decode row counters)");
+  if (!a.scratch_zeroed) {   // otherwise zero by contract (every error-free call leaves them zero)
+    e = cudaMemsetAsync(counter, 0, static_cast<size_t>(a.B) * a.Hkv * sizeof(int32_t), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(decode row counters)");
+  }
   attn_decode_kernel<<<grid, kThreads, smem, stream>>>(kmap, vmap, qmap, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "attn_decode_kernel launch");

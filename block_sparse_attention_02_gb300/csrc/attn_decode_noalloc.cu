@@ -70,5 +70,8 @@ extern "C" msa_status msa_sparse_attn_decode_noalloc(const msa_decode_args* a, m
   }
   void* scratch = nullptr;
   if (msa_status st = scratch_address(&scratch); st != MSA_OK) return st;
-  return msa_sparse_attn_decode(a, scratch, kNoallocScratchBytes, stream);
+  // the shared array serves calls of every shape, so its counters are always cleared
+  msa_decode_args cleared = *a;
+  cleared.scratch_zeroed = 0;
+  return msa_sparse_attn_decode(&cleared, scratch, kNoallocScratchBytes, stream);
 }

@@ -480,6 +480,7 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
         if (own > 0 && mine64 > 0) {
           const int mine = static_cast<int>(mine64);
           if (atomicAdd(&p.counter[r], mine) + mine == own) {   // this CTA completed row r
+            p.counter[r] = 0;                                   // no other CTA touches it again: leave it zero
             if (own <= 2048 || own <= m) s_rows[atomicAdd(&s_nrows, 1)] = r;
             else s_long[atomicAdd(&s_nlong, 1)] = r;
           }
@@ -559,7 +560,7 @@ msa_status launch_index_decode(const msa_index_args& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(index_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(index_decode)");
-  if (p.sel != nullptr) {
+  if (p.sel != nullptr && !a.scratch_zeroed) {   // otherwise zero by contract
     e = cudaMemsetAsync(p.counter, 0, static_cast<size_t>(a.B) * a.Hkv * sizeof(int32_t), stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(index row counters)");
   }

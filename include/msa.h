@@ -120,8 +120,13 @@ const char *msa_status_string(msa_status s);
  *   each (b, g) row as soon as the row's scores are complete, and when `pt` is
  *   also non-NULL a3 (exactly what msa_build_page_table computes).  This saves
  *   two launches per decode step.  `row_scratch` is then required: B*Hkv int32
- *   of caller scratch, cleared by the call.  Outputs are those of a2 / a3:
- *   sel [B,Hkv,k], count [B,Hkv], pt [B*Hkv,k], n and last_len [B*Hkv].
+ *   of caller scratch (one completion counter per row).  Outputs are those of
+ *   a2 / a3: sel [B,Hkv,k], count [B,Hkv], pt [B*Hkv,k], n and last_len [B*Hkv].
+ *   scratch_zeroed = 0: the call clears row_scratch first (one memset on the
+ *   stream).  scratch_zeroed = 1: the caller guarantees row_scratch is zero
+ *   (freshly zero-filled, or left by a previous call) and the memset is
+ *   skipped.  Either way a call that raises no device error leaves row_scratch
+ *   zero; after one that does, zero it again (or pass 0).
  * ------------------------------------------------------------------------ */
 typedef struct msa_index_args {
     msa_mode mode;
@@ -148,6 +153,7 @@ typedef struct msa_index_args {
     int32_t *n;
     int32_t *last_len;
     int32_t *row_scratch;
+    int scratch_zeroed;
 } msa_index_args;
 
 msa_status msa_index_score(const msa_index_args *args, msa_stream_t stream);
@@ -259,8 +265,14 @@ msa_status msa_sparse_attn_prefill(const msa_prefill_args *args, void *ws, size_
  *     O [B, Hq, D] bf16 (dense), LSE [B, Hq] fp32 (dense).
  * Workspace: msa_sparse_attn_decode_workspace_size(args) bytes (fp32 partial
  * outputs and LSEs and one counter per row: B*Hq*k*(D+1)*4 + B*Hkv*4 + 256
- * bytes); the call clears the counters itself.  Page ids outside [0, num_pages)
- * are skipped (MSA_DEVERR_BAD_PAGE).  softmax_scale <= 0 selects 1/sqrt(D).
+ * bytes; the B*Hkv int32 counters start at byte B*Hq*k*(D+1)*4).
+ * scratch_zeroed = 0: the call clears the counters first (one memset on the
+ * stream).  scratch_zeroed = 1: the caller guarantees they are zero (a
+ * zero-filled workspace, or one left by a previous call with the same B, Hq,
+ * Hkv, k and D) and the memset is skipped.  Either way a call that raises no
+ * device error leaves the counters zero; after one that does, zero them again
+ * (or pass 0).  Page ids outside [0, num_pages) are skipped
+ * (MSA_DEVERR_BAD_PAGE).  softmax_scale <= 0 selects 1/sqrt(D).
  * ------------------------------------------------------------------------ */
 typedef struct msa_decode_args {
     int B, Hq, Hkv, D, Bk, k;
@@ -277,6 +289,7 @@ typedef struct msa_decode_args {
     void *O;
     float *LSE;
     int32_t *dev_err;
+    int scratch_zeroed;
 } msa_decode_args;
 
 size_t msa_sparse_attn_decode_workspace_size(const msa_decode_args *args);
@@ -303,7 +316,8 @@ msa_status msa_sparse_attn_decode(const msa_decode_args *args, void *ws, size_t 
  *   - All calls share the array, which keeps the last call's contents.  Calls
  *     whose kernels overlap on the GPU (other streams, other host threads)
  *     race on it: serialise them.  Each call clears the per-row counters it
- *     needs and writes every partial the merge reads before reading it.
+ *     needs (scratch_zeroed is ignored) and writes every partial the merge
+ *     reads before reading it.
  * ------------------------------------------------------------------------ */
 #define MSA_NOALLOC_SCRATCH_BYTES (32u << 20)
 

@@ -141,6 +141,26 @@ def test_decode_is_deterministic(msa):
         assert torch.equal(a[n], b[n]), n
 
 
+@pytest.mark.parametrize("wl", SMALL[:2] + [workload("decode_b8_l60001")], ids=lambda w: w.name)
+def test_scratch_zeroed_calls_leave_counters_zero(msa, wl):
+    """With scratch_zeroed the counter clears are skipped: repeated calls on the
+    same zero-filled scratch give the bits of the default calls and leave every
+    row counter (row_scratch and the workspace's counter words) zero."""
+    sh = wl.shape
+    inp = decode_inputs(wl, device="cuda")
+    ref = run_gpu(msa, inp, sh.k)
+    bufs = msa.decode_buffers(wl.B, sh.Hq, sh.Hkv, sh.k, inp["seq_pt"].shape[1], "cuda")
+    off = wl.B * sh.Hq * sh.k * (sh.D + 1)          # counter words follow the partials and LSEs (4-byte units)
+    for _ in range(3):
+        msa.decode_step(inp, sh.k, bufs, scratch_zeroed=True)
+        torch.cuda.synchronize()
+        assert int(bufs["dev_err"].item()) == 0
+        for n in ("C", "sel", "count", "pt", "n", "last_len", "O", "LSE"):
+            assert torch.equal(bufs[n].cpu(), ref[n]), n
+        assert int(bufs["row_scratch"].abs().sum().item()) == 0
+        assert int(bufs["ws"].view(torch.int32)[off: off + wl.B * sh.Hkv].abs().sum().item()) == 0
+
+
 def test_decode_bad_page_is_reported_not_read(msa):
     """A page id outside the pool is skipped and flagged; nothing faults."""
     wl = DecodeWorkload("badpage", lengths=(1000, 1000), shape=MSAShape(), seed=37)
