@@ -322,18 +322,20 @@ def run_decode_ours(args, wl, world, rank):
     peaks = load_peaks()
     alg = decode_algorithmic_bytes(wl)
     achieved = alg["index_kernel"] / (idx_ms * 1e-3) / 1e9
-    traffic, traffic_src = read_profile_traffic("index_decode_b8_l60001.txt", DECODE_INDEX_FILES)
+    traffic, traffic_src = read_profile_traffic(f"index_decode_{wl.name}.txt", DECODE_INDEX_FILES)
     tokens_per_step = wl.B * world
     step_ms = total_ms / K
     res = {
         "metric": METRIC, "value": tokens_per_step / (step_ms * 1e-3), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl.name, "batch": wl.B, "context": wl.lengths[0], "Hq": wl.shape.Hq,
+        "config": {"workload": wl.name, "batch": wl.B,
+                   "context": wl.lengths[0] if len(set(wl.lengths)) == 1 else f"ragged {min(wl.lengths)}..{max(wl.lengths)}, total {sum(wl.lengths)}",
+                   "Hq": wl.shape.Hq,
                    "Hkv": wl.shape.Hkv, "D": wl.shape.D, "HI": wl.shape.HI, "dI": wl.shape.dI, "Bk": wl.shape.Bk,
                    "k": wl.shape.k, "pages": "128-token, shuffled", "cuda_graphs": graphs,
                    "scratch": "zero-filled once; calls skip the counter clears (scratch_zeroed) and leave them zero",
-                   "l2": "no flush: inputs larger than L2 (491 MB k_idx pool read per step)",
+                   "l2": f"no flush: inputs larger than L2 ({alg['index_kernel'] / 1e6:.0f} MB of k_idx read per step)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "kernel": "index_decode_kernel (with fused selection)", "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],

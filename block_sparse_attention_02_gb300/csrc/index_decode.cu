@@ -181,6 +181,55 @@ __device__ void select_row(const Params& p, int b, int g, int own, uint64_t* s_k
   __syncthreads();
 }
 
+// Exact top-(k-1) of a long row (own > 2048 earlier blocks) in two phases:
+// the row is cut into slices of at most 2048 blocks; each warp selects the best
+// m of its slices with the register-based warp select into a pool (slot
+// slice * m + y; 0 = empty, below every real key); then every thread ranks
+// the pool's keys exactly and the m best are the picks.  The row's best m
+// blocks are among the pool: a block outside its slice's best m has m better
+// blocks in its own slice.  Falls back to select_row when the pool does not
+// fit.  All threads of the CTA call this.
+__device__ void select_long_row(const Params& p, int b, int g, int own, uint64_t* s_pool, int pool_cap,
+                                uint64_t* s_surv, int (*s_wpick)[kMaxK], int (*s_wout)[kMaxK], int* s_final,
+                                uint64_t* s_w) {
+  const int m = p.k - 1;
+  const int nslices = (own + 2047) / 2048;
+  if (own <= m || static_cast<int64_t>(nslices) * m > pool_cap) {
+    select_row(p, b, g, own, s_pool, pool_cap, s_w, s_final);
+    return;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ssz = (own + nslices - 1) / nslices;     // <= 2048
+  const float* crow = p.C + b * p.cs0 + g * p.cs1;
+  for (int sl = warp; sl < nslices; sl += kThreads / 32) {
+    const int lo = sl * ssz, n = min(ssz, own - lo);
+    int* out = s_wout[warp];
+    int npick = n;
+    if (n <= m) {
+      for (int y = lane; y < n; y += 32) out[y] = y;
+    } else {
+      warp_select_any(crow + lo, n, m, s_surv + warp * kSelCap, s_wpick[warp], out);
+      npick = m;
+    }
+    __syncwarp();
+    for (int y = lane; y < m; y += 32)
+      s_pool[sl * m + y] = y < npick ? select_key(__ldcg(crow + lo + out[y]), lo + out[y]) : 0ull;
+    __syncwarp();
+  }
+  __syncthreads();
+  const int npool = nslices * m;
+  for (int x = threadIdx.x; x < npool; x += kThreads) {
+    const uint64_t kx = s_pool[x];
+    if (kx == 0ull) continue;
+    int rank = 0;
+    for (int y = 0; y < npool; ++y) rank += s_pool[y] > kx;
+    if (rank < m) s_final[rank] = select_key_index(kx);
+  }
+  __syncthreads();
+  emit_row(p, b, g, own, true, s_final, m);
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -457,6 +506,7 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
     __shared__ uint64_t s_w[kThreads / 32 + 1];
     __shared__ int s_picks[kThreads / 32][kMaxK];
     __shared__ int s_out[kThreads / 32][kMaxK];
+    __shared__ int s_final[kMaxK];
     uint8_t* ring = s_stage;                          // the TMA ring is idle now
     uint64_t* s_surv = reinterpret_cast<uint64_t*>(ring);                  // [warps][kSelCap]
     uint64_t* s_keys = reinterpret_cast<uint64_t*>(ring + (kThreads / 32) * kSelCap * 8);
@@ -520,7 +570,8 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
       // long rows: the whole CTA
       for (int x = 0; x < s_nlong; ++x) {
         const int rr = s_long[x];
-        select_row(p, rr / p.Hkv, rr % p.Hkv, s_own[rr / p.Hkv], s_keys, key_cap, s_w, s_picks[0]);
+        select_long_row(p, rr / p.Hkv, rr % p.Hkv, s_own[rr / p.Hkv], s_keys, key_cap, s_surv, s_picks, s_out,
+                        s_final, s_w);
       }
       __syncthreads();
     }
