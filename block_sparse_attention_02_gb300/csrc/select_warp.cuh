@@ -27,10 +27,16 @@ __device__ __forceinline__ void warp_select(const float* crow, int n, int m, uin
   const int lane = threadIdx.x & 31;
   uint32_t u[NPL];
   uint32_t lmax = 0;
+  // every load first, then the keys: the loads stay in flight together
 #pragma unroll
   for (int i = 0; i < NPL; ++i) {
     const int j = lane + 32 * i;
-    u[i] = (j < n) ? score_order_key(__ldcg(crow + j)) : 0u;
+    u[i] = (j < n) ? __float_as_uint(__ldcg(crow + j)) : 0u;
+  }
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int j = lane + 32 * i;
+    u[i] = (j < n) ? score_order_key(__uint_as_float(u[i])) : 0u;
     lmax = max(lmax, u[i]);
   }
   uint32_t T0 = 0;
