@@ -173,7 +173,8 @@ def read_profile_traffic(name: str, kernel_files):
 # ---------------------------------------------------------------------------
 
 DECODE_INDEX_FILES = ["block_sparse_attention_02_gb300/csrc/index_decode.cu",
-                      "block_sparse_attention_02_gb300/csrc/msa_ptx.cuh"]
+                      "block_sparse_attention_02_gb300/csrc/msa_ptx.cuh",
+                      "block_sparse_attention_02_gb300/csrc/select_warp.cuh"]
 
 
 def decode_algorithmic_bytes(wl):
