@@ -7,35 +7,46 @@
 // alcance", MSA paragraph and caption; the formula is this library's).  The own
 // block and later blocks are written -inf.
 //
-// This is a dense contraction on the tensor cores.  Work item = (b, g, query
-// block qb): 128 queries against the qb earlier key blocks.  Items are paired
-// (qb, nbq-1-qb) so every pair costs nbq-1 blocks, and a persistent CTA per SM
-// takes pairs round-robin.
-//   warp 0    TMA: the HI q_idx tiles of the item (128 queries x 64, one per
-//             index head, double-buffered across items) and a 4-deep ring of
-//             k_idx blocks (128 tokens x 64), all 128-byte swizzled;
-//   warp 1    tcgen05: per key block, passes of two index heads:
-//             D_h[query, token] = q_idx_h . k_idx  (M=128, N=128, K=64) for
-//             both heads into a 256-column TMEM buffer, the two MMA chains
-//             interleaved step by step (a single accumulation chain leaves the
-//             tensor core waiting on its own results); two buffers;
-//   warps 2-5 epilogue, thread = query: acc_t = sum_h w_h ReLU(D_h[t]) with
-//             packed fp32 FMAs, carried across the passes in registers, then
-//             the max over the block's 128 tokens, one store per (query, block).
+// This is a dense contraction on the tensor cores.  An item is (b, g, query
+// block qb of 64 queries); its queries share the own 128-token block qb / 2,
+// so the item scores the key blocks j < qb / 2.  One pass = one key block:
+//     D[t, (h, q)] = k_idx[t] . q_idx[q, h]    M = 128 tokens, N = 64 * HI
+//                                              (heads x queries), K = 64
+// With the tokens on M and the four heads side by side on N every MMA is
+// N = 256 (the tensor core's full width), and the epilogue needs no state across
+// passes: thread = token t forms s_t = sum_h w_h ReLU(D[t, (h, q)]) for its
+// queries, the block max over tokens is one `redux.sync.max` per warp and query
+// (order-preserving integer keys) plus a 4-warp combine in shared memory.
+// Items pair query block qb with nq-1-qb (constant cost per pair); a persistent
+// CTA per SM takes pairs round-robin and runs two independent item streams
+// ("slots") at once:
+//   warp 0    TMA: per slot a q_idx tile (HI heads x 64 queries, one box per
+//             head) and, in the merged pass order, a 6-deep ring of k_idx blocks
+//             (128 tokens x 64), all 128-byte swizzled;
+//   warp 1    tcgen05: per pass 4 MMAs into the slot's 256-column TMEM buffer;
+//   warps 2-17: four epilogue warpgroups, two per slot, each reducing 32 of
+//             the slot's 64 queries (TMEM loads of the next 8 queries in flight
+//             while the current 8 are reduced).
 #include "msa_internal.h"
 #include "msa_ptx.cuh"
 
 namespace msa {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kTile = 128 * 64 * 2;            // 16 KiB: 128 rows x 64 bf16
-constexpr int kKStages = 4;
+constexpr int kQB = 64;                             // queries per item
+constexpr int kHalves = 2;                          // epilogue warpgroups per slot (query halves)
+constexpr int kQW = kQB / kHalves;                  // queries per epilogue warpgroup
+constexpr int kThreads = 64 + 2 * kHalves * 128;    // w0 TMA, w1 MMA, then the epilogue warpgroups
+constexpr int kKTile = 128 * 64 * 2;                // 16 KiB: one k_idx block
+constexpr int kQHead = kQB * 64 * 2;                // 8 KiB: one head of a q_idx tile
+constexpr int kQTile = kMaxHI * kQHead;             // 32 KiB
+constexpr int kKStages = 6;
+constexpr int kBufCols = 256;                       // TMEM per slot: HI x 64 columns
 constexpr int kTmemCols = 512;
-constexpr int kBufCols = 256;                  // one TMEM buffer: 2 heads x 128 tokens
+constexpr int kFlush = 32;                          // block scores staged per query before a store
 
 struct Params {
-  int B, S, Hkv, HI, nbq, nb_stride;
+  int B, S, Hkv, HI, nq, nb_stride;                 // nq = ceil(S / 64)
   const float* w;
   int64_t ws0, ws1, ws2;
   float* C;
@@ -44,21 +55,120 @@ struct Params {
 };
 
 struct Item {
-  int b, g, qb;
+  int b, g, qb, own;                                // own = number of key blocks to score
 };
 
-// item t of pair p: pairs enumerate (b, g, pp) with qb in {pp, nbq-1-pp}
-__device__ __forceinline__ int pair_items(const Params& p, int64_t pair, Item* it) {
-  const int half = (p.nbq + 1) / 2;
+// item `which` (0 or 1) of pair `pair`: pairs enumerate (b, g, pp) with qb in
+// {pp, nq-1-pp}; false when the pair has no such item
+__device__ __forceinline__ bool pair_item(const Params& p, int64_t pair, int which, Item* it) {
+  const int half = (p.nq + 1) / 2;
   const int pp = static_cast<int>(pair % half);
   const int64_t bg = pair / half;
-  const int g = static_cast<int>(bg % p.Hkv), b = static_cast<int>(bg / p.Hkv);
-  it[0] = {b, g, pp};
-  const int other = p.nbq - 1 - pp;
-  if (other == pp) return 1;
-  it[1] = {b, g, other};
-  return 2;
+  const int other = p.nq - 1 - pp;
+  if (which == 1 && other == pp) return false;
+  const int qb = which == 0 ? pp : other;
+  *it = {static_cast<int>(bg / p.Hkv), static_cast<int>(bg % p.Hkv), qb, (qb * kQB) / kBk};
+  return true;
 }
+
+// The items of one slot: in the k-th pair of this CTA the slot takes item
+// slot ^ (k & 1), so long and short items alternate between the slots.
+struct Stream {
+  int64_t pr;      // next pair to look at
+  int k;           // its ordinal in this CTA
+  Item it;         // current item
+  int j;           // next key block of the current item
+  bool done;
+};
+
+// keep_empty: also stop at items with no key block to score (the epilogue
+// still writes their -inf rows; the producer and the MMA warp skip them)
+__device__ __forceinline__ void stream_advance(const Params& p, Stream& s, int slot, int64_t npairs,
+                                               bool keep_empty) {
+  for (;;) {
+    if (s.pr >= npairs) {
+      s.done = true;
+      return;
+    }
+    Item it;
+    const bool ok = pair_item(p, s.pr, slot ^ (s.k & 1), &it);
+    s.pr += gridDim.x;
+    ++s.k;
+    if (ok && (keep_empty || it.own > 0)) {
+      s.it = it;
+      s.j = 0;
+      return;
+    }
+  }
+}
+
+__device__ __forceinline__ void stream_init(const Params& p, Stream& s, int slot, int64_t npairs, bool keep_empty) {
+  s.pr = blockIdx.x;
+  s.k = 0;
+  s.done = false;
+  stream_advance(p, s, slot, npairs, keep_empty);
+}
+
+// One pass of stream `st` (slot `slot`): hand it to f(slot, item, j, first,
+// last) and step the stream.  first/last = first/last pass of the item.
+template <class F>
+__device__ __forceinline__ bool stream_pass(const Params& p, Stream& st, int slot, int64_t npairs, F& f) {
+  const Item it = st.it;
+  const int j = st.j;
+  if (++st.j == it.own) stream_advance(p, st, slot, npairs, false);
+  return f(slot, it, j, j == 0, j == it.own - 1);
+}
+
+// The merged pass order of the producer and the MMA warp: the two slots'
+// passes alternate while both have passes left.  Both streams stay in
+// registers (a runtime-indexed pair would live in local memory, whose
+// round trips the single-thread loops would pay on every pass).  Stops early
+// when f returns false.
+template <class F>
+__device__ __forceinline__ void for_each_pass(const Params& p, int64_t npairs, F&& f) {
+  Stream s0, s1;
+  stream_init(p, s0, 0, npairs, false);
+  stream_init(p, s1, 1, npairs, false);
+  bool turn = false;
+  for (;;) {
+    bool one;
+    if (!s0.done && !s1.done) {
+      one = turn;
+      turn = !turn;
+    } else if (!s0.done) {
+      one = false;
+    } else if (!s1.done) {
+      one = true;
+    } else {
+      return;
+    }
+    if (!(one ? stream_pass(p, s1, 1, npairs, f) : stream_pass(p, s0, 0, npairs, f))) return;
+  }
+}
+
+// Named barrier over n threads that also returns the AND of `v` over them:
+// every warp of an epilogue group leaves a pass with the same verdict.
+__device__ __forceinline__ bool named_bar_and(int id, int n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+// Order-preserving signed-integer key of a float score (larger float, larger
+// key) and its inverse: the magnitude bits of negative values are flipped.
+// Scores here are never -0 (every sum starts from +0).
+__device__ __forceinline__ int score_key(float f) {
+  const int i = __float_as_int(f);
+  return i ^ ((i >> 31) & 0x7FFFFFFF);
+}
+__device__ __forceinline__ float score_from_key(int k) { return __int_as_float(k ^ ((k >> 31) & 0x7FFFFFFF)); }
 
 __device__ __forceinline__ uint64_t pack2(float x, float y) {
   uint64_t r;
@@ -68,36 +178,42 @@ __device__ __forceinline__ uint64_t pack2(float x, float y) {
 __device__ __forceinline__ void unpack2(uint64_t v, float& x, float& y) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(v));
 }
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {   // two IEEE fmas
   uint64_t d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
   return d;
 }
-__device__ __forceinline__ float max3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
+// After tcgen05.wait::ld: ties the loaded registers to the wait so that no use
+// of them is scheduled before it (emits no instruction).
+__device__ __forceinline__ void regs_after_wait(uint32_t (&r)[8]) {
+  asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]));
 }
 
+constexpr int kCQ = 8;                               // queries per epilogue chunk
+constexpr int kNC = kQW / kCQ;                       // chunks per pass and warp
+
+template <int HI>
 __global__ void __launch_bounds__(kThreads, 1)
 index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                      const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* s_a = smem;                              // [2][4] q_idx tiles
-  uint8_t* s_k = smem + 2 * kMaxHI * kTile;         // [kKStages] k_idx blocks
+  uint8_t* s_q = smem;                              // [2 slots] q_idx tiles: [head][64 queries][64]
+  uint8_t* s_k = smem + 2 * kQTile;                 // [kKStages] k_idx blocks: [128 tokens][64]
 
-  __shared__ __align__(8) uint64_t bar_afull[2], bar_aempty[2], bar_kfull[kKStages], bar_kempty[kKStages];
+  __shared__ __align__(8) uint64_t bar_qfull[2], bar_qempty[2], bar_kfull[kKStages], bar_kempty[kKStages];
   __shared__ __align__(8) uint64_t bar_tfull[2], bar_tempty[2], bar_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ float s_cst[128][33];   // block scores staged per query row, 32 blocks at a time
+  __shared__ __align__(16) float2 s_w[2][kQB / 2][kMaxHI];   // per slot: (w[2e][h], w[2e+1][h]) per query pair e
+  __shared__ __align__(16) int s_red[2][2][4][kQB]; // per slot and pass parity: warp maxima per query (keys)
+  __shared__ float s_cst[2][kQB][kFlush + 1];       // per slot: staged block scores per query row
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar_afull[i], 1); mbar_init(&bar_aempty[i], 1);
-      mbar_init(&bar_tfull[i], 1); mbar_init(&bar_tempty[i], 4);
+      mbar_init(&bar_qfull[i], 1); mbar_init(&bar_qempty[i], 1);
+      mbar_init(&bar_tfull[i], 1); mbar_init(&bar_tempty[i], 4 * kHalves);
     }
     for (int i = 0; i < kKStages; ++i) { mbar_init(&bar_kfull[i], 1); mbar_init(&bar_kempty[i], 1); }
     mbar_init(&bar_drain, 1);
@@ -109,184 +225,192 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   volatile int* abort_flag = &s_abort;
-  const int64_t npairs = static_cast<int64_t>(p.B) * p.Hkv * ((p.nbq + 1) / 2);
+  const int64_t npairs = static_cast<int64_t>(p.B) * p.Hkv * ((p.nq + 1) / 2);
 
   if (warp == 0) {
     // ===================== TMA producer =====================
     if (lane == 0) {
-      int na = 0, nk = 0;
-      bool ok = true;
-      for (int64_t pr = blockIdx.x; pr < npairs && ok; pr += gridDim.x) {
-        Item its[2];
-        const int ni = pair_items(p, pr, its);
-        for (int x = 0; x < ni && ok; ++x) {
-          const Item it = its[x];
-          if (it.qb == 0) continue;
-          const int a = na & 1;
-          if (!(ok = mbar_wait(&bar_aempty[a], ((na >> 1) & 1) ^ 1, abort_flag, p.dev_err))) break;
-          mbar_arrive_expect_tx(&bar_afull[a], p.HI * kTile);
-          for (int h = 0; h < p.HI; ++h)
-            tma_load_5d(s_a + (a * kMaxHI + h) * kTile, &qmap, &bar_afull[a], 0, h, it.g, it.qb * kBk, it.b);
-          ++na;
-          for (int j = 0; j < it.qb; ++j) {
-            const int st = nk % kKStages;
-            if (!(ok = mbar_wait(&bar_kempty[st], ((nk / kKStages) & 1) ^ 1, abort_flag, p.dev_err))) break;
-            mbar_arrive_expect_tx(&bar_kfull[st], kTile);
-            tma_load_4d(s_k + st * kTile, &kmap, &bar_kfull[st], 0, it.g, j * kBk, it.b);
-            ++nk;
-          }
+      int n = 0, nql0 = 0, nql1 = 0;   // k blocks issued; q tiles issued per slot
+      for_each_pass(p, npairs, [&](int slot, const Item& it, int j, bool first, bool) -> bool {
+        if (first) {   // the item's q_idx tile into the slot's buffer, once its previous item is done
+          const int c = slot ? nql1 : nql0;
+          if (!mbar_wait(&bar_qempty[slot], (c & 1) ^ 1, abort_flag, p.dev_err)) return false;
+          mbar_arrive_expect_tx(&bar_qfull[slot], HI * kQHead);
+          for (int h = 0; h < HI; ++h)
+            tma_load_5d(s_q + slot * kQTile + h * kQHead, &qmap, &bar_qfull[slot], 0, h, it.g, it.qb * kQB, it.b);
+          if (slot) nql1 = c + 1; else nql0 = c + 1;
         }
-      }
+        const int st = n % kKStages;
+        if (!mbar_wait(&bar_kempty[st], ((n / kKStages) & 1) ^ 1, abort_flag, p.dev_err)) return false;
+        mbar_arrive_expect_tx(&bar_kfull[st], kKTile);
+        tma_load_4d(s_k + st * kKTile, &kmap, &bar_kfull[st], 0, it.g, j * kBk, it.b);
+        ++n;
+        return true;
+      });
       if (*abort_flag) {  // let loads in flight land before the CTA exits
-        for (int n = max(0, nk - kKStages); n < nk; ++n) {
-          uint64_t t0 = global_timer_ns();
-          while (!mbar_try_wait(&bar_kfull[n % kKStages], (n / kKStages) & 1) &&
+        const uint64_t t0 = global_timer_ns();
+        for (int x = max(0, n - kKStages); x < n; ++x)
+          while (!mbar_try_wait(&bar_kfull[x % kKStages], (x / kKStages) & 1) &&
                  global_timer_ns() - t0 < MSA_WAIT_LIMIT_NS) {
           }
-        }
-        for (int n = max(0, na - 2); n < na; ++n) {
-          uint64_t t0 = global_timer_ns();
-          while (!mbar_try_wait(&bar_afull[n & 1], (n >> 1) & 1) && global_timer_ns() - t0 < MSA_WAIT_LIMIT_NS) {
+        if (nql0 > 0)
+          while (!mbar_try_wait(&bar_qfull[0], (nql0 - 1) & 1) && global_timer_ns() - t0 < MSA_WAIT_LIMIT_NS) {
           }
-        }
+        if (nql1 > 0)
+          while (!mbar_try_wait(&bar_qfull[1], (nql1 - 1) & 1) && global_timer_ns() - t0 < MSA_WAIT_LIMIT_NS) {
+          }
       }
     }
   } else if (warp == 1) {
     // ===================== tcgen05 issuer =====================
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(128, 128, false, false);
-      const int npass = (p.HI + 1) / 2;
-      int na = 0, nk = 0, nt = 0;
-      bool ok = true;
-      for (int64_t pr = blockIdx.x; pr < npairs && ok; pr += gridDim.x) {
-        Item its[2];
-        const int ni = pair_items(p, pr, its);
-        for (int x = 0; x < ni && ok; ++x) {
-          const Item it = its[x];
-          if (it.qb == 0) continue;
-          const int a = na & 1;
-          if (!(ok = mbar_wait(&bar_afull[a], (na >> 1) & 1, abort_flag, p.dev_err))) break;
-          const uint32_t abase = smem_u32(s_a + a * kMaxHI * kTile);
-          for (int j = 0; j < it.qb && ok; ++j) {
-            const int st = nk % kKStages;
-            if (!(ok = mbar_wait(&bar_kfull[st], (nk / kKStages) & 1, abort_flag, p.dev_err))) break;
-            const uint32_t kbase = smem_u32(s_k + st * kTile);
-            for (int ps = 0; ps < npass; ++ps) {
-              const int buf = nt & 1;
-              if (!(ok = mbar_wait(&bar_tempty[buf], ((nt >> 1) & 1) ^ 1, abort_flag, p.dev_err))) break;
-              tc_fence_after();
-              const int h0 = 2 * ps, nh = min(2, p.HI - h0);
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                for (int hh = 0; hh < nh; ++hh)
-                  umma_bf16(tmem + buf * kBufCols + hh * 128, sdesc_sw128(abase + (h0 + hh) * kTile + 32 * kk, 16, 1024),
-                            sdesc_sw128(kbase + 32 * kk, 16, 1024), idesc, kk > 0);
-              umma_commit(&bar_tfull[buf]);
-              ++nt;
-            }
-            umma_commit(&bar_kempty[st]);
-            ++nk;
-          }
-          umma_commit(&bar_aempty[a]);
-          ++na;
+      constexpr uint32_t idesc = idesc_bf16(128, kQB * HI, false, false);
+      int n = 0, nqw0 = 0, nqw1 = 0, np0 = 0, np1 = 0;   // passes; q tiles and passes per slot
+      for_each_pass(p, npairs, [&](int slot, const Item&, int, bool first, bool last) -> bool {
+        if (first) {
+          const int c = slot ? nqw1 : nqw0;
+          if (!mbar_wait(&bar_qfull[slot], c & 1, abort_flag, p.dev_err)) return false;
+          if (slot) nqw1 = c + 1; else nqw0 = c + 1;
         }
-      }
+        const int st = n % kKStages;
+        const int np = slot ? np1 : np0;
+        if (!mbar_wait(&bar_kfull[st], (n / kKStages) & 1, abort_flag, p.dev_err)) return false;
+        if (!mbar_wait(&bar_tempty[slot], (np & 1) ^ 1, abort_flag, p.dev_err)) return false;
+        tc_fence_after();
+        const uint32_t kb = smem_u32(s_k + st * kKTile), qb = smem_u32(s_q + slot * kQTile);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)   // D[t, (h, q)] += k[t, 16kk..] . q[(h, q), 16kk..]
+          umma_bf16(tmem + slot * kBufCols, sdesc_sw128(kb + 32 * kk, 16, 1024), sdesc_sw128(qb + 32 * kk, 16, 1024),
+                    idesc, kk > 0);
+        umma_commit(&bar_tfull[slot]);
+        umma_commit(&bar_kempty[st]);
+        if (last) umma_commit(&bar_qempty[slot]);
+        if (slot) np1 = np + 1; else np0 = np + 1;
+        ++n;
+        return true;
+      });
       umma_commit(&bar_drain);
-      uint64_t t0 = global_timer_ns();
+      const uint64_t t0 = global_timer_ns();
       while (!mbar_try_wait(&bar_drain, 0) && global_timer_ns() - t0 < MSA_WAIT_LIMIT_NS) {
       }
     }
     __syncwarp();
   } else {
-    // ===================== epilogue (warps 2..5), thread = query =====================
-    const int q = warp & 3;
-    const int r = q * 32 + lane;
-    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
-    int nt = 0;
+    // ===================== epilogue; thread = token =====================
+    // warpgroup wg = (warp - 2) / 4 serves slot wg % 2 and the slot's queries
+    // q0 .. q0 + 31 of every pass, q0 = 32 (wg / 2)
+    const int wg = (warp - 2) >> 2;
+    const int sl = wg & 1;
+    const int q0 = (wg >> 1) * kQW;
+    const int q4 = warp & 3;                          // TMEM lane quarter
+    const int tw = tid - 64 - wg * 128;               // thread within the warpgroup
+    const int bar_id = 1 + wg;
+    const uint32_t base = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + sl * kBufCols + q0;
+    Stream st;
+    stream_init(p, st, sl, npairs, true);
+    int np = 0;
     bool ok = true;
-    for (int64_t pr = blockIdx.x; pr < npairs && ok; pr += gridDim.x) {
-      Item its[2];
-      const int ni = pair_items(p, pr, its);
-      for (int x = 0; x < ni && ok; ++x) {
-        const Item it = its[x];
-        const int i = it.qb * kBk + r;
-        const bool valid = i < p.S;
-        uint64_t w2[kMaxHI];
+    while (ok && !st.done) {
+      const Item it = st.it;
+      named_bar_sync(bar_id, 128);                    // the previous item's s_w / s_cst are no longer read
+      if (tw < kQW) {
+        const int i = it.qb * kQB + q0 + tw;
+        const float* wp = p.w + it.b * p.ws0 + static_cast<int64_t>(i) * p.ws1 + it.g * p.ws2;
+        float* sw = reinterpret_cast<float*>(&s_w[sl][(q0 + tw) >> 1][0]) + (tw & 1);
 #pragma unroll
-        for (int h = 0; h < kMaxHI; ++h) {
-          const float wv = (valid && h < p.HI) ? p.w[it.b * p.ws0 + static_cast<int64_t>(i) * p.ws1 + it.g * p.ws2 + h]
-                                               : 0.f;
-          w2[h] = pack2(wv, wv);
-        }
-        // rows of this warp: queries it.qb*Bk + q*32 + rr, rr < 32
-        const int row0 = it.qb * kBk + q * 32;
-        auto flush = [&](int j0, int cnt) {   // coalesced: one 128-byte row segment per step
-          __syncwarp();
-          for (int rr = 0; rr < 32; ++rr) {
-            if (row0 + rr < p.S && lane < cnt)
-              p.C[it.b * p.cs0 + static_cast<int64_t>(row0 + rr) * p.cs1 + it.g * p.cs2 + j0 + lane] =
-                  s_cst[q * 32 + rr][lane];
-          }
-          __syncwarp();
+        for (int h = 0; h < HI; ++h) sw[2 * h] = i < p.S ? wp[h] : 0.f;
+      }
+      named_bar_sync(bar_id, 128);
+      for (int j = 0; j < it.own; ++j) {
+        // warp-uniform decision: the TMEM loads below are warp-collective
+        const bool got = __all_sync(0xffffffffu, mbar_wait(&bar_tfull[sl], np & 1, abort_flag, p.dev_err));
+        if (got) tc_fence_after();
+        int* red = &s_red[sl][np & 1][q4][q0];
+        // chunk c = queries 8c .. 8c+7; the TMEM loads of chunk c+1 are in flight
+        // while chunk c is reduced
+        uint32_t va[HI][kCQ], vb[HI][kCQ];
+        auto load = [&](int c, uint32_t (&v)[HI][kCQ]) {
+#pragma unroll
+          for (int h = 0; h < HI; ++h) tmem_ld8(base + h * kQB + c * kCQ, v[h]);
         };
-        const int npass = (p.HI + 1) / 2;
-        for (int j = 0; j < it.qb; ++j) {
-          // acc[t/2] = sum over heads of w_h ReLU(D_h[query, t]) for t = 2e, 2e+1 (packed)
-          uint64_t acc[64];
+        auto wait = [&](uint32_t (&v)[HI][kCQ]) {
+          tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 64; ++e) acc[e] = 0ull;
+          for (int h = 0; h < HI; ++h) regs_after_wait(v[h]);
+        };
+        auto reduce = [&](int c, uint32_t (&v)[HI][kCQ]) {
+          // s_t = sum_h w_h ReLU(D[t, (h, q)]) for the chunk's 8 queries (two per fma.f32x2),
+          // heads in order; then the max over this warp's 32 tokens
+          int km[kCQ];
 #pragma unroll
-          for (int ps = 0; ps < (kMaxHI + 1) / 2; ++ps) {
-            if (ps >= npass) break;
-            const int buf = nt & 1;
-            // warp-uniform decision: the TMEM loads below are warp-collective
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar_tfull[buf], (nt >> 1) & 1, abort_flag, p.dev_err))))
-              break;
-            tc_fence_after();
-            const uint32_t base = tmem + lane_addr + buf * kBufCols;
-            const bool two = 2 * ps + 1 < p.HI;
+          for (int e = 0; e < kCQ / 2; ++e) {
+            const float4* wq = reinterpret_cast<const float4*>(&s_w[sl][(q0 + c * kCQ) / 2 + e][0]);
+            const float4 w01 = wq[0], w23 = wq[1];
+            const float wx[4] = {w01.x, w01.z, w23.x, w23.z}, wy[4] = {w01.y, w01.w, w23.y, w23.w};
+            uint64_t acc = 0ull;
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-              uint32_t v[2][32];
-              tmem_ld32(base + cc * 32, v[0]);
-              if (two) tmem_ld32(base + 128 + cc * 32, v[1]);
-              tmem_ld_wait();
+            for (int h = 0; h < HI; ++h)
+              acc = fma2(pack2(wx[h], wy[h]),
+                         pack2(fmaxf(__uint_as_float(v[h][2 * e]), 0.f), fmaxf(__uint_as_float(v[h][2 * e + 1]), 0.f)),
+                         acc);
+            float s0, s1;
+            unpack2(acc, s0, s1);
+            km[2 * e] = __reduce_max_sync(0xffffffffu, score_key(s0));
+            km[2 * e + 1] = __reduce_max_sync(0xffffffffu, score_key(s1));
+          }
+          if (lane == 0) {
+            int4* dst = reinterpret_cast<int4*>(red + c * kCQ);
+            dst[0] = make_int4(km[0], km[1], km[2], km[3]);
+            dst[1] = make_int4(km[4], km[5], km[6], km[7]);
+          }
+        };
+        if (got) {
+          load(0, va);
+          wait(va);
 #pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                if (hh == 1 && !two) break;
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                  const uint64_t rl = pack2(fmaxf(__uint_as_float(v[hh][2 * e]), 0.f),
-                                            fmaxf(__uint_as_float(v[hh][2 * e + 1]), 0.f));
-                  acc[cc * 16 + e] = fma2(w2[2 * ps + hh], rl, acc[cc * 16 + e]);
-                }
-              }
+          for (int c = 0; c < kNC; c += 2) {
+            load(c + 1, vb);
+            reduce(c, va);
+            wait(vb);
+            if (c + 2 < kNC) {
+              load(c + 2, va);
+            } else {                                  // every load of the pass is done: free the buffer
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bar_tempty[sl]);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar_tempty[buf]);
-            ++nt;
+            reduce(c + 1, vb);
+            if (c + 2 < kNC) wait(va);
           }
-          if (!ok) break;
-          float m = -INFINITY;
-#pragma unroll
-          for (int e = 0; e < 64; e += 2) {
-            float a0, a1, b0, b1;
-            unpack2(acc[e], a0, a1);
-            unpack2(acc[e + 1], b0, b1);
-            m = max3(m, max3(a0, a1, b0), b1);
-          }
-          s_cst[r][j & 31] = m;
-          if ((j & 31) == 31 || j == it.qb - 1) flush(j & ~31, (j & 31) + 1);
         }
-        if (!ok) break;
-        // -inf for the own block and every later entry, one row segment at a time
-        for (int rr = 0; rr < 32; ++rr) {
-          if (row0 + rr >= p.S) break;
-          float* rowp = p.C + it.b * p.cs0 + static_cast<int64_t>(row0 + rr) * p.cs1 + it.g * p.cs2;
-          for (int j = it.qb + lane; j < p.nb_stride; j += 32) rowp[j] = -INFINITY;
+        // all four warps' maxima of this pass are staged (or some warp gave up waiting)
+        if (!(ok = named_bar_and(bar_id, 128, got))) break;
+        if (tw < kQW) {
+          const int* rp = &s_red[sl][np & 1][0][q0 + tw];
+          const int k = max(max(rp[0], rp[kQB]), max(rp[2 * kQB], rp[3 * kQB]));
+          s_cst[sl][q0 + tw][j % kFlush] = score_from_key(k);
+        }
+        ++np;
+        if (j % kFlush == kFlush - 1 || j == it.own - 1) {
+          named_bar_sync(bar_id, 128);
+          const int j0 = j - j % kFlush, cnt = j % kFlush + 1;
+          for (int rr = 0; rr < kQW / 4; ++rr) {     // warp q4: query rows q0 + 8 q4 .. q0 + 8 q4 + 7
+            const int qrow = q0 + q4 * (kQW / 4) + rr;
+            const int i = it.qb * kQB + qrow;
+            if (i < p.S && lane < cnt)
+              p.C[it.b * p.cs0 + static_cast<int64_t>(i) * p.cs1 + it.g * p.cs2 + j0 + lane] = s_cst[sl][qrow][lane];
+          }
         }
       }
+      if (!ok) break;
+      // -inf for the own block and every later entry of the item's rows
+      for (int rr = 0; rr < kQW / 4; ++rr) {
+        const int i = it.qb * kQB + q0 + q4 * (kQW / 4) + rr;
+        if (i >= p.S) break;
+        float* rowp = p.C + it.b * p.cs0 + static_cast<int64_t>(i) * p.cs1 + it.g * p.cs2;
+        for (int jj = it.own + lane; jj < p.nb_stride; jj += 32) rowp[jj] = -INFINITY;
+      }
+      stream_advance(p, st, sl, npairs, true);
     }
   }
 
@@ -303,16 +427,16 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
 msa_status launch_index_prefill(const msa_index_args& a, cudaStream_t stream) {
   DeviceInfo dev;
   if (msa_status st = current_device(&dev); st != MSA_OK) return st;
-  // q_idx as 5-D (dI, h, g, s, b); box = one head of 128 queries
   CUtensorMap qmap, kmap;
   {
+    // q_idx as 5-D (dI, h, g, s, b); box = one head of 64 queries
     const uint64_t dims[5] = {static_cast<uint64_t>(a.dI), static_cast<uint64_t>(a.HI), static_cast<uint64_t>(a.Hkv),
                               static_cast<uint64_t>(a.S), static_cast<uint64_t>(a.B)};
     const uint64_t strides[4] = {static_cast<uint64_t>(a.q_idx_stride[3]) * 2,
                                  static_cast<uint64_t>(a.q_idx_stride[2]) * 2,
                                  static_cast<uint64_t>(a.q_idx_stride[1]) * 2,
                                  static_cast<uint64_t>(a.q_idx_stride[0]) * 2};
-    const uint32_t box[5] = {64, 1, 1, 128, 1};
+    const uint32_t box[5] = {64, 1, 1, kQB, 1};
     if (msa_status st = encode_tiled_map(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, a.q_idx, dims, strides, box,
                                          CU_TENSOR_MAP_SWIZZLE_128B, "q_idx");
         st != MSA_OK)
@@ -325,7 +449,7 @@ msa_status launch_index_prefill(const msa_index_args& a, cudaStream_t stream) {
     const uint64_t strides[3] = {static_cast<uint64_t>(a.k_idx_stride[2]) * 2,
                                  static_cast<uint64_t>(a.k_idx_stride[1]) * 2,
                                  static_cast<uint64_t>(a.k_idx_stride[0]) * 2};
-    const uint32_t box[4] = {64, 1, 128, 1};
+    const uint32_t box[4] = {64, 1, kBk, 1};
     if (msa_status st = encode_tiled_map(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, a.k_idx, dims, strides, box,
                                          CU_TENSOR_MAP_SWIZZLE_128B, "k_idx");
         st != MSA_OK)
@@ -333,19 +457,21 @@ msa_status launch_index_prefill(const msa_index_args& a, cudaStream_t stream) {
   }
   Params p;
   p.B = a.B; p.S = a.S; p.Hkv = a.Hkv; p.HI = a.HI;
-  p.nbq = (a.S + kBk - 1) / kBk;
+  p.nq = (a.S + kQB - 1) / kQB;
   p.nb_stride = a.nb_stride;
   p.w = a.w; p.ws0 = a.w_stride[0]; p.ws1 = a.w_stride[1]; p.ws2 = a.w_stride[2];
   p.C = a.C; p.cs0 = a.C_stride[0]; p.cs1 = a.C_stride[1]; p.cs2 = a.C_stride[2];
   p.dev_err = a.dev_err;
-  const size_t smem = 1024 + (2 * kMaxHI + kKStages) * static_cast<size_t>(kTile);
+  const size_t smem = 1024 + 2 * static_cast<size_t>(kQTile) + static_cast<size_t>(kKStages) * kKTile;
   if (smem > dev.max_smem_optin) return fail(MSA_ERR_UNSUPPORTED, "prefill index score: not enough shared memory");
-  cudaError_t e = cudaFuncSetAttribute(index_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  void (*kern)(const CUtensorMap, const CUtensorMap, const Params) =
+      a.HI == 1 ? index_prefill_kernel<1> : a.HI == 2 ? index_prefill_kernel<2>
+                                          : a.HI == 3 ? index_prefill_kernel<3> : index_prefill_kernel<4>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(index_prefill)");
-  const int64_t npairs = static_cast<int64_t>(a.B) * a.Hkv * ((p.nbq + 1) / 2);
+  const int64_t npairs = static_cast<int64_t>(a.B) * a.Hkv * ((p.nq + 1) / 2);
   const int grid = static_cast<int>(std::min<int64_t>(dev.num_sms, std::max<int64_t>(npairs, 1)));
-  index_prefill_kernel<<<grid, kThreads, smem, stream>>>(qmap, kmap, p);
+  kern<<<grid, kThreads, smem, stream>>>(qmap, kmap, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "index_prefill_kernel launch");
   return MSA_OK;
