@@ -15,8 +15,8 @@
 // With the tokens on M and the four heads side by side on N every MMA is
 // N = 256 (the tensor core's full width), and the epilogue needs no state across
 // passes: thread = token t forms s_t = sum_h w_h ReLU(D[t, (h, q)]) for its
-// queries, the block max over tokens is one `redux.sync.max` per warp and query
-// (order-preserving integer keys) plus a 4-warp combine in shared memory.
+// queries, the block max over tokens is one `redux.sync.max.f32` per warp and
+// query plus a 4-warp combine in shared memory.
 // Items pair query block qb with nq-1-qb (constant cost per pair); a persistent
 // CTA per SM takes pairs round-robin and runs two independent item streams
 // ("slots") at once:
@@ -29,6 +29,8 @@
 //             while the current 8 are reduced).
 #include "msa_internal.h"
 #include "msa_ptx.cuh"
+
+#include <type_traits>
 
 namespace msa {
 namespace {
@@ -109,21 +111,24 @@ __device__ __forceinline__ void stream_init(const Params& p, Stream& s, int slot
   stream_advance(p, s, slot, npairs, keep_empty);
 }
 
-// One pass of stream `st` (slot `slot`): hand it to f(slot, item, j, first,
-// last) and step the stream.  first/last = first/last pass of the item.
-template <class F>
-__device__ __forceinline__ bool stream_pass(const Params& p, Stream& st, int slot, int64_t npairs, F& f) {
+template <int N>
+using SlotC = std::integral_constant<int, N>;
+
+// One pass of stream `st` (slot SLOT): hand it to f(SlotC<SLOT>, item, j,
+// first, last) and step the stream.  first/last = first/last pass of the item.
+template <int SLOT, class F>
+__device__ __forceinline__ bool stream_pass(const Params& p, Stream& st, int64_t npairs, F& f) {
   const Item it = st.it;
   const int j = st.j;
-  if (++st.j == it.own) stream_advance(p, st, slot, npairs, false);
-  return f(slot, it, j, j == 0, j == it.own - 1);
+  if (++st.j == it.own) stream_advance(p, st, SLOT, npairs, false);
+  return f(SlotC<SLOT>{}, it, j, j == 0, j == it.own - 1);
 }
 
 // The merged pass order of the producer and the MMA warp: the two slots'
-// passes alternate while both have passes left.  Both streams stay in
-// registers (a runtime-indexed pair would live in local memory, whose
-// round trips the single-thread loops would pay on every pass).  Stops early
-// when f returns false.
+// passes alternate while both have passes left.  The slot reaches f as a
+// compile-time constant, so per-slot state and barrier addresses need no
+// runtime selection, and both streams stay in registers.  Stops early when f
+// returns false.
 template <class F>
 __device__ __forceinline__ void for_each_pass(const Params& p, int64_t npairs, F&& f) {
   Stream s0, s1;
@@ -142,8 +147,59 @@ __device__ __forceinline__ void for_each_pass(const Params& p, int64_t npairs, F
     } else {
       return;
     }
-    if (!(one ? stream_pass(p, s1, 1, npairs, f) : stream_pass(p, s0, 0, npairs, f))) return;
+    if (!(one ? stream_pass<1>(p, s1, npairs, f) : stream_pass<0>(p, s0, npairs, f))) return;
   }
+}
+
+// Position in a ring of kKStages buffers: stage and the parity of its use.
+struct Ring {
+  int st = 0;
+  uint32_t ph = 0;
+  __device__ __forceinline__ void next() {
+    if (++st == kKStages) {
+      st = 0;
+      ph ^= 1u;
+    }
+  }
+};
+
+// The four K=16 steps of one pass, issued by one elected lane of a converged
+// warp: D[d] = A[a] B[b]^T over K = 64 (descriptor start addresses advance by
+// 32 bytes = 2 units per step inside the 128-byte swizzled rows).
+__device__ __forceinline__ void umma_pass_elect(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p, f, t;\n\t"
+      ".reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+      "setp.ne.b32 f, %4, %4;\n\t"
+      "setp.eq.b32 t, %4, %4;\n\t"
+      "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"
+      "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, f;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, t;\n\t}"
+      ::"r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(0)
+      : "memory");
+}
+// tcgen05.commit from one elected lane of a converged warp.
+__device__ __forceinline__ void umma_commit_elect(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "@p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
+}
+
+// true in exactly one (the lowest) active lane of the warp
+__device__ __forceinline__ bool elect_one() {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r));
+  return r != 0;
 }
 
 // Named barrier over n threads that also returns the AND of `v` over them:
@@ -161,14 +217,12 @@ __device__ __forceinline__ bool named_bar_and(int id, int n, bool v) {
   return r != 0;
 }
 
-// Order-preserving signed-integer key of a float score (larger float, larger
-// key) and its inverse: the magnitude bits of negative values are flipped.
-// Scores here are never -0 (every sum starts from +0).
-__device__ __forceinline__ int score_key(float f) {
-  const int i = __float_as_int(f);
-  return i ^ ((i >> 31) & 0x7FFFFFFF);
+// Max of a float over the 32 lanes of the warp (exact: a max rounds nothing).
+__device__ __forceinline__ float warp_max_f32(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
 }
-__device__ __forceinline__ float score_from_key(int k) { return __int_as_float(k ^ ((k >> 31) & 0x7FFFFFFF)); }
 
 __device__ __forceinline__ uint64_t pack2(float x, float y) {
   uint64_t r;
@@ -206,7 +260,7 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ __align__(16) float2 s_w[2][kQB / 2][kMaxHI];   // per slot: (w[2e][h], w[2e+1][h]) per query pair e
-  __shared__ __align__(16) int s_red[2][2][4][kQB]; // per slot and pass parity: warp maxima per query (keys)
+  __shared__ __align__(16) float s_red[2][2][4][kQB];   // per slot and pass parity: warp maxima per query
   __shared__ float s_cst[2][kQB][kFlush + 1];       // per slot: staged block scores per query row
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -229,66 +283,71 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
 
   if (warp == 0) {
     // ===================== TMA producer =====================
-    if (lane == 0) {
-      int n = 0, nql0 = 0, nql1 = 0;   // k blocks issued; q tiles issued per slot
-      for_each_pass(p, npairs, [&](int slot, const Item& it, int j, bool first, bool) -> bool {
-        if (first) {   // the item's q_idx tile into the slot's buffer, once its previous item is done
-          const int c = slot ? nql1 : nql0;
-          if (!mbar_wait(&bar_qempty[slot], (c & 1) ^ 1, abort_flag, p.dev_err)) return false;
+    // The whole warp runs the (warp-uniform) loop; one elected lane issues.
+    const bool leader = elect_one();
+    Ring kr;
+    int n = 0, nql[2] = {0, 0};   // k blocks issued; q tiles issued per slot
+    for_each_pass(p, npairs, [&](auto slot_c, const Item& it, int j, bool first, bool) -> bool {
+      constexpr int slot = decltype(slot_c)::value;
+      if (first) {   // the item's q_idx tile into the slot's buffer, once its previous item is done
+        if (!__all_sync(0xffffffffu, mbar_wait(&bar_qempty[slot], (nql[slot] & 1) ^ 1, abort_flag, p.dev_err)))
+          return false;
+        if (leader) {
           mbar_arrive_expect_tx(&bar_qfull[slot], HI * kQHead);
+#pragma unroll
           for (int h = 0; h < HI; ++h)
             tma_load_5d(s_q + slot * kQTile + h * kQHead, &qmap, &bar_qfull[slot], 0, h, it.g, it.qb * kQB, it.b);
-          if (slot) nql1 = c + 1; else nql0 = c + 1;
         }
-        const int st = n % kKStages;
-        if (!mbar_wait(&bar_kempty[st], ((n / kKStages) & 1) ^ 1, abort_flag, p.dev_err)) return false;
-        mbar_arrive_expect_tx(&bar_kfull[st], kKTile);
-        tma_load_4d(s_k + st * kKTile, &kmap, &bar_kfull[st], 0, it.g, j * kBk, it.b);
-        ++n;
-        return true;
-      });
-      if (*abort_flag) {  // let loads in flight land before the CTA exits
-        const uint64_t t0 = global_timer_ns();
-        for (int x = max(0, n - kKStages); x < n; ++x)
-          while (!mbar_try_wait(&bar_kfull[x % kKStages], (x / kKStages) & 1) &&
-                 global_timer_ns() - t0 < MSA_WAIT_LIMIT_NS) {
-          }
-        if (nql0 > 0)
-          while (!mbar_try_wait(&bar_qfull[0], (nql0 - 1) & 1) && global_timer_ns() - t0 < MSA_WAIT_LIMIT_NS) {
-          }
-        if (nql1 > 0)
-          while (!mbar_try_wait(&bar_qfull[1], (nql1 - 1) & 1) && global_timer_ns() - t0 < MSA_WAIT_LIMIT_NS) {
-          }
+        ++nql[slot];
       }
-    }
-  } else if (warp == 1) {
-    // ===================== tcgen05 issuer =====================
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(128, kQB * HI, false, false);
-      int n = 0, nqw0 = 0, nqw1 = 0, np0 = 0, np1 = 0;   // passes; q tiles and passes per slot
-      for_each_pass(p, npairs, [&](int slot, const Item&, int, bool first, bool last) -> bool {
-        if (first) {
-          const int c = slot ? nqw1 : nqw0;
-          if (!mbar_wait(&bar_qfull[slot], c & 1, abort_flag, p.dev_err)) return false;
-          if (slot) nqw1 = c + 1; else nqw0 = c + 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar_kempty[kr.st], kr.ph ^ 1, abort_flag, p.dev_err))) return false;
+      if (leader) {
+        mbar_arrive_expect_tx(&bar_kfull[kr.st], kKTile);
+        tma_load_4d(s_k + kr.st * kKTile, &kmap, &bar_kfull[kr.st], 0, it.g, j * kBk, it.b);
+      }
+      kr.next();
+      ++n;
+      return true;
+    });
+    if (leader && *abort_flag) {  // let loads in flight land before the CTA exits
+      const uint64_t t0 = global_timer_ns();
+      for (int x = max(0, n - kKStages); x < n; ++x)
+        while (!mbar_try_wait(&bar_kfull[x % kKStages], (x / kKStages) & 1) &&
+               global_timer_ns() - t0 < MSA_WAIT_LIMIT_NS) {
         }
-        const int st = n % kKStages;
-        const int np = slot ? np1 : np0;
-        if (!mbar_wait(&bar_kfull[st], (n / kKStages) & 1, abort_flag, p.dev_err)) return false;
-        if (!mbar_wait(&bar_tempty[slot], (np & 1) ^ 1, abort_flag, p.dev_err)) return false;
-        tc_fence_after();
-        const uint32_t kb = smem_u32(s_k + st * kKTile), qb = smem_u32(s_q + slot * kQTile);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)   // D[t, (h, q)] += k[t, 16kk..] . q[(h, q), 16kk..]
-          umma_bf16(tmem + slot * kBufCols, sdesc_sw128(kb + 32 * kk, 16, 1024), sdesc_sw128(qb + 32 * kk, 16, 1024),
-                    idesc, kk > 0);
-        umma_commit(&bar_tfull[slot]);
-        umma_commit(&bar_kempty[st]);
-        if (last) umma_commit(&bar_qempty[slot]);
-        if (slot) np1 = np + 1; else np0 = np + 1;
-        ++n;
-        return true;
-      });
+      for (int sl = 0; sl < 2; ++sl)
+        if (nql[sl] > 0)
+          while (!mbar_try_wait(&bar_qfull[sl], (nql[sl] - 1) & 1) && global_timer_ns() - t0 < MSA_WAIT_LIMIT_NS) {
+          }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ===================== tcgen05 issuer (warp-uniform loop, one elected lane issues) =====================
+    constexpr uint32_t idesc = idesc_bf16(128, kQB * HI, false, false);
+    const uint64_t kdesc0 = sdesc_sw128(smem_u32(s_k), 16, 1024);
+    const uint64_t qdesc0 = sdesc_sw128(smem_u32(s_q), 16, 1024);
+    Ring kr;
+    uint32_t qph[2] = {0, 0}, tph[2] = {0, 0};   // parities of the slots' qfull / tempty waits
+    for_each_pass(p, npairs, [&](auto slot_c, const Item&, int, bool first, bool last) -> bool {
+      constexpr int slot = decltype(slot_c)::value;
+      if (first) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bar_qfull[slot], qph[slot], abort_flag, p.dev_err))) return false;
+        qph[slot] ^= 1u;
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar_kfull[kr.st], kr.ph, abort_flag, p.dev_err))) return false;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar_tempty[slot], tph[slot] ^ 1, abort_flag, p.dev_err))) return false;
+      tph[slot] ^= 1u;
+      tc_fence_after();
+      // D[t, (h, q)] = k[t, :] . q[(h, q), :]; descriptor units are 16 bytes
+      umma_pass_elect(tmem + slot * kBufCols, kdesc0 + static_cast<uint64_t>(kr.st * (kKTile >> 4)),
+                      qdesc0 + static_cast<uint64_t>(slot * (kQTile >> 4)), idesc);
+      umma_commit_elect(&bar_tfull[slot]);
+      umma_commit_elect(&bar_kempty[kr.st]);
+      if (last) umma_commit_elect(&bar_qempty[slot]);
+      kr.next();
+      return true;
+    });
+    if (elect_one()) {
       umma_commit(&bar_drain);
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try_wait(&bar_drain, 0) && global_timer_ns() - t0 < MSA_WAIT_LIMIT_NS) {
@@ -325,7 +384,7 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
         // warp-uniform decision: the TMEM loads below are warp-collective
         const bool got = __all_sync(0xffffffffu, mbar_wait(&bar_tfull[sl], np & 1, abort_flag, p.dev_err));
         if (got) tc_fence_after();
-        int* red = &s_red[sl][np & 1][q4][q0];
+        float* red = &s_red[sl][np & 1][q4][q0];
         // chunk c = queries 8c .. 8c+7; the TMEM loads of chunk c+1 are in flight
         // while chunk c is reduced
         uint32_t va[HI][kCQ], vb[HI][kCQ];
@@ -341,7 +400,7 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
         auto reduce = [&](int c, uint32_t (&v)[HI][kCQ]) {
           // s_t = sum_h w_h ReLU(D[t, (h, q)]) for the chunk's 8 queries (two per fma.f32x2),
           // heads in order; then the max over this warp's 32 tokens
-          int km[kCQ];
+          float km[kCQ];
 #pragma unroll
           for (int e = 0; e < kCQ / 2; ++e) {
             const float4* wq = reinterpret_cast<const float4*>(&s_w[sl][(q0 + c * kCQ) / 2 + e][0]);
@@ -355,13 +414,13 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
                          acc);
             float s0, s1;
             unpack2(acc, s0, s1);
-            km[2 * e] = __reduce_max_sync(0xffffffffu, score_key(s0));
-            km[2 * e + 1] = __reduce_max_sync(0xffffffffu, score_key(s1));
+            km[2 * e] = warp_max_f32(s0);
+            km[2 * e + 1] = warp_max_f32(s1);
           }
           if (lane == 0) {
-            int4* dst = reinterpret_cast<int4*>(red + c * kCQ);
-            dst[0] = make_int4(km[0], km[1], km[2], km[3]);
-            dst[1] = make_int4(km[4], km[5], km[6], km[7]);
+            float4* dst = reinterpret_cast<float4*>(red + c * kCQ);
+            dst[0] = make_float4(km[0], km[1], km[2], km[3]);
+            dst[1] = make_float4(km[4], km[5], km[6], km[7]);
           }
         };
         if (got) {
@@ -386,9 +445,8 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
         // all four warps' maxima of this pass are staged (or some warp gave up waiting)
         if (!(ok = named_bar_and(bar_id, 128, got))) break;
         if (tw < kQW) {
-          const int* rp = &s_red[sl][np & 1][0][q0 + tw];
-          const int k = max(max(rp[0], rp[kQB]), max(rp[2 * kQB], rp[3 * kQB]));
-          s_cst[sl][q0 + tw][j % kFlush] = score_from_key(k);
+          const float* rp = &s_red[sl][np & 1][0][q0 + tw];
+          s_cst[sl][q0 + tw][j % kFlush] = fmaxf(fmaxf(rp[0], rp[kQB]), fmaxf(rp[2 * kQB], rp[3 * kQB]));
         }
         ++np;
         if (j % kFlush == kFlush - 1 || j == it.own - 1) {
