@@ -22,9 +22,10 @@
 //                                          V is the MN-major A operand
 //   epilogue: one thread per d, coalesced fp32 partial rows.
 // Warp 0 streams K, V (64 KiB) and the row's 16 Q rows by TMA into a 3-deep
-// ring; warp 1 issues the MMAs (S of the next unit before O of this one);
-// warps 2-5 and 6-9 are two softmax/epilogue warpgroups taking alternate
-// units, each with its own TMEM slot, and merge the rows they complete.
+// ring; warp 1 issues each unit's S and O MMAs as soon as their inputs are ready
+// (polling both); warps 2-5 and 6-9 are two softmax/epilogue warpgroups
+// taking alternate units, each with its own TMEM slot, and merge the rows
+// they complete.
 // Each CTA first copies its units' page ids and valid lengths into shared
 // memory, so no role waits on a global load per unit.
 #include "msa_internal.h"
@@ -44,6 +45,18 @@ constexpr int kThreads = 320;   // w0 TMA, w1 MMA, w2-5 and w6-9 softmax/epilogu
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kMaxUnits = 512;          // (row, page) units per CTA, kept in shared memory
+
+__device__ __forceinline__ float fast_exp2(float x) {   // hardware 2^x (ex2.approx), 2^-inf = 0
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// Max of a float over the 32 lanes of the warp (exact).
+__device__ __forceinline__ float warp_max_f32(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
 
 struct Params {
   int B, Hq, Hkv, G, k;
@@ -73,7 +86,8 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
   __shared__ __align__(8) uint64_t bar_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ float s_red[2][4][kMaxG];
+  __shared__ __align__(16) float s_max[2][4][kMaxG];   // per warpgroup and warp: per-head key maxima
+  __shared__ __align__(16) float s_sum[2][4][kMaxG];   // and sums
   __shared__ int s_upage[kMaxUnits];    // physical page of each unit of this CTA
   __shared__ int s_uvalid[kMaxUnits];   // valid tokens of the page; 0 = no such split
   __shared__ int s_un[kMaxUnits];       // selected pages of the unit's row
@@ -173,49 +187,68 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     }
   } else if (warp == 1) {
     // ===================== tcgen05 issuer =====================
-    // S of unit n+1 is issued before O of unit n, so the two softmax warpgroups
-    // (slot n mod 2) overlap.
+    // S of unit n (keys x heads) needs its stage loaded and its TMEM slot
+    // (n mod 2) free; O of unit n needs P(n).  Both are polled and each MMA
+    // group is issued as soon as its inputs are ready, so O(n) never waits
+    // behind the load of unit n+1.
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 16, false, false);
       constexpr uint32_t idesc_o = idesc_bf16(128, 16, true, false);
       const int nlive = s_nlive;
-      auto issue_s = [&](int n) -> bool {
-        const int st = n % kStages, slot = n & 1;
-        if (!mbar_wait(&bar_full[st], (n / kStages) & 1, abort_flag, p.dev_err)) return false;
-        if (!mbar_wait(&bar_sfree[slot], ((n >> 1) & 1) ^ 1, abort_flag, p.dev_err)) return false;
-        tc_fence_after();
-        const uint32_t sb = smem_u32(s_stage + st * kStageBytes);
+      int ns = 0, no = 0;
+      uint32_t spins = 0;
+      uint64_t idle_since = 0;
+      while (no < nlive) {
+        bool progress = false;
+        if (ns < nlive) {
+          const int st = ns % kStages, slot = ns & 1;
+          if (mbar_test_wait(&bar_full[st], (ns / kStages) & 1) &&
+              mbar_test_wait(&bar_sfree[slot], ((ns >> 1) & 1) ^ 1)) {
+            tc_fence_after();
+            const uint32_t sb = smem_u32(s_stage + st * kStageBytes);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalf + 32 * (kk & 3);
-          const uint32_t qoff = 4 * kHalf + (kk >> 2) * kQHalf + 32 * (kk & 3);
-          umma_bf16(tmem + slot * 32, sdesc_sw128(sb + off, 16, 1024), sdesc_sw128(sb + qoff, 16, 1024), idesc_s,
-                    kk > 0);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t off = (kk >> 2) * kHalf + 32 * (kk & 3);
+              const uint32_t qoff = 4 * kHalf + (kk >> 2) * kQHalf + 32 * (kk & 3);
+              umma_bf16(tmem + slot * 32, sdesc_sw128(sb + off, 16, 1024), sdesc_sw128(sb + qoff, 16, 1024), idesc_s,
+                        kk > 0);
+            }
+            umma_commit(&bar_sfull[slot]);
+            ++ns;
+            progress = true;
+          }
         }
-        umma_commit(&bar_sfull[slot]);
-        return true;
-      };
-      auto issue_o = [&](int n) -> bool {
-        const int st = n % kStages, slot = n & 1;
-        if (!mbar_wait(&bar_pready[slot], (n >> 1) & 1, abort_flag, p.dev_err)) return false;
-        tc_fence_after();
-        const uint32_t sb = smem_u32(s_stage + st * kStageBytes);
-        const uint32_t pb = smem_u32(s_p + slot * kPTile);
+        if (no < ns) {
+          const int st = no % kStages, slot = no & 1;
+          if (mbar_test_wait(&bar_pready[slot], (no >> 1) & 1)) {
+            tc_fence_after();
+            const uint32_t sb = smem_u32(s_stage + st * kStageBytes);
+            const uint32_t pb = smem_u32(s_p + slot * kPTile);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t voff = 2 * kHalf + kk * 2048;          // 16 keys per step
-          const uint32_t poff = (kk >> 2) * kQHalf + 32 * (kk & 3);
-          umma_bf16(tmem + slot * 32 + 16, sdesc_sw128(sb + voff, kHalf, 1024), sdesc_sw128(pb + poff, 16, 1024),
-                    idesc_o, kk > 0);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t voff = 2 * kHalf + kk * 2048;          // 16 keys per step
+              const uint32_t poff = (kk >> 2) * kQHalf + 32 * (kk & 3);
+              umma_bf16(tmem + slot * 32 + 16, sdesc_sw128(sb + voff, kHalf, 1024), sdesc_sw128(pb + poff, 16, 1024),
+                        idesc_o, kk > 0);
+            }
+            umma_commit(&bar_ofull[slot]);
+            umma_commit(&bar_empty[st]);
+            ++no;
+            progress = true;
+          }
         }
-        umma_commit(&bar_ofull[slot]);
-        umma_commit(&bar_empty[st]);
-        return true;
-      };
-      bool ok = nlive > 0 ? issue_s(0) : true;
-      for (int n = 0; n < nlive && ok; ++n) {
-        if (n + 1 < nlive) ok = issue_s(n + 1);
-        if (ok) ok = issue_o(n);
+        if (progress) {
+          spins = 0;
+        } else if ((++spins & 63u) == 0) {
+          const uint64_t now = global_timer_ns();
+          if (spins == 64) idle_since = now;
+          if (*abort_flag) break;
+          if (now - idle_since > MSA_WAIT_LIMIT_NS) {
+            *abort_flag = 1;
+            report(p.dev_err, MSA_DEVERR_TIMEOUT);
+            break;
+          }
+        }
       }
       umma_commit(&bar_drain);
       uint64_t t0 = global_timer_ns();
@@ -318,35 +351,50 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
       tmem_ld8(tmem + lane_addr + slot * 32, sv);
       tmem_ld_wait();
       float z[kMaxG];
-      float mx[kMaxG];
 #pragma unroll
-      for (int h = 0; h < kMaxG; ++h) {
-        z[h] = (t < valid) ? __uint_as_float(sv[h]) * p.scale_log2 : -INFINITY;
-        float v = z[h];
+      for (int h = 0; h < kMaxG; ++h) z[h] = (t < valid) ? __uint_as_float(sv[h]) * p.scale_log2 : -INFINITY;
+      // per-head maximum over this warp's 32 keys (exact), then over the 4 warps
+      {
+        float wm[kMaxG];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-        mx[h] = v;
-      }
-      if (lane == 0) {
-#pragma unroll
-        for (int h = 0; h < kMaxG; ++h) s_red[wg][q][h] = mx[h];
+        for (int h = 0; h < kMaxG; ++h) wm[h] = warp_max_f32(z[h]);
+        if (lane == 0) {
+          float4* d = reinterpret_cast<float4*>(&s_max[wg][q][0]);
+          d[0] = make_float4(wm[0], wm[1], wm[2], wm[3]);
+          d[1] = make_float4(wm[4], wm[5], wm[6], wm[7]);
+        }
       }
       named_bar_sync(bar_id, 128);
-      float l[kMaxG];
-#pragma unroll
-      for (int h = 0; h < kMaxG; ++h) {
-        mx[h] = fmaxf(fmaxf(s_red[wg][0][h], s_red[wg][1][h]), fmaxf(s_red[wg][2][h], s_red[wg][3][h]));
-        const float e = (t < valid) ? exp2f(z[h] - mx[h]) : 0.f;
-        z[h] = e;
-        float v = e;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        l[h] = v;
+      float mx[kMaxG];
+      {
+        const float4* m4 = reinterpret_cast<const float4*>(&s_max[wg][0][0]);
+        const float4 a0 = m4[0], a1 = m4[1], b0 = m4[2], b1 = m4[3], c0 = m4[4], c1 = m4[5], d0 = m4[6], d1 = m4[7];
+        mx[0] = fmaxf(fmaxf(a0.x, b0.x), fmaxf(c0.x, d0.x)); mx[1] = fmaxf(fmaxf(a0.y, b0.y), fmaxf(c0.y, d0.y));
+        mx[2] = fmaxf(fmaxf(a0.z, b0.z), fmaxf(c0.z, d0.z)); mx[3] = fmaxf(fmaxf(a0.w, b0.w), fmaxf(c0.w, d0.w));
+        mx[4] = fmaxf(fmaxf(a1.x, b1.x), fmaxf(c1.x, d1.x)); mx[5] = fmaxf(fmaxf(a1.y, b1.y), fmaxf(c1.y, d1.y));
+        mx[6] = fmaxf(fmaxf(a1.z, b1.z), fmaxf(c1.z, d1.z)); mx[7] = fmaxf(fmaxf(a1.w, b1.w), fmaxf(c1.w, d1.w));
       }
-      named_bar_sync(bar_id, 128);           // everyone has read the maxima
-      if (lane == 0) {
 #pragma unroll
-        for (int h = 0; h < kMaxG; ++h) s_red[wg][q][h] = l[h];
+      for (int h = 0; h < kMaxG; ++h) z[h] = (t < valid) ? fast_exp2(z[h] - mx[h]) : 0.f;
+      // per-head sums over the warp's 32 keys by a transposed butterfly: after
+      // the xor-16/8/4 steps each lane carries one head (lane >> 2), then xor 2, 1
+      {
+        const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+        float u[4], w2[2];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float send = b4 ? z[i] : z[i + 4], keep = b4 ? z[i + 4] : z[i];
+          u[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const float send = b3 ? u[i] : u[i + 2], keep = b3 ? u[i + 2] : u[i];
+          w2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+        }
+        float x = (b2 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? w2[0] : w2[1], 4);
+        x += __shfl_xor_sync(0xffffffffu, x, 2);
+        x += __shfl_xor_sync(0xffffffffu, x, 1);
+        if ((lane & 3) == 0) s_sum[wg][q][lane >> 2] = x;
       }
       // P^T[h][t] into the K-major B tile of this slot
       uint8_t* pt_tile = s_p + slot * kPTile + (t >> 6) * kQHalf;
@@ -363,8 +411,12 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_pready[slot]);
       named_bar_sync(bar_id, 128);
+      float l[kMaxG], inv_l[kMaxG];
 #pragma unroll
-      for (int h = 0; h < kMaxG; ++h) l[h] = s_red[wg][0][h] + s_red[wg][1][h] + s_red[wg][2][h] + s_red[wg][3][h];
+      for (int h = 0; h < kMaxG; ++h) {
+        l[h] = (s_sum[wg][0][h] + s_sum[wg][1][h]) + (s_sum[wg][2][h] + s_sum[wg][3][h]);
+        inv_l[h] = __frcp_rn(l[h]);
+      }
       // ---- O^T ready
       if (!mbar_wait(&bar_ofull[slot], ph_slot, abort_flag, p.dev_err)) s_fail[wg] = 1;
       named_bar_sync(bar_id, 128);
@@ -383,7 +435,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
       for (int h = 0; h < kMaxG; ++h) {
         if (h < G) {
           const int64_t row = (static_cast<int64_t>(r) * G + h) * p.k + s;
-          p.o_part[row * kD + t] = bad ? 0.f : __uint_as_float(ov[h]) / l[h];
+          p.o_part[row * kD + t] = bad ? 0.f : __uint_as_float(ov[h]) * inv_l[h];
           if (t == h) p.lse_part[row] = bad ? -INFINITY : (mx[h] + log2f(l[h])) * kLn2;
         }
       }
