@@ -71,6 +71,11 @@ SMALL = [
     PrefillWorkload("k64_long", B=1, S=9000, shape=MSAShape(Hq=12, Hkv=2, k=64), seed=45),
     PrefillWorkload("msa_shape_s4096", B=1, S=4096, shape=MSAShape(), seed=46),
     PrefillWorkload("tail_1", B=3, S=129, shape=MSAShape(Hq=12, Hkv=2, k=16), seed=47),
+    # shorter than one key block: no index pass runs, every score row is -inf
+    PrefillWorkload("edge_s1", B=2, S=1, shape=MSAShape(Hq=12, Hkv=2, k=4), seed=48),
+    PrefillWorkload("edge_s64", B=1, S=64, shape=MSAShape(), seed=49),
+    # one query block pair with a partial second 64-query block
+    PrefillWorkload("edge_s200_hi2", B=2, S=200, shape=MSAShape(Hq=12, Hkv=2, HI=2, k=2), seed=50),
 ]
 
 
