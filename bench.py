@@ -15,8 +15,9 @@ inputs (the 491 MB index-key pool alone) exceed the 129 MB L2, so no flush is
 needed between steps.  ``roofline`` reports the dominant kernel (decode index
 scoring): algorithmic bytes per launch / its mean event-timed duration against
 the measured HBM copy bandwidth.  ``e2e`` repeats the step through the same C
-ABI with the step's inputs copied from pinned host memory and its output read
-back inside the timed region.  ``cpu_baseline`` times the fp64 oracle on a
+ABI with the step's inputs copied from pinned host memory and its outputs read
+back inside the timed region (inputs and outputs each packed in one buffer:
+one copy each way per step).  ``cpu_baseline`` times the fp64 oracle on a
 bounded sample of the same workload on the host cores.
 
 ``--impl reference`` times the oracle itself (the only reference this method
@@ -193,6 +194,24 @@ def decode_algorithmic_bytes(wl):
     return {"index_kernel": idx + small_idx, "step": idx + small_idx + kv + q_o}
 
 
+def pack_tensors(ts, device):
+    """Copies the tensors into one contiguous byte buffer (256-byte aligned
+    offsets) and returns it with views of the same shapes and dtypes into it."""
+    import torch
+    offs, total = {}, 0
+    for n, t in ts.items():
+        offs[n] = total
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    pack = torch.empty(total, dtype=torch.uint8, device=device)
+    views = {}
+    for n, t in ts.items():
+        nbytes = t.numel() * t.element_size()
+        v = pack[offs[n]: offs[n] + nbytes].view(t.dtype).view(t.shape)
+        v.copy_(t)
+        views[n] = v
+    return pack, views
+
+
 def run_decode_ours(args, wl, world, rank):
     import torch
     import block_sparse_attention_02_gb300 as msa
@@ -201,6 +220,14 @@ def run_decode_ours(args, wl, world, rank):
     inp = decode_inputs(wl, device="cuda")
     bufs = msa.decode_buffers(wl.B, sh.Hq, sh.Hkv, sh.k, inp["seq_pt"].shape[1], "cuda")
     stream = torch.cuda.current_stream()
+    # The per-step inputs (Q, q_idx, w, seq_pt, seq_len) and outputs (O, LSE)
+    # each live in one contiguous device buffer, so that a step's host
+    # round trip is one copy in and one copy out (the page pools stay resident).
+    step_in = ("Q", "q_idx", "w", "seq_pt", "seq_len")
+    in_pack, in_views = pack_tensors({n: inp[n] for n in step_in}, "cuda")
+    inp.update(in_views)
+    out_pack, out_views = pack_tensors({n: bufs[n] for n in ("O", "LSE")}, "cuda")
+    bufs.update(out_views)
 
     def index_part():
         # a1 index score with a2 selection and a3 page table fused into the same kernel
@@ -293,19 +320,15 @@ def run_decode_ours(args, wl, world, rank):
     rest_ms = per_call["attention+merge"]
 
     # ---- end to end through the C ABI with host buffers ----
-    small = ("Q", "q_idx", "w", "seq_pt", "seq_len")
-    host_in = {n: inp[n].cpu().pin_memory() for n in small}
-    host_out = {"O": torch.empty_like(bufs["O"], device="cpu").pin_memory(),
-                "LSE": torch.empty_like(bufs["LSE"], device="cpu").pin_memory()}
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    host_in = in_pack.cpu().pin_memory()          # the step inputs, packed as on the device
+    host_out = torch.empty_like(out_pack, device="cpu").pin_memory()
+    h2d = host_in.numel()
+    d2h = host_out.numel()
 
     def e2e_step():
-        for n in small:
-            inp[n].copy_(host_in[n], non_blocking=True)
+        in_pack.copy_(host_in, non_blocking=True)
         run_step()
-        host_out["O"].copy_(bufs["O"], non_blocking=True)
-        host_out["LSE"].copy_(bufs["LSE"], non_blocking=True)
+        host_out.copy_(out_pack, non_blocking=True)
 
     for _ in range(args.warmup):
         e2e_step()
