@@ -69,29 +69,49 @@ struct CsrParams {
   int32_t* dev_err;
 };
 
-// one thread per (query in chunk, group, slot)
+// Entry e of the chunk as (query in chunk, group, slot).  Lanes of a warp
+// take 32 consecutive queries at the same (group, slot): neighbouring queries
+// mostly select the same block there, so their counter updates combine into
+// one atomic per distinct block (the hot blocks get one update per warp, not
+// one per query).  `where` keeps the (query, group, slot) order.
+struct CsrEntry {
+  int64_t e;     // index into where[nq, Hkv, k]
+  int64_t item;  // (b, g, j) item of the selected block, -1 if the slot is empty
+  int64_t bs;    // flattened query b*S + i
+};
+__device__ __forceinline__ CsrEntry csr_entry(const CsrParams& p, int64_t t, bool report_bad) {
+  const int qi = static_cast<int>(t % p.nq);
+  const int64_t rest = t / p.nq;
+  const int g = static_cast<int>(rest % p.Hkv), s = static_cast<int>(rest / p.Hkv);
+  CsrEntry x;
+  x.e = (static_cast<int64_t>(qi) * p.Hkv + g) * p.k + s;
+  x.bs = p.q0 + qi;
+  x.item = -1;
+  const int b = static_cast<int>(x.bs / p.S), i = static_cast<int>(x.bs % p.S);
+  if (s < p.count[x.bs * p.Hkv + g]) {
+    const int j = p.sel[(x.bs * p.Hkv + g) * p.k + s];
+    if (j < 0 || j > i / kBk) {
+      if (report_bad) report(p.dev_err, MSA_DEVERR_BAD_SEL);
+    } else {
+      x.item = (static_cast<int64_t>(b) * p.Hkv + g) * p.nb + j;
+    }
+  }
+  return x;
+}
+
 __global__ void csr_count_kernel(const CsrParams p) {
   const int64_t total = static_cast<int64_t>(p.nq) * p.Hkv * p.k;
-  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
-       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int s = static_cast<int>(e % p.k);
-    const int64_t qg = e / p.k;
-    const int g = static_cast<int>(qg % p.Hkv);
-    const int qi = static_cast<int>(qg / p.Hkv);
-    const int64_t bs = p.q0 + qi;
-    const int b = static_cast<int>(bs / p.S), i = static_cast<int>(bs % p.S);
-    const int c = p.count[bs * p.Hkv + g];
-    bool live = false;
-    if (s < c) {
-      const int j = p.sel[(bs * p.Hkv + g) * p.k + s];
-      if (j < 0 || j > i / kBk) {
-        report(p.dev_err, MSA_DEVERR_BAD_SEL);
-      } else {
-        atomicAdd(&p.cnt[(static_cast<int64_t>(b) * p.Hkv + g) * p.nb + j], 1);
-        live = true;
-      }
-    }
-    if (!live) p.where[e] = -1;
+  const int lane = threadIdx.x & 31;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  // the loop is warp-uniform: every lane takes part in the match below
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31); base < total;
+       base += stride) {
+    const int64_t t = base + lane;
+    CsrEntry x{0, -1, 0};
+    if (t < total) x = csr_entry(p, t, true);
+    const unsigned grp = __match_any_sync(0xffffffffu, static_cast<int>(x.item));
+    if (x.item >= 0 && lane == __ffs(grp) - 1) atomicAdd(&p.cnt[x.item], __popc(grp));
+    if (t < total && x.item < 0) p.where[x.e] = -1;
   }
 }
 
@@ -155,35 +175,37 @@ __global__ void __launch_bounds__(1024) csr_scan_kernel(const CsrParams p, int64
   }
 }
 
-// one thread per (query in chunk, group, slot): claims the entry's place in its
-// item and writes the entry table and the slot map; the first entry of each
-// tile writes the tile's descriptor
+// Each entry claims its place in its item (lanes of one block in a warp
+// claim consecutive places with one atomic) and writes the entry table and
+// the slot map; the first entry of each tile writes the tile's descriptor.
 __global__ void csr_fill_kernel(const CsrParams p) {
   const int64_t total = static_cast<int64_t>(p.nq) * p.Hkv * p.k;
-  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
-       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int s = static_cast<int>(e % p.k);
-    const int64_t qg = e / p.k;
-    const int g = static_cast<int>(qg % p.Hkv);
-    const int qi = static_cast<int>(qg / p.Hkv);
-    const int64_t bs = p.q0 + qi;
-    const int b = static_cast<int>(bs / p.S), i = static_cast<int>(bs % p.S);
-    const int c = p.count[bs * p.Hkv + g];
-    if (s >= c) continue;
-    const int j = p.sel[(bs * p.Hkv + g) * p.k + s];
-    if (j < 0 || j > i / kBk) continue;
-    const int64_t item = (static_cast<int64_t>(b) * p.Hkv + g) * p.nb + j;
-    const int pos = atomicAdd(&p.cursor[item], 1);
-    const int idx = pos - p.off[item];                                  // entry index within the item
-    const int es = p.tile_off[item] * kEntries + idx;                   // entry slot in tile order
-    p.tile_q[es] = static_cast<int>(bs);
-    p.where[e] = es * 8;                                                // tile row of head 0
-    if (idx % kEntries == 0) {
-      const int c = p.off[item + 1] - p.off[item], u = idx / kEntries, nt = tiles_of(c);
-      const int flags = (u == 0 ? kTileFirst : 0) | (u == nt - 1 ? kTileLast : 0);
-      p.tile_info[es / kEntries] = make_int4(static_cast<int>(item), min(kEntries, c - idx), p.ord[item], flags);
+  const int lane = threadIdx.x & 31;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31); base < total;
+       base += stride) {
+    const int64_t t = base + lane;
+    CsrEntry x{0, -1, 0};
+    if (t < total) x = csr_entry(p, t, false);
+    const unsigned grp = __match_any_sync(0xffffffffu, static_cast<int>(x.item));
+    if (x.item >= 0) {   // no early exit: every lane reaches the next iteration's match together
+      const int leader = __ffs(grp) - 1;
+      int pos0 = 0;
+      if (lane == leader) pos0 = atomicAdd(&p.cursor[x.item], __popc(grp));
+      pos0 = __shfl_sync(grp, pos0, leader);
+      const int pos = pos0 + __popc(grp & ((1u << lane) - 1u));
+      const int64_t item = x.item;
+      const int idx = pos - p.off[item];                                  // entry index within the item
+      const int es = p.tile_off[item] * kEntries + idx;                   // entry slot in tile order
+      p.tile_q[es] = static_cast<int>(x.bs);
+      p.where[x.e] = es * 8;                                              // tile row of head 0
+      if (idx % kEntries == 0) {
+        const int c = p.off[item + 1] - p.off[item], u = idx / kEntries, nt = tiles_of(c);
+        const int flags = (u == 0 ? kTileFirst : 0) | (u == nt - 1 ? kTileLast : 0);
+        p.tile_info[es / kEntries] = make_int4(static_cast<int>(item), min(kEntries, c - idx), p.ord[item], flags);
+      }
     }
-
+    __syncwarp();
   }
 }
 
