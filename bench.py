@@ -346,7 +346,9 @@ def run_decode_ours(args, wl, world, rank):
     peaks = load_peaks()
     alg = decode_algorithmic_bytes(wl)
     achieved = alg["index_kernel"] / (idx_ms * 1e-3) / 1e9
-    traffic, traffic_src = read_profile_traffic(f"index_decode_{wl.name}.txt", DECODE_INDEX_FILES)
+    # profiles/index_decode_<workload without its "decode_" prefix>.txt
+    short = wl.name[len("decode_"):] if wl.name.startswith("decode_") else wl.name
+    traffic, traffic_src = read_profile_traffic(f"index_decode_{short}.txt", DECODE_INDEX_FILES)
     tokens_per_step = wl.B * world
     step_ms = total_ms / K
     res = {
