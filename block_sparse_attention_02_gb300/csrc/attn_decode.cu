@@ -104,10 +104,12 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
   // this CTA's units: page id, valid length and row size, read once
   for (int64_t u = lo + tid; u < hi; u += kThreads) {
     const int r = static_cast<int>(u / p.k), s = static_cast<int>(u % p.k);
-    const int nr = min(max(p.n[r], 0), p.k);
+    // the three loads are independent: one round trip to L2
+    const int n_raw = p.n[r], page = p.pt[u], ll = p.last_len[r];
+    const int nr = min(max(n_raw, 0), p.k);
     const bool live = s < nr;
-    s_upage[u - lo] = live ? p.pt[u] : -1;
-    s_uvalid[u - lo] = live ? (s == nr - 1 ? min(max(p.last_len[r], 1), kBk) : kBk) : 0;
+    s_upage[u - lo] = live ? page : -1;
+    s_uvalid[u - lo] = live ? (s == nr - 1 ? min(max(ll, 1), kBk) : kBk) : 0;
     s_un[u - lo] = nr;
     if (nr == 0 && s == 0) {   // a row with nothing selected: O = 0, LSE = -inf
       for (int h = 0; h < p.G; ++h) {
