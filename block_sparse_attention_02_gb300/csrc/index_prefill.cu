@@ -203,7 +203,7 @@ __device__ __forceinline__ bool elect_one() {
 }
 
 // Named barrier over n threads that also returns the AND of `v` over them:
-// every warp of an epilogue group leaves a pass with the same verdict.
+// every warp of an epilogue group leaves a pass with the same decision.
 __device__ __forceinline__ bool named_bar_and(int id, int n, bool v) {
   uint32_t r;
   asm volatile(
