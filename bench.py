@@ -281,7 +281,16 @@ def run_decode_ours(args, wl, world, rank):
     assert int(bufs["dev_err"].item()) == 0, "device error during the timed steps"
 
     # ---- per-call breakdown (separate pass, one graph per C-ABI call; not part of `value`) ----
+    # The cache append (the step before a decode step) rewrites each sequence's
+    # current token with the values it already holds, so the cache is unchanged.
+    L = inp["seq_len"].long()
+    pages = inp["seq_pt"].long().gather(1, ((L - 1) // sh.Bk).view(-1, 1)).view(-1)
+    slot = (L - 1) % sh.Bk
+    new_tok = [pool[pages, :, slot, :].contiguous() for pool in (inp["K_pool"], inp["V_pool"], inp["kidx_pool"])]
     calls = {
+        "cache_append (the step before)": lambda: msa.msa_cache_append(*new_tok, inp["K_pool"], inp["V_pool"],
+                                                                        inp["kidx_pool"], inp["seq_pt"],
+                                                                        inp["seq_len"], dev_err=bufs["dev_err"]),
         "index_score+topk+page_table": index_part,
         "topk (standalone)": lambda: msa.msa_topk_blocks(msa.MSA_MODE_DECODE, bufs["C"], sh.k, bufs["sel"],
                                                          bufs["count"], seq_len=inp["seq_len"],

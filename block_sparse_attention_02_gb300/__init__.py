@@ -24,7 +24,8 @@ from ._abi import (MSA_DEVERR_BAD_LEN, MSA_DEVERR_BAD_PAGE, MSA_DEVERR_BAD_SEL, 
 __all__ = [
     "msa_index_score", "msa_topk_blocks", "msa_build_page_table", "msa_sparse_attn_prefill",
     "msa_sparse_attn_decode", "msa_sparse_attn_decode_noalloc", "msa_lse_merge", "msa_sparse_attn_prefill_workspace_size",
-    "msa_sparse_attn_decode_workspace_size", "decode_step", "prefill_layer", "lib", "MSAError",
+    "msa_sparse_attn_decode_workspace_size", "msa_cache_append", "decode_step", "prefill_layer", "lib",
+    "MSAError",
     "MSA_MODE_PREFILL", "MSA_MODE_DECODE", "MSA_DEVERR_TIMEOUT", "MSA_DEVERR_BAD_PAGE",
     "MSA_DEVERR_BAD_SEL", "MSA_DEVERR_BAD_LEN", "Bk", "D", "dI",
 ]
@@ -266,6 +267,41 @@ def msa_lse_merge(O_part: torch.Tensor, LSE_part: torch.Tensor, O: torch.Tensor,
             raise ValueError(f"{nm} must be contiguous")
     _abi.check(lib().msa_lse_merge(_ptr(O_part), _ptr(LSE_part), rows, parts, d, _ptr(O), _ptr(LSE),
                                    _ptr(dev_err), _stream(stream)), "msa_lse_merge")
+
+
+# ---------------------------------------------------------------------------
+# the step before a decode step: append the current tokens to the paged caches
+# ---------------------------------------------------------------------------
+
+def msa_cache_append(K_new: torch.Tensor, V_new: torch.Tensor, kidx_new: torch.Tensor, K_pool: torch.Tensor,
+                     V_pool: torch.Tensor, kidx_pool: torch.Tensor, seq_pt: torch.Tensor, seq_len: torch.Tensor,
+                     *, dev_err=None, stream=None) -> None:
+    """Writes token L_b - 1 of every sequence into its page (see msa.h, cache append).
+
+    K_new, V_new [B,Hkv,D], kidx_new [B,Hkv,dI] bf16; K_pool, V_pool [P,Hkv,Bk,D] and
+    kidx_pool [P,Hkv,Bk,dI] bf16; seq_pt [B,max_pages] int32 (contiguous rows), seq_len [B].
+    """
+    for t, nm in ((K_new, "K_new"), (V_new, "V_new"), (kidx_new, "kidx_new"), (K_pool, "K_pool"),
+                  (V_pool, "V_pool"), (kidx_pool, "kidx_pool")):
+        _inner_contig(t, nm)
+    if K_pool.stride() != V_pool.stride():
+        raise ValueError("K_pool and V_pool must share strides")
+    if not seq_pt.is_contiguous():
+        raise ValueError("seq_pt must be contiguous")
+    a = _abi.AppendArgs()
+    a.B, a.Hkv, a.D = K_new.shape
+    a.dI, a.Bk = kidx_new.shape[2], K_pool.shape[2]
+    a.K_new, a.V_new, a.kidx_new = _ptr(K_new), _ptr(V_new), _ptr(kidx_new)
+    a.K_new_stride[:] = _strides(K_new, 2)
+    a.V_new_stride[:] = _strides(V_new, 2)
+    a.kidx_new_stride[:] = _strides(kidx_new, 2)
+    a.K_pool, a.V_pool, a.kidx_pool = _ptr(K_pool), _ptr(V_pool), _ptr(kidx_pool)
+    a.kv_stride[:] = _strides(K_pool, 3)
+    a.kidx_stride[:] = _strides(kidx_pool, 3)
+    a.num_pages = K_pool.shape[0]
+    a.seq_pt, a.max_pages, a.seq_len = _ptr(seq_pt), seq_pt.shape[1], _ptr(seq_len)
+    a.dev_err = _ptr(dev_err)
+    _abi.check(lib().msa_cache_append(C.byref(a), _stream(stream)), "msa_cache_append")
 
 
 # ---------------------------------------------------------------------------

@@ -76,6 +76,16 @@ class DecodeArgs(C.Structure):
     ]
 
 
+class AppendArgs(C.Structure):
+    _fields_ = [
+        ("B", C.c_int), ("Hkv", C.c_int), ("D", C.c_int), ("dI", C.c_int), ("Bk", C.c_int),
+        ("K_new", _p), ("K_new_stride", _i64x2), ("V_new", _p), ("V_new_stride", _i64x2),
+        ("kidx_new", _p), ("kidx_new_stride", _i64x2),
+        ("K_pool", _p), ("V_pool", _p), ("kv_stride", _i64x3), ("kidx_pool", _p), ("kidx_stride", _i64x3),
+        ("num_pages", C.c_int64), ("seq_pt", _p), ("max_pages", C.c_int64), ("seq_len", _p), ("dev_err", _p),
+    ]
+
+
 # exported function name -> (restype, argtypes)
 SIGNATURES = {
     "msa_version": (C.c_int, []),
@@ -91,6 +101,7 @@ SIGNATURES = {
     "msa_sparse_attn_decode": (C.c_int, [C.POINTER(DecodeArgs), _p, C.c_size_t, _p]),
     "msa_sparse_attn_decode_noalloc": (C.c_int, [C.POINTER(DecodeArgs), _p]),
     "msa_lse_merge": (C.c_int, [_p, _p, C.c_int64, C.c_int, C.c_int, _p, _p, _p, _p]),
+    "msa_cache_append": (C.c_int, [C.POINTER(AppendArgs), _p]),
 }
 
 _lock = threading.Lock()

@@ -331,4 +331,30 @@ msa_status msa_lse_merge(const float* O_part, const float* LSE_part, int64_t row
   return launch_lse_merge(O_part, LSE_part, rows, parts, D, O, LSE, dev_err, reinterpret_cast<cudaStream_t>(stream));
 }
 
+// ---------------------------------------------------------------------------
+msa_status msa_cache_append(const msa_append_args* a, msa_stream_t stream) {
+  g_last_error.clear();
+  MSA_REQUIRE(a != nullptr, MSA_ERR_INVALID_ARG, "args is NULL");
+  MSA_REQUIRE(a->B >= 0 && a->Hkv >= 1, MSA_ERR_INVALID_ARG, "B = %d, Hkv = %d", a->B, a->Hkv);
+  MSA_REQUIRE(a->Bk == kBk, MSA_ERR_UNSUPPORTED, "Bk = %d, supported %d", a->Bk, kBk);
+  MSA_REQUIRE(a->D >= 8 && a->D % 8 == 0 && a->dI >= 8 && a->dI % 8 == 0, MSA_ERR_UNSUPPORTED,
+              "D = %d, dI = %d: need positive multiples of 8", a->D, a->dI);
+  MSA_REQUIRE(a->num_pages >= 1 && a->max_pages >= 1 && a->max_pages < (int64_t(1) << 31) / a->Bk,
+              MSA_ERR_INVALID_ARG, "num_pages = %" PRId64 ", max_pages = %" PRId64, a->num_pages, a->max_pages);
+  MSA_REQUIRE(a->K_new && a->V_new && a->kidx_new && a->K_pool && a->V_pool && a->kidx_pool && a->seq_pt && a->seq_len,
+              MSA_ERR_INVALID_ARG, "tensor pointers must be non-NULL");
+  MSA_REQUIRE(aligned16(a->K_new) && aligned16(a->V_new) && aligned16(a->kidx_new) && aligned16(a->K_pool) &&
+                  aligned16(a->V_pool) && aligned16(a->kidx_pool),
+              MSA_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  for (int i = 0; i < 2; ++i)
+    MSA_REQUIRE(vec_stride_ok(a->K_new_stride[i], 2) && vec_stride_ok(a->V_new_stride[i], 2) &&
+                    vec_stride_ok(a->kidx_new_stride[i], 2),
+                MSA_ERR_INVALID_ARG, "new-token strides must be positive multiples of 8 elements");
+  for (int i = 0; i < 3; ++i)
+    MSA_REQUIRE(vec_stride_ok(a->kv_stride[i], 2) && vec_stride_ok(a->kidx_stride[i], 2), MSA_ERR_INVALID_ARG,
+                "pool strides must be positive multiples of 8 elements");
+  if (a->B == 0) return MSA_OK;
+  return launch_cache_append(*a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

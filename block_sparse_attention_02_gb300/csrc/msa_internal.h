@@ -46,6 +46,7 @@ msa_status launch_lse_merge(const float* o_part, const float* lse_part, int64_t 
 msa_status launch_lse_merge_bf16(const __nv_bfloat16* o_part, const float* lse_part, int64_t rows, int parts, int D,
                                  __nv_bfloat16* O, float* LSE, cudaStream_t stream);
 msa_status launch_attn_prefill(const msa_prefill_args& a, void* ws, size_t ws_bytes, cudaStream_t stream);
+msa_status launch_cache_append(const msa_append_args& a, cudaStream_t stream);
 // Host-side argument checks of msa_sparse_attn_decode (no CUDA call).
 msa_status check_decode_args(const msa_decode_args* a);
 size_t attn_prefill_workspace_size(const msa_prefill_args& a, int64_t chunk_queries);

@@ -339,6 +339,47 @@ msa_status msa_sparse_attn_decode_noalloc(const msa_decode_args *args, msa_strea
 msa_status msa_lse_merge(const float *O_part, const float *LSE_part, int64_t rows, int parts,
                          int D, void *O, float *LSE, int32_t *dev_err, msa_stream_t stream);
 
+/* --------------------------------------------------------------------------
+ * Cache append: the step before a decode step
+ *
+ * Writes each sequence's current token into the 128-token paged caches that
+ * index scoring and attention read ([serving], "MSA con paged attention":
+ * fixed-size pages; the current token's K, V and index key are in the cache
+ * before the step).  For sequence b of length L_b (the new token at position
+ * L_b - 1), page = seq_pt[b][(L_b - 1) / Bk], t = (L_b - 1) % Bk, and every
+ * KV group g:
+ *     K_pool[page, g, t, :]    = K_new[b, g, :]
+ *     V_pool[page, g, t, :]    = V_new[b, g, :]
+ *     kidx_pool[page, g, t, :] = kidx_new[b, g, :]
+ *     K_new, V_new [B, Hkv, D] bf16 strides (b, g); kidx_new [B, Hkv, dI] bf16
+ *     strides (b, g); pools as in msa_sparse_attn_decode / msa_index_score
+ *     (element strides (page, g, t)); seq_pt [B, max_pages], seq_len [B].
+ * A sequence whose length is outside [1, max_pages * Bk] (MSA_DEVERR_BAD_LEN)
+ * or whose page id is outside [0, num_pages) (MSA_DEVERR_BAD_PAGE) is not
+ * written.  Pointers and strides must be 16-byte aligned; D and dI multiples of 8.
+ * ------------------------------------------------------------------------ */
+typedef struct msa_append_args {
+    int B, Hkv, D, dI, Bk;
+    const void *K_new;
+    int64_t K_new_stride[2];
+    const void *V_new;
+    int64_t V_new_stride[2];
+    const void *kidx_new;
+    int64_t kidx_new_stride[2];
+    void *K_pool;
+    void *V_pool;
+    int64_t kv_stride[3];
+    void *kidx_pool;
+    int64_t kidx_stride[3];
+    int64_t num_pages;
+    const int32_t *seq_pt;
+    int64_t max_pages;
+    const int32_t *seq_len;
+    int32_t *dev_err;
+} msa_append_args;
+
+msa_status msa_cache_append(const msa_append_args *args, msa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -25,6 +25,9 @@ Functions and the passages they follow (page title and passage):
 * ``page_table`` -- decode page table from the selected blocks with the KV
   group flattened into the batch (same post, paragraph "MSA con paged
   attention").
+* ``cache_append`` -- the step before a decode step: the current token's K, V
+  and index key written into the fixed-size pages (same paragraph; the token
+  is in the cache before the step).  Plain numpy copies.
 """
 from __future__ import annotations
 
@@ -237,3 +240,30 @@ def own_blocks_prefill(S: int, Bk: int, rows):
 def own_blocks_decode(seq_len, Bk: int):
     """Own block (L_b - 1) // Bk of each decode sequence (index bookkeeping)."""
     return ((_i64(seq_len) - 1) // Bk).astype(np.int32)
+
+
+def cache_append(K_new, V_new, kidx_new, K_pool, V_pool, kidx_pool, seq_pt, seq_len, Bk: int):
+    """The three pools after token L_b - 1 of every sequence b is written to slot
+    (L_b - 1) % Bk of page seq_pt[b][(L_b - 1) // Bk] (raw 16-bit patterns, copies;
+    the inputs are not modified).  Sequences whose length is outside
+    [1, max_pages * Bk] or whose page id is outside the pool are left out and
+    listed in the returned ``skipped``."""
+    K, V, X = _u16(K_pool).copy(), _u16(V_pool).copy(), _u16(kidx_pool).copy()
+    kn, vn, xn = _u16(K_new), _u16(V_new), _u16(kidx_new)
+    pt, sl = _i32(seq_pt), _i32(seq_len)
+    P, max_pages = K.shape[0], pt.shape[1]
+    skipped = []
+    for b in range(sl.shape[0]):
+        L = int(sl[b])
+        if L < 1 or L > max_pages * Bk:
+            skipped.append(b)
+            continue
+        page = int(pt[b, (L - 1) // Bk])
+        if page < 0 or page >= P:
+            skipped.append(b)
+            continue
+        t = (L - 1) % Bk
+        K[page, :, t, :] = kn[b]
+        V[page, :, t, :] = vn[b]
+        X[page, :, t, :] = xn[b]
+    return K, V, X, skipped

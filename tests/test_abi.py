@@ -42,7 +42,8 @@ def test_exports_every_declared_symbol(abi):
 
 def test_struct_layout_matches_header(abi, tmp_path):
     structs = {"msa_index_args": abi.IndexArgs, "msa_topk_args": abi.TopkArgs,
-               "msa_prefill_args": abi.PrefillArgs, "msa_decode_args": abi.DecodeArgs}
+               "msa_prefill_args": abi.PrefillArgs, "msa_decode_args": abi.DecodeArgs,
+               "msa_append_args": abi.AppendArgs}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "msa.h"', "int main(void) {"]
     for cname, py in structs.items():
         lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
@@ -177,3 +178,11 @@ def test_valid_call_without_device_reports_cuda_error(abi):
     a = _index_args(abi)
     assert lib.msa_index_score(C.byref(a), None) == abi.MSA_ERR_CUDA
     assert b"cuda" in lib.msa_last_error_string().lower()
+
+
+def test_cache_append_rejects(abi):
+    a = abi.AppendArgs()
+    a.B, a.Hkv, a.D, a.dI, a.Bk = 2, 2, 128, 64, 64          # Bk must be 128
+    assert abi.load().msa_cache_append(C.byref(a), None) == 2
+    a.Bk = 128
+    assert abi.load().msa_cache_append(C.byref(a), None) == 1   # NULL pointers

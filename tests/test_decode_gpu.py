@@ -212,3 +212,36 @@ def test_decode_b1_l1048576_unfused(msa):
     u = run_gpu(msa, inp, wl.shape.k, fused=False)
     for n in ("sel", "count", "pt", "n", "last_len"):
         assert torch.equal(f[n], u[n]), n
+
+
+def _bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("bad", [False, True], ids=["valid", "bad_len_and_page"])
+def test_cache_append_matches_oracle(msa, bad):
+    """msa_cache_append writes token L-1 of every sequence into its page slot,
+    bit for bit as the oracle's copies; a bad length or page id is flagged and
+    that sequence writes nothing."""
+    g = torch.Generator(device="cuda").manual_seed(61)
+    P, Hkv, Bk_, D_, dI_, mp = 64, 8, 128, 128, 64, 8
+    seq_len = torch.tensor([1, 127, 128, 129, 700, 1024], dtype=torch.int32, device="cuda")
+    B = seq_len.shape[0]
+    pools = [torch.randn(P, Hkv, Bk_, d, generator=g, device="cuda").to(torch.bfloat16) for d in (D_, D_, dI_)]
+    new = [torch.randn(B, Hkv, d, generator=g, device="cuda").to(torch.bfloat16) for d in (D_, D_, dI_)]
+    seq_pt = torch.randperm(P, generator=g, device="cuda")[: B * mp].view(B, mp).to(torch.int32).contiguous()
+    if bad:
+        seq_len[0] = 0                                   # not a valid length
+        seq_pt[3, (129 - 1) // 128] = P + 3              # page id outside the pool
+    K2, V2, X2, skipped = oracle.cache_append(*new, *pools, seq_pt, seq_len, 128)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    msa.msa_cache_append(*new, *pools, seq_pt, seq_len, dev_err=err)
+    torch.cuda.synchronize()
+    for got, want in zip(pools, (K2, V2, X2)):
+        assert np.array_equal(_bits(got), want)
+    e = int(err.item())
+    if bad:
+        assert skipped == [0, 3]
+        assert e & msa.MSA_DEVERR_BAD_LEN and e & msa.MSA_DEVERR_BAD_PAGE
+    else:
+        assert skipped == [] and e == 0

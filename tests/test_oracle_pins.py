@@ -373,3 +373,32 @@ def test_decode_own_block_and_last_len():
     assert list(last.reshape(4, sh.Hkv)[:, 0]) == [1, 128, 1, 97]
     assert list(cnt[:, 0]) == [1, 1, 2, 16]
     assert np.all(C[0] == -np.inf) and np.all(C[3, :, 468:] == -np.inf) and np.all(np.isfinite(C[3, :, :468]))
+
+
+def test_cache_append_slots_by_hand():
+    """Token L-1 lands in slot (L-1) % 128 of page seq_pt[b][(L-1) // 128], in
+    every group, and nothing else changes: lengths 1, 128, 129 and 300 give
+    (block 0, slot 0), (0, 127), (1, 0) and (2, 43) by hand; a length of 0 and a
+    page id outside the pool are skipped."""
+    P, Hkv, Bk, D, dI = 8, 2, 128, 16, 8
+    K = np.zeros((P, Hkv, Bk, D), dtype=np.uint16)
+    V = np.zeros((P, Hkv, Bk, D), dtype=np.uint16)
+    X = np.zeros((P, Hkv, Bk, dI), dtype=np.uint16)
+    seq_pt = np.array([[5, 1, 2], [3, 0, 4], [6, 7, 2], [2, 4, 1], [0, 1, 3], [4, 99, 5]], dtype=np.int32)
+    seq_len = np.array([1, 128, 129, 300, 0, 200], dtype=np.int32)
+    B = seq_len.shape[0]
+    kn = (np.arange(B * Hkv * D, dtype=np.uint16) + 1).reshape(B, Hkv, D)
+    vn = (np.arange(B * Hkv * D, dtype=np.uint16) + 1000).reshape(B, Hkv, D)
+    xn = (np.arange(B * Hkv * dI, dtype=np.uint16) + 2000).reshape(B, Hkv, dI)
+    K2, V2, X2, skipped = oracle.cache_append(kn, vn, xn, K, V, X, seq_pt, seq_len, Bk)
+    assert skipped == [4, 5]   # length 0; page 99 is outside the pool of 8
+    expect = {0: (5, 0), 1: (3, 127), 2: (7, 0), 3: (1, 43)}   # b -> (page, slot)
+    for b, (page, t) in expect.items():
+        for g in range(Hkv):
+            assert np.array_equal(K2[page, g, t], kn[b, g])
+            assert np.array_equal(V2[page, g, t], vn[b, g])
+            assert np.array_equal(X2[page, g, t], xn[b, g])
+    written = np.zeros((P, Hkv, Bk), dtype=bool)
+    for page, t in expect.values():
+        written[page, :, t] = True
+    assert not K2[~written].any() and not V2[~written].any() and not X2[~written].any()
