@@ -178,14 +178,15 @@ DECODE_INDEX_FILES = ["block_sparse_attention_02_gb300/csrc/index_decode.cu",
                       "block_sparse_attention_02_gb300/csrc/select_warp.cuh"]
 
 
-def decode_algorithmic_bytes(wl):
-    """Algorithmic HBM bytes of one decode step (unmasked, selected work only)."""
+def decode_algorithmic_bytes(wl, shared_index=False):
+    """Algorithmic HBM bytes of one decode step (unmasked, selected work only).
+    With ``shared_index`` one index-key pool serves every KV group."""
     sh = wl.shape
     idx = 0
     kv = 0
     for L in wl.lengths:
         own = (L - 1) // sh.Bk
-        idx += sh.Hkv * own * sh.Bk * sh.dI * 2                  # k_idx of every scored block
+        idx += (1 if shared_index else sh.Hkv) * own * sh.Bk * sh.dI * 2   # k_idx of every scored block
         nsel = min(own, sh.k - 1)
         kv += sh.Hkv * (nsel * sh.Bk + (L - own * sh.Bk)) * sh.D * 2 * 2   # selected K and V tokens
     small_idx = wl.B * sh.Hkv * (sh.HI * sh.dI * 2 + sh.HI * 4) + wl.B * sh.Hkv * max(
@@ -218,6 +219,8 @@ def run_decode_ours(args, wl, world, rank):
     from workloads import decode_inputs
     sh = wl.shape
     inp = decode_inputs(wl, device="cuda")
+    if args.shared_index:   # one index-key pool for all KV groups: group stride 0
+        inp["kidx_pool"] = inp["kidx_pool"][:, :1].expand(-1, sh.Hkv, -1, -1)
     bufs = msa.decode_buffers(wl.B, sh.Hq, sh.Hkv, sh.k, inp["seq_pt"].shape[1], "cuda")
     stream = torch.cuda.current_stream()
     # The per-step inputs (Q, q_idx, w, seq_pt, seq_len) and outputs (O, LSE)
@@ -353,11 +356,12 @@ def run_decode_ours(args, wl, world, rank):
     e2e_ms = max_over_ranks(s2.elapsed_time(e2), world)
 
     peaks = load_peaks()
-    alg = decode_algorithmic_bytes(wl)
+    alg = decode_algorithmic_bytes(wl, args.shared_index)
     achieved = alg["index_kernel"] / (idx_ms * 1e-3) / 1e9
     # profiles/index_decode_<workload without its "decode_" prefix>.txt
     short = wl.name[len("decode_"):] if wl.name.startswith("decode_") else wl.name
-    traffic, traffic_src = read_profile_traffic(f"index_decode_{short}.txt", DECODE_INDEX_FILES)
+    traffic, traffic_src = read_profile_traffic(
+        f"index_decode_{'shared_' if args.shared_index else ''}{short}.txt", DECODE_INDEX_FILES)
     tokens_per_step = wl.B * world
     step_ms = total_ms / K
     res = {
@@ -368,7 +372,9 @@ def run_decode_ours(args, wl, world, rank):
                    "context": wl.lengths[0] if len(set(wl.lengths)) == 1 else f"ragged {min(wl.lengths)}..{max(wl.lengths)}, total {sum(wl.lengths)}",
                    "Hq": wl.shape.Hq,
                    "Hkv": wl.shape.Hkv, "D": wl.shape.D, "HI": wl.shape.HI, "dI": wl.shape.dI, "Bk": wl.shape.Bk,
-                   "k": wl.shape.k, "pages": "128-token, shuffled", "cuda_graphs": graphs,
+                   "k": wl.shape.k, "pages": "128-token, shuffled",
+                   "index_keys": "one pool shared by the KV groups" if args.shared_index else "per KV group",
+                   "cuda_graphs": graphs,
                    "scratch": "zero-filled once; calls skip the counter clears (scratch_zeroed) and leave them zero",
                    "l2": f"no flush: inputs larger than L2 ({alg['index_kernel'] / 1e6:.0f} MB of k_idx read per step)",
                    "parallelism": f"replicas x{world}"},
@@ -509,6 +515,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--prefill-chunk", type=int, default=8192)
+    ap.add_argument("--shared-index", action="store_true",
+                    help="decode with one index-key pool for all KV groups (k_idx group stride 0)")
     ap.add_argument("--seq", type=int, default=None, help="override the prefill sequence length (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:

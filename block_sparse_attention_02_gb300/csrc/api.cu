@@ -200,7 +200,8 @@ msa_status msa_index_score(const msa_index_args* a, msa_stream_t stream) {
   MSA_REQUIRE(a->max_pages >= 1 && a->max_pages < (int64_t(1) << 31) / a->Bk, MSA_ERR_INVALID_ARG,
               "max_pages = %" PRId64, a->max_pages);
   for (int i = 0; i < 3; ++i) {
-    MSA_REQUIRE(vec_stride_ok(a->k_idx_stride[i], 2), MSA_ERR_INVALID_ARG,
+    // a group stride of 0: one index-key pool shared by all KV groups
+    MSA_REQUIRE(vec_stride_ok(a->k_idx_stride[i], 2) || (i == 1 && a->k_idx_stride[i] == 0), MSA_ERR_INVALID_ARG,
                 "k_idx_stride[%d] = %" PRId64 " must be a positive multiple of 8 elements", i, a->k_idx_stride[i]);
     MSA_REQUIRE(i == 2 || vec_stride_ok(a->q_idx_stride[i], 2), MSA_ERR_INVALID_ARG,
                 "q_idx_stride[%d] = %" PRId64 " must be a positive multiple of 8 elements", i, a->q_idx_stride[i]);
@@ -348,11 +349,12 @@ msa_status msa_cache_append(const msa_append_args* a, msa_stream_t stream) {
               MSA_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
   for (int i = 0; i < 2; ++i)
     MSA_REQUIRE(vec_stride_ok(a->K_new_stride[i], 2) && vec_stride_ok(a->V_new_stride[i], 2) &&
-                    vec_stride_ok(a->kidx_new_stride[i], 2),
+                    (vec_stride_ok(a->kidx_new_stride[i], 2) || (i == 1 && a->kidx_new_stride[i] == 0)),
                 MSA_ERR_INVALID_ARG, "new-token strides must be positive multiples of 8 elements");
   for (int i = 0; i < 3; ++i)
-    MSA_REQUIRE(vec_stride_ok(a->kv_stride[i], 2) && vec_stride_ok(a->kidx_stride[i], 2), MSA_ERR_INVALID_ARG,
-                "pool strides must be positive multiples of 8 elements");
+    MSA_REQUIRE(vec_stride_ok(a->kv_stride[i], 2) &&
+                    (vec_stride_ok(a->kidx_stride[i], 2) || (i == 1 && a->kidx_stride[i] == 0)),
+                MSA_ERR_INVALID_ARG, "pool strides must be positive multiples of 8 elements (k_idx: group stride 0 allowed)");
   if (a->B == 0) return MSA_OK;
   return launch_cache_append(*a, reinterpret_cast<cudaStream_t>(stream));
 }

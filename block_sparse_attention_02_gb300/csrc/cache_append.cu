@@ -51,7 +51,9 @@ __global__ void __launch_bounds__(256) cache_append_kernel(const AppendParams p)
   const int t = (L - 1) % p.Bk;
   copy_row(p.K_pool + page * p.kv0 + g * p.kv1 + t * p.kv2, p.K_new + b * p.kn0 + g * p.kn1, p.D * 2, lane);
   copy_row(p.V_pool + page * p.kv0 + g * p.kv1 + t * p.kv2, p.V_new + b * p.vn0 + g * p.vn1, p.D * 2, lane);
-  copy_row(p.kidx_pool + page * p.x0 + g * p.x1 + t * p.x2, p.kidx_new + b * p.xn0 + g * p.xn1, p.dI * 2, lane);
+  // one index-key pool shared by the groups (group stride 0): group 0 writes it
+  if (p.x1 != 0 || g == 0)
+    copy_row(p.kidx_pool + page * p.x0 + g * p.x1 + t * p.x2, p.kidx_new + b * p.xn0 + g * p.xn1, p.dI * 2, lane);
 }
 
 }  // namespace

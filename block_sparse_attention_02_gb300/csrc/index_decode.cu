@@ -39,6 +39,11 @@ constexpr int kSlotCols = 16;
 constexpr int kTmemCols = 128;
 constexpr int kStageBytes = kBk * kDI * 2;   // 16 KiB
 constexpr int kQTileBytes = 16 * kDI * 2;    // 2 KiB: 16 rows (HI used) x 64
+// Shared-index variant (one k_idx pool for all KV groups): an item is (b, j),
+// the B operand holds the index heads of all groups (g*HI + h, HI = 4,
+// Hkv <= 8: 32 rows) and one M=128 x N=32 contraction scores every group.
+constexpr int kSharedRows = 32;
+constexpr int kSharedHI = 4;
 constexpr int kThreads = 192;
 // Partial-max buffers of the epilogue.  A warp can be at most kSlots items
 // ahead of the slowest one (TMEM slots are released by all four), so twice
@@ -230,21 +235,28 @@ __device__ void select_long_row(const Params& p, int b, int g, int own, uint64_t
   __syncthreads();
 }
 
+template <bool SHARED>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
+  constexpr int QROWS = SHARED ? kSharedRows : 16;            // rows of the B operand (N)
+  constexpr int SLOT = SHARED ? kSharedRows : kSlotCols;      // TMEM columns per slot
+  constexpr int TCOLS = SHARED ? 2 * kTmemCols : kTmemCols;
+  constexpr int QTILE = QROWS * kDI * 2;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* s_stage = smem;                                   // kStages x 16 KiB
-  uint8_t* s_q = smem + kStages * kStageBytes;               // 2 x 2 KiB
-  int* s_pre = reinterpret_cast<int*>(s_q + 2 * kQTileBytes); // B + 1
+  uint8_t* s_q = smem + kStages * kStageBytes;               // 2 q_idx tiles
+  int* s_pre = reinterpret_cast<int*>(s_q + 2 * QTILE);      // B + 1
   int* s_own = s_pre + (p.B + 1);                             // B
+  // items per (b, j): one per group, or one for all groups with a shared index
+  const int hkv_items = SHARED ? 1 : p.Hkv;
 
   __shared__ __align__(8) uint64_t bar_full[kStages], bar_empty[kStages];
   __shared__ __align__(8) uint64_t bar_tfull[kSlots], bar_tempty[kSlots];
   __shared__ __align__(8) uint64_t bar_qdone[2], bar_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ uint32_t s_red[kRedBufs][4];
+  __shared__ uint32_t s_red[kRedBufs][4][SHARED ? 8 : 1];
   __shared__ int s_cnt[kRedBufs];
   __shared__ int s_chunk[kThreads];
 
@@ -266,7 +278,7 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
     const int per = (p.B + kThreads - 1) / kThreads;
     const int b0 = tid * per, b1 = min(p.B, b0 + per);
     int sum = 0;
-    for (int b = b0; b < b1; ++b) sum += s_own[b] * p.Hkv;
+    for (int b = b0; b < b1; ++b) sum += s_own[b] * hkv_items;
     s_chunk[tid] = sum;
     __syncthreads();
     if (tid == 0) {
@@ -276,7 +288,7 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
     }
     __syncthreads();
     int run = s_chunk[tid];
-    for (int b = b0; b < b1; ++b) { s_pre[b] = run; run += s_own[b] * p.Hkv; }
+    for (int b = b0; b < b1; ++b) { s_pre[b] = run; run += s_own[b] * hkv_items; }
   }
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) { mbar_init(&bar_full[i], 1); mbar_init(&bar_empty[i], 1); }
@@ -286,7 +298,7 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
     for (int i = 0; i < kRedBufs; ++i) s_cnt[i] = 0;
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(&s_tmem, kTmemCols);
+  if (warp == 1) tmem_alloc(&s_tmem, TCOLS);
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
@@ -340,7 +352,7 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
       Walker w;
       int64_t page = -1;
       if (lane < nb) {
-        walk_init(w, lo + base + lane, s_pre, s_own, p.B, p.Hkv);
+        walk_init(w, lo + base + lane, s_pre, s_own, p.B, hkv_items);
         page = p.seq_pt[w.b * p.max_pages + w.j];
       }
       for (int i = 0; i < nb; ++i) {
@@ -374,9 +386,9 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
     }
   } else if (warp == 1) {
     // ===================== tcgen05 issuer =====================
-    constexpr uint32_t idesc = idesc_bf16(128, 16, false, false);
+    constexpr uint32_t idesc = idesc_bf16(128, QROWS, false, false);
     Walker it;
-    if (count > 0) walk_init(it, lo, s_pre, s_own, p.B, p.Hkv);
+    if (count > 0) walk_init(it, lo, s_pre, s_own, p.B, hkv_items);
     int cur_b = -1, cur_g = -1, seg = -1;
     for (int n = 0; n < count; ++n) {
       const int st = n % kStages, slot = n % kSlots;
@@ -389,12 +401,18 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
         if (seg >= 2 && lane == 0) ok = mbar_wait(&bar_qdone[buf], ((seg >> 1) - 1) & 1, abort_flag, p.dev_err);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        uint8_t* qt = s_q + buf * kQTileBytes;
-        for (int c = lane; c < 16 * 8; c += 32) {
+        uint8_t* qt = s_q + buf * QTILE;
+        for (int c = lane; c < QROWS * 8; c += 32) {
           const int r = c >> 3, ch = c & 7;
           uint4 v = make_uint4(0, 0, 0, 0);
-          if (r < p.HI)
-            v = *reinterpret_cast<const uint4*>(p.q_idx + it.b * p.qs0 + it.g * p.qs1 + r * p.qs2 + ch * 8);
+          if constexpr (SHARED) {   // row r = (group r / HI, head r % HI)
+            if (r < p.Hkv * kSharedHI)
+              v = *reinterpret_cast<const uint4*>(p.q_idx + it.b * p.qs0 + (r / kSharedHI) * p.qs1 +
+                                                  (r % kSharedHI) * p.qs2 + ch * 8);
+          } else {
+            if (r < p.HI)
+              v = *reinterpret_cast<const uint4*>(p.q_idx + it.b * p.qs0 + it.g * p.qs1 + r * p.qs2 + ch * 8);
+          }
           *reinterpret_cast<uint4*>(qt + sw128_offset(r, ch)) = v;
         }
         fence_proxy_async_smem();
@@ -409,10 +427,10 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
         if (ok) {
           tc_fence_after();
           const uint32_t a0 = smem_u32(s_stage + st * kStageBytes);
-          const uint32_t b0 = smem_u32(s_q + (seg & 1) * kQTileBytes);
+          const uint32_t b0 = smem_u32(s_q + (seg & 1) * QTILE);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            umma_bf16(tmem + slot * kSlotCols, sdesc_sw128(a0 + 32 * k, 16, 1024), sdesc_sw128(b0 + 32 * k, 16, 1024),
+            umma_bf16(tmem + slot * SLOT, sdesc_sw128(a0 + 32 * k, 16, 1024), sdesc_sw128(b0 + 32 * k, 16, 1024),
                       idesc, k > 0);
           umma_commit(&bar_empty[st]);
           umma_commit(&bar_tfull[slot]);
@@ -420,7 +438,7 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
-      walk_next(it, s_own, p.B, p.Hkv);
+      walk_next(it, s_own, p.B, hkv_items);
     }
     if (lane == 0) {  // every MMA issued by this thread is complete before TMEM is freed
       umma_commit(&bar_drain);
@@ -436,55 +454,85 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
     Walker it;
     int64_t page_cur = 0;
     if (count > 0) {
-      walk_init(it, lo, s_pre, s_own, p.B, p.Hkv);
+      walk_init(it, lo, s_pre, s_own, p.B, hkv_items);
       page_cur = p.seq_pt[it.b * p.max_pages + it.j];
     }
     int cur_b = -1, cur_g = -1;
-    float wv[kMaxHI] = {0.f, 0.f, 0.f, 0.f};
+    constexpr int NW = SHARED ? kSharedRows : kMaxHI;   // weights: (g, h) pairs, or the HI heads of one group
+    constexpr int NG = SHARED ? 8 : 1;                  // groups scored per item
+    float wv[NW];
+#pragma unroll
+    for (int c = 0; c < NW; ++c) wv[c] = 0.f;
     for (int n = 0; n < count; ++n) {
       const int slot = n % kSlots;
       // the next item's page id is loaded one item ahead, off the critical path
       Walker nxt = it;
       int64_t page_next = 0;
       if (n + 1 < count) {
-        walk_next(nxt, s_own, p.B, p.Hkv);
+        walk_next(nxt, s_own, p.B, hkv_items);
         page_next = p.seq_pt[nxt.b * p.max_pages + nxt.j];
       }
       if (it.b != cur_b || it.g != cur_g) {
-        for (int h = 0; h < kMaxHI; ++h) wv[h] = h < p.HI ? p.w[it.b * p.ws0 + it.g * p.ws1 + h] : 0.f;
+#pragma unroll
+        for (int c = 0; c < NW; ++c) {
+          if constexpr (SHARED)
+            wv[c] = c < p.Hkv * kSharedHI ? p.w[it.b * p.ws0 + (c / kSharedHI) * p.ws1 + c % kSharedHI] : 0.f;
+          else
+            wv[c] = c < p.HI ? p.w[it.b * p.ws0 + it.g * p.ws1 + c] : 0.f;
+        }
         cur_b = it.b;
         cur_g = it.g;
       }
       // the warp decides together: the TMEM load below is warp-collective
       if (!__all_sync(0xffffffffu, mbar_wait(&bar_tfull[slot], (n / kSlots) & 1, abort_flag, p.dev_err))) break;
       tc_fence_after();
-      uint32_t v[4];
-      tmem_ld4(tmem + lane_addr + slot * kSlotCols, v);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_tempty[slot]);
-      float s = 0.f;
+      uint32_t wmax[NG];
+      if constexpr (SHARED) {
+        uint32_t v[kSharedRows];
+        tmem_ld32(tmem + lane_addr + slot * SLOT, v);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_tempty[slot]);
 #pragma unroll
-      for (int h = 0; h < kMaxHI; ++h) s = fmaf(wv[h], fmaxf(__uint_as_float(v[h]), 0.f), s);
-      // warp max in one step on order-preserving integer keys
-      const uint32_t wmax = redux_max_u32(float_order_key(s));
+        for (int g = 0; g < NG; ++g) {
+          float sg = 0.f;
+#pragma unroll
+          for (int h = 0; h < kSharedHI; ++h)
+            sg = fmaf(wv[g * kSharedHI + h], fmaxf(__uint_as_float(v[g * kSharedHI + h]), 0.f), sg);
+          wmax[g] = redux_max_u32(float_order_key(sg));
+        }
+      } else {
+        uint32_t v[4];
+        tmem_ld4(tmem + lane_addr + slot * SLOT, v);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_tempty[slot]);
+        float sg = 0.f;
+#pragma unroll
+        for (int h = 0; h < kMaxHI; ++h) sg = fmaf(wv[h], fmaxf(__uint_as_float(v[h]), 0.f), sg);
+        // warp max in one step on order-preserving integer keys
+        wmax[0] = redux_max_u32(float_order_key(sg));
+      }
       // cross-warp max without a barrier: the last of the four warps to arrive
-      // combines the partial maxima and stores the block score.
+      // combines the partial maxima and stores the block score(s).
       if (lane == 0) {
         const int rb = n % kRedBufs;
-        s_red[rb][q] = wmax;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) s_red[rb][q][g] = wmax[g];
         __threadfence_block();
         if (atomicAdd(&s_cnt[rb], 1) == 3) {
           __threadfence_block();
-          const uint32_t mk = max(max(s_red[rb][0], s_red[rb][1]), max(s_red[rb][2], s_red[rb][3]));
           s_cnt[rb] = 0;
-          float m = float_from_order_key(mk);
-          if (page_cur < 0 || page_cur >= p.num_pages) {
-            m = -INFINITY;
-            report(p.dev_err, MSA_DEVERR_BAD_PAGE);
+          const bool bad = page_cur < 0 || page_cur >= p.num_pages;
+          if (bad) report(p.dev_err, MSA_DEVERR_BAD_PAGE);
+          const int ng = SHARED ? p.Hkv : 1;
+          for (int g = 0; g < ng; ++g) {
+            const uint32_t mk = max(max(s_red[rb][0][g], s_red[rb][1][g]), max(s_red[rb][2][g], s_red[rb][3][g]));
+            const int gg = SHARED ? g : it.g;
+            p.C[it.b * p.cs0 + gg * p.cs1 + it.j] = bad ? -INFINITY : float_from_order_key(mk);
           }
-          p.C[it.b * p.cs0 + it.g * p.cs1 + it.j] = m;
         }
       }
       it = nxt;
@@ -496,7 +544,7 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, TCOLS);
   }
 
   // ---- fused selection: the CTA whose scores complete a (b, g) row selects it ----
@@ -515,9 +563,10 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
     __threadfence();                                   // this CTA's scores, device-wide
     // this CTA's items cover the contiguous rows r_first .. r_last
     Walker wf, wl;
-    walk_init(wf, lo, s_pre, s_own, p.B, p.Hkv);
-    walk_init(wl, hi - 1, s_pre, s_own, p.B, p.Hkv);
-    const int r_first = wf.b * p.Hkv + wf.g, r_last = wl.b * p.Hkv + wl.g;
+    walk_init(wf, lo, s_pre, s_own, p.B, hkv_items);
+    walk_init(wl, hi - 1, s_pre, s_own, p.B, hkv_items);
+    // with a shared index an item of sequence b counts toward all its groups' rows
+    const int r_first = wf.b * p.Hkv + wf.g, r_last = wl.b * p.Hkv + (SHARED ? p.Hkv - 1 : wl.g);
     for (int base = r_first; base <= r_last; base += kThreads) {
       if (tid == 0) { s_nrows = 0; s_nlong = 0; }
       __syncthreads();
@@ -525,7 +574,7 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
       if (r <= r_last) {
         const int b = r / p.Hkv, g = r % p.Hkv;
         const int own = s_own[b];
-        const int64_t row_start = s_pre[b] + static_cast<int64_t>(g) * own;
+        const int64_t row_start = s_pre[b] + (SHARED ? 0 : static_cast<int64_t>(g) * own);
         const int64_t mine64 = min(row_start + own, hi) - max(row_start, lo);
         if (own > 0 && mine64 > 0) {
           const int mine = static_cast<int>(mine64);
@@ -583,11 +632,16 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
 msa_status launch_index_decode(const msa_index_args& a, cudaStream_t stream) {
   DeviceInfo dev;
   if (msa_status st = current_device(&dev); st != MSA_OK) return st;
-  // k_idx pool as a 4-D tensor (dI, t, g, page) with a 64 x 128 x 1 x 1 box
+  // k_idx pool as a 4-D tensor (dI, t, g, page) with a 64 x 128 x 1 x 1 box; a
+  // group stride of 0 means one index pool shared by all groups (a g extent of 1)
+  const bool shared = a.k_idx_stride[1] == 0;
+  if (shared && (a.HI != kSharedHI || a.Hkv * a.HI > kSharedRows))
+    return fail(MSA_ERR_UNSUPPORTED, "shared index keys (k_idx group stride 0): supported for HI = 4 and Hkv <= 8");
   CUtensorMap kmap;
   const uint64_t dims[4] = {static_cast<uint64_t>(a.dI), static_cast<uint64_t>(a.Bk),
-                            static_cast<uint64_t>(a.Hkv), static_cast<uint64_t>(a.num_pages)};
-  const uint64_t strides[3] = {static_cast<uint64_t>(a.k_idx_stride[2]) * 2, static_cast<uint64_t>(a.k_idx_stride[1]) * 2,
+                            static_cast<uint64_t>(shared ? 1 : a.Hkv), static_cast<uint64_t>(a.num_pages)};
+  const uint64_t strides[3] = {static_cast<uint64_t>(a.k_idx_stride[2]) * 2,
+                               static_cast<uint64_t>(shared ? a.k_idx_stride[2] * a.Bk : a.k_idx_stride[1]) * 2,
                                static_cast<uint64_t>(a.k_idx_stride[0]) * 2};
   const uint32_t box[4] = {64, 128, 1, 1};
   if (msa_status st = encode_tiled_map(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, a.k_idx, dims, strides, box,
@@ -606,17 +660,18 @@ msa_status launch_index_decode(const msa_index_args& a, cudaStream_t stream) {
   p.k = a.k; p.sel = a.sel; p.count = a.count; p.pt = a.pt; p.n_out = a.n; p.last_len = a.last_len;
   p.counter = a.row_scratch;
 
-  const size_t smem = 1024 + kStages * kStageBytes + 2 * kQTileBytes + (2 * static_cast<size_t>(a.B) + 1) * 4;
+  const size_t qtile = static_cast<size_t>(shared ? kSharedRows : 16) * kDI * 2;
+  const size_t smem = 1024 + kStages * kStageBytes + 2 * qtile + (2 * static_cast<size_t>(a.B) + 1) * 4;
   if (smem > dev.max_smem_optin) return fail(MSA_ERR_UNSUPPORTED, "decode index score: batch too large for shared memory");
-  cudaError_t e = cudaFuncSetAttribute(index_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  auto kern = shared ? index_decode_kernel<true> : index_decode_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(index_decode)");
   if (p.sel != nullptr && !a.scratch_zeroed) {   // otherwise zero by contract
     e = cudaMemsetAsync(p.counter, 0, static_cast<size_t>(a.B) * a.Hkv * sizeof(int32_t), stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(index row counters)");
   }
   const int grid = dev.num_sms * kCtasPerSm;
-  index_decode_kernel<<<grid, kThreads, smem, stream>>>(kmap, p);
+  kern<<<grid, kThreads, smem, stream>>>(kmap, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "index_decode_kernel launch");
   return MSA_OK;

@@ -357,6 +357,8 @@ msa_status msa_lse_merge(const float *O_part, const float *LSE_part, int64_t row
  * A sequence whose length is outside [1, max_pages * Bk] (MSA_DEVERR_BAD_LEN)
  * or whose page id is outside [0, num_pages) (MSA_DEVERR_BAD_PAGE) is not
  * written.  Pointers and strides must be 16-byte aligned; D and dI multiples of 8.
+ * A kidx_pool group stride of 0 (one index-key pool shared by the KV groups,
+ * as msa_index_score accepts) stores the index key of group 0 only.
  * ------------------------------------------------------------------------ */
 typedef struct msa_append_args {
     int B, Hkv, D, dI, Bk;

@@ -242,12 +242,14 @@ def own_blocks_decode(seq_len, Bk: int):
     return ((_i64(seq_len) - 1) // Bk).astype(np.int32)
 
 
-def cache_append(K_new, V_new, kidx_new, K_pool, V_pool, kidx_pool, seq_pt, seq_len, Bk: int):
+def cache_append(K_new, V_new, kidx_new, K_pool, V_pool, kidx_pool, seq_pt, seq_len, Bk: int,
+                 shared_index: bool = False):
     """The three pools after token L_b - 1 of every sequence b is written to slot
     (L_b - 1) % Bk of page seq_pt[b][(L_b - 1) // Bk] (raw 16-bit patterns, copies;
     the inputs are not modified).  Sequences whose length is outside
     [1, max_pages * Bk] or whose page id is outside the pool are left out and
-    listed in the returned ``skipped``."""
+    listed in the returned ``skipped``.  With ``shared_index`` the index-key
+    pool is one pool for all groups and takes group 0's key."""
     K, V, X = _u16(K_pool).copy(), _u16(V_pool).copy(), _u16(kidx_pool).copy()
     kn, vn, xn = _u16(K_new), _u16(V_new), _u16(kidx_new)
     pt, sl = _i32(seq_pt), _i32(seq_len)
@@ -265,5 +267,5 @@ def cache_append(K_new, V_new, kidx_new, K_pool, V_pool, kidx_pool, seq_pt, seq_
         t = (L - 1) % Bk
         K[page, :, t, :] = kn[b]
         V[page, :, t, :] = vn[b]
-        X[page, :, t, :] = xn[b]
+        X[page, :, t, :] = xn[b] if not shared_index else xn[b, 0]
     return K, V, X, skipped

@@ -218,11 +218,13 @@ def _bits(t):
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-@pytest.mark.parametrize("bad", [False, True], ids=["valid", "bad_len_and_page"])
-def test_cache_append_matches_oracle(msa, bad):
+@pytest.mark.parametrize("bad,shared", [(False, False), (True, False), (False, True)],
+                         ids=["valid", "bad_len_and_page", "shared_index_pool"])
+def test_cache_append_matches_oracle(msa, bad, shared):
     """msa_cache_append writes token L-1 of every sequence into its page slot,
     bit for bit as the oracle's copies; a bad length or page id is flagged and
-    that sequence writes nothing."""
+    that sequence writes nothing; a shared index-key pool (group stride 0)
+    takes group 0's key."""
     g = torch.Generator(device="cuda").manual_seed(61)
     P, Hkv, Bk_, D_, dI_, mp = 64, 8, 128, 128, 64, 8
     seq_len = torch.tensor([1, 127, 128, 129, 700, 1024], dtype=torch.int32, device="cuda")
@@ -233,7 +235,9 @@ def test_cache_append_matches_oracle(msa, bad):
     if bad:
         seq_len[0] = 0                                   # not a valid length
         seq_pt[3, (129 - 1) // 128] = P + 3              # page id outside the pool
-    K2, V2, X2, skipped = oracle.cache_append(*new, *pools, seq_pt, seq_len, 128)
+    if shared:   # one index pool for all groups, seen through a broadcast view
+        pools[2] = pools[2][:, :1].expand(-1, Hkv, -1, -1)
+    K2, V2, X2, skipped = oracle.cache_append(*new, *pools, seq_pt, seq_len, 128, shared_index=shared)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     msa.msa_cache_append(*new, *pools, seq_pt, seq_len, dev_err=err)
     torch.cuda.synchronize()
@@ -245,3 +249,22 @@ def test_cache_append_matches_oracle(msa, bad):
         assert e & msa.MSA_DEVERR_BAD_LEN and e & msa.MSA_DEVERR_BAD_PAGE
     else:
         assert skipped == [] and e == 0
+
+
+SHARED_INDEX = [
+    DecodeWorkload("shared_edges", lengths=(1, 2, 127, 128, 129, 257, 1000, 2049, 5000), shape=MSAShape(), seed=62),
+    DecodeWorkload("shared_hkv4", lengths=(3000, 20000, 640), shape=MSAShape(Hq=24, Hkv=4, k=16), seed=63),
+]
+
+
+@pytest.mark.parametrize("wl", SHARED_INDEX, ids=[w.name for w in SHARED_INDEX])
+def test_decode_shared_index_keys(msa, wl):
+    """One index-key pool for all KV groups (k_idx group stride 0, the lighter
+    index): each (page) block is scored for every group in one pass; scores,
+    selection, page table and attention match the oracle on the broadcast pool."""
+    inp = decode_inputs(wl, device="cuda")
+    base = inp["kidx_pool"][:, :1]
+    inp["kidx_pool"] = base.expand(-1, wl.shape.Hkv, -1, -1)
+    assert inp["kidx_pool"].stride(1) == 0
+    exact, tie, errs = check_decode(msa, wl, inp, wl.shape.k)
+    print(f"{wl.name}: exact rows {exact}, near-tie rows {tie}, O max/mean {errs[0]:.2e}/{errs[1]:.2e}")
