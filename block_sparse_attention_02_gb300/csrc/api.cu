@@ -184,8 +184,8 @@ msa_status msa_index_score(const msa_index_args* a, msa_stream_t stream) {
     for (int i = 0; i < 4; ++i)
       MSA_REQUIRE(vec_stride_ok(a->q_idx_stride[i], 2), MSA_ERR_INVALID_ARG,
                   "q_idx_stride[%d] = %" PRId64 " must be a positive multiple of 8 elements", i, a->q_idx_stride[i]);
-    for (int i = 0; i < 3; ++i)
-      MSA_REQUIRE(vec_stride_ok(a->k_idx_stride[i], 2), MSA_ERR_INVALID_ARG,
+    for (int i = 0; i < 3; ++i)   // strides (b, s, g); a group stride of 0: one k_idx for all KV groups
+      MSA_REQUIRE(vec_stride_ok(a->k_idx_stride[i], 2) || (i == 2 && a->k_idx_stride[i] == 0), MSA_ERR_INVALID_ARG,
                   "k_idx_stride[%d] = %" PRId64 " must be a positive multiple of 8 elements", i, a->k_idx_stride[i]);
     for (int i = 0; i < 3; ++i)
       MSA_REQUIRE(a->w_stride[i] > 0 && a->C_stride[i] > 0, MSA_ERR_INVALID_ARG, "w / C strides must be positive");

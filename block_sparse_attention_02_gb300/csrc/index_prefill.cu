@@ -49,6 +49,7 @@ constexpr int kFlush = 32;                          // block scores staged per q
 
 struct Params {
   int B, S, Hkv, HI, nq, nb_stride;                 // nq = ceil(S / 64)
+  int kgroups;                                      // 0: one k_idx shared by all groups (group stride 0)
   const float* w;
   int64_t ws0, ws1, ws2;
   float* C;
@@ -303,7 +304,7 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
       if (!__all_sync(0xffffffffu, mbar_wait(&bar_kempty[kr.st], kr.ph ^ 1, abort_flag, p.dev_err))) return false;
       if (leader) {
         mbar_arrive_expect_tx(&bar_kfull[kr.st], kKTile);
-        tma_load_4d(s_k + kr.st * kKTile, &kmap, &bar_kfull[kr.st], 0, it.g, j * kBk, it.b);
+        tma_load_4d(s_k + kr.st * kKTile, &kmap, &bar_kfull[kr.st], 0, p.kgroups ? it.g : 0, j * kBk, it.b);
       }
       kr.next();
       ++n;
@@ -501,10 +502,13 @@ msa_status launch_index_prefill(const msa_index_args& a, cudaStream_t stream) {
       return st;
   }
   {
-    // k_idx as 4-D (dI, g, s, b); box = 128 tokens of one group
-    const uint64_t dims[4] = {static_cast<uint64_t>(a.dI), static_cast<uint64_t>(a.Hkv), static_cast<uint64_t>(a.S),
-                              static_cast<uint64_t>(a.B)};
-    const uint64_t strides[3] = {static_cast<uint64_t>(a.k_idx_stride[2]) * 2,
+    // k_idx as 4-D (dI, g, s, b); box = 128 tokens of one group.  A group
+    // stride of 0 (one k_idx for all groups) becomes a g extent of 1.
+    // (k_idx_stride is (b, s, g): the group stride is the last one)
+    const bool shared = a.k_idx_stride[2] == 0;
+    const uint64_t dims[4] = {static_cast<uint64_t>(a.dI), static_cast<uint64_t>(shared ? 1 : a.Hkv),
+                              static_cast<uint64_t>(a.S), static_cast<uint64_t>(a.B)};
+    const uint64_t strides[3] = {static_cast<uint64_t>(shared ? a.k_idx_stride[1] : a.k_idx_stride[2]) * 2,
                                  static_cast<uint64_t>(a.k_idx_stride[1]) * 2,
                                  static_cast<uint64_t>(a.k_idx_stride[0]) * 2};
     const uint32_t box[4] = {64, 1, kBk, 1};
@@ -516,6 +520,7 @@ msa_status launch_index_prefill(const msa_index_args& a, cudaStream_t stream) {
   Params p;
   p.B = a.B; p.S = a.S; p.Hkv = a.Hkv; p.HI = a.HI;
   p.nq = (a.S + kQB - 1) / kQB;
+  p.kgroups = a.k_idx_stride[2] != 0;
   p.nb_stride = a.nb_stride;
   p.w = a.w; p.ws0 = a.w_stride[0]; p.ws1 = a.w_stride[1]; p.ws2 = a.w_stride[2];
   p.C = a.C; p.cs0 = a.C_stride[0]; p.cs1 = a.C_stride[1]; p.cs2 = a.C_stride[2];

@@ -98,7 +98,8 @@ const char *msa_status_string(msa_status s);
  *   same sequence's index keys.
  *     q_idx [B, S, Hkv, HI, dI] bf16, strides q_idx_stride = (b, s, g, h)
  *     w     [B, S, Hkv, HI]     fp32, strides w_stride     = (b, s, g)
- *     k_idx [B, S, Hkv, dI]     bf16, strides k_idx_stride = (b, s, g)
+ *     k_idx [B, S, Hkv, dI]     bf16, strides k_idx_stride = (b, s, g); a group
+ *           stride of 0 means one index-key tensor shared by all KV groups
  *     C     [B, S, Hkv, nb_stride] fp32, strides C_stride = (b, s, g),
  *           nb_stride >= ceil(S / Bk)
  * DECODE: one query per sequence at position L_b - 1 (its own token already in
@@ -106,7 +107,9 @@ const char *msa_status_string(msa_status s);
  *   Bk tokens: logical block j of sequence b is page seq_pt[b][j].
  *     q_idx [B, Hkv, HI, dI] bf16, strides (b, g, h, unused)
  *     w     [B, Hkv, HI]     fp32, strides (b, g, unused)
- *     k_idx page pool [num_pages, Hkv, Bk, dI] bf16, strides (page, g, t)
+ *     k_idx page pool [num_pages, Hkv, Bk, dI] bf16, strides (page, g, t); a
+ *           group stride of 0 means one pool shared by all KV groups (scored
+ *           once per block for every group; HI = 4 and Hkv <= 8)
  *     seq_pt [B, max_pages] int32 (row stride max_pages), seq_len [B] int32
  *     C     [B, Hkv, nb_stride] fp32, strides (b, g, unused);
  *           nb_stride >= max over b of ceil(L_b / Bk) (entries past the own

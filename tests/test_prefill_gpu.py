@@ -138,3 +138,14 @@ def test_prefill_s131072_sampled(msa):
     rows = sampled_rows(wl.S, wl.shape.Bk, 24, seed=1)
     exact, tie, errs, _ = check_prefill(msa, wl, inp, rows=rows)
     print(f"prefill_s131072: {len(rows)} sampled rows, exact {exact}, near-tie {tie}, errs {errs}")
+
+
+def test_prefill_shared_index_keys(msa):
+    """One k_idx for all KV groups (group stride 0): scores, selection and
+    attention match the oracle on the broadcast tensor."""
+    wl = PrefillWorkload("shared_k_idx", B=2, S=1000, shape=MSAShape(Hq=12, Hkv=2, k=4), seed=64)
+    inp = prefill_inputs(wl, device="cuda")
+    inp["k_idx"] = inp["k_idx"][:, :, :1].expand(-1, -1, wl.shape.Hkv, -1)
+    assert inp["k_idx"].stride(2) == 0
+    exact, tie, errs, _ = check_prefill(msa, wl, inp)
+    print(f"shared k_idx: exact rows {exact}, near-tie rows {tie}, O max/mean {errs[0]:.2e}/{errs[1]:.2e}")
