@@ -28,6 +28,18 @@ Functions and the passages they follow (page title and passage):
 * ``cache_append`` -- the step before a decode step: the current token's K, V
   and index key written into the fixed-size pages (same paragraph; the token
   is in the cache before the step).  Plain numpy copies.
+* ``chunk_layer`` -- a chunk of S queries per sequence over a paged cache:
+  chunked prefill after a cached prefix ("MiniMax M3: MoE de 428B con 1M de
+  contexto en Blackwell", section "Como se sirve en inferencia open source?",
+  the serving command's 8,192-token prefill chunks; the serving post's
+  measurement paragraph, a 60,000-token cached prefix), and with a small S the
+  decode of several tokens per sequence (the M2-report article names
+  multi-token prediction for speculative decoding).  No new arithmetic: the
+  cached tokens are gathered out of the pages (``gather_pages``), the chunk's
+  queries are placed at their positions of the whole context
+  (``place_chunk``), and the prefill step functions above run on the chunk's
+  rows only -- a query at position p sees exactly what query p of a prefill of
+  the whole context sees.
 """
 from __future__ import annotations
 
@@ -269,3 +281,67 @@ def cache_append(K_new, V_new, kidx_new, K_pool, V_pool, kidx_pool, seq_pt, seq_
         V[page, :, t, :] = vn[b]
         X[page, :, t, :] = xn[b] if not shared_index else xn[b, 0]
     return K, V, X, skipped
+
+
+def gather_pages(pool, seq_pt, lengths, Bk: int):
+    """Dense [B, T, Hkv, X] copy (raw 16-bit patterns) of the first lengths[b]
+    tokens of every sequence b in a page pool [P, Hkv, Bk, X]: token t is slot
+    t % Bk of page seq_pt[b][t // Bk].  T = max length; zeros past a sequence's
+    end.  Data movement only."""
+    pool_, pt, L = _u16(pool), _i32(seq_pt), _i64(lengths)
+    B = pt.shape[0]
+    T = int(L.max()) if B else 0
+    out = np.zeros((B, T) + pool_.shape[1:2] + pool_.shape[3:], dtype=np.uint16)
+    for b in range(B):
+        t = np.arange(int(L[b]))
+        out[b, :len(t)] = pool_[pt[b, t // Bk], :, t % Bk]
+    return out
+
+
+def place_chunk(x, q_pos, T: int):
+    """The chunk tensor x [B, S, ...] copied to rows q_pos[b] .. q_pos[b] + S - 1
+    of a zero [B, T, ...] tensor (same dtype; raw copies)."""
+    a, qp = _np(x), _i64(q_pos)
+    B, S = a.shape[:2]
+    out = np.zeros((B, T) + a.shape[2:], dtype=a.dtype)
+    for b in range(B):
+        out[b, qp[b]:qp[b] + S] = a[b]
+    return out
+
+
+def chunk_rows(q_pos, S: int, T: int):
+    """Flattened context rows b*T + q_pos[b] + s of the chunk's queries, in
+    [B, S] order (index bookkeeping)."""
+    qp = _i64(q_pos)
+    return (np.arange(len(qp), dtype=np.int64)[:, None] * T + qp[:, None] + np.arange(S)[None, :]).reshape(-1)
+
+
+def chunk_layer(Q, q_idx, w, K_pool, V_pool, kidx_pool, seq_pt, q_pos, k: int, scale: float, Bk: int = 128):
+    """Index scores, selection and attention of a chunk of S queries per
+    sequence at positions q_pos[b] + s over a paged cache holding each
+    sequence's q_pos[b] + S tokens.
+
+    Q [B,S,Hq,D], q_idx [B,S,Hkv,HI,dI] (bf16), w [B,S,Hkv,HI] fp32, pools
+    [P,Hkv,Bk,*], seq_pt [B,max_pages], q_pos [B].  Returns a dict with C
+    [B,S,Hkv,nbT] (nbT = blocks of the longest context), sel [B,S,Hkv,k],
+    count [B,S,Hkv], c_last / c_next (as ``select``), O [B,S,Hq,D] and LSE
+    [B,S,Hq] (fp64).
+    """
+    qp = _i64(q_pos)
+    B, S = _np(Q).shape[:2]
+    lengths = qp + S
+    T = int(lengths.max())
+    Kd = gather_pages(K_pool, seq_pt, lengths, Bk)
+    Vd = gather_pages(V_pool, seq_pt, lengths, Bk)
+    Xd = gather_pages(kidx_pool, seq_pt, lengths, Bk)
+    Qd, QId, Wd = (place_chunk(_u16(Q), qp, T), place_chunk(_u16(q_idx), qp, T),
+                   place_chunk(_f32(w), qp, T))
+    rows = chunk_rows(qp, S, T)
+    Cs = prefill_scores(QId, Xd, Wd, Bk, rows)
+    own = np.repeat(own_blocks_prefill(T, Bk, rows), Cs.shape[1]).reshape(Cs.shape[:2])
+    sel, cnt, cl, cn = select(Cs, own, k)
+    O, LSE = prefill_attend(Qd, Kd, Vd, sel, cnt, Bk, scale, rows)
+    Hkv, nb = Cs.shape[1], Cs.shape[2]
+    return {"C": Cs.reshape(B, S, Hkv, nb), "sel": sel.reshape(B, S, Hkv, k), "count": cnt.reshape(B, S, Hkv),
+            "c_last": cl.reshape(B, S, Hkv), "c_next": cn.reshape(B, S, Hkv),
+            "O": O.reshape(B, S, -1, O.shape[-1]), "LSE": LSE.reshape(B, S, -1)}

@@ -12,7 +12,10 @@ off-by-one in causality or in the selection order) fails at least one test:
 * closed forms  -- one-hot index vectors give hand-derivable block scores;
                    one key gives O = V, LSE = z; equal keys give the mean of V.
 * cross-path    -- decode at length L equals prefill row L-1; page order and
-                   the flattened (B*Hkv) page table do not change the result.
+                   the flattened (B*Hkv) page table do not change the result;
+                   a chunk over paged caches equals the same rows of a prefill
+                   of the whole context, and a one-token chunk equals decode
+                   (whose C code reads the pages itself).
 """
 import math
 
@@ -21,7 +24,8 @@ import pytest
 import torch
 
 import oracle
-from workloads import DecodeWorkload, MSAShape, PrefillWorkload, decode_inputs, prefill_inputs, workload
+from workloads import (ChunkWorkload, DecodeWorkload, MSAShape, PrefillWorkload, chunk_inputs, decode_inputs,
+                       prefill_inputs, workload)
 
 
 def f64(t):
@@ -402,3 +406,69 @@ def test_cache_append_slots_by_hand():
     for page, t in expect.values():
         written[page, :, t] = True
     assert not K2[~written].any() and not V2[~written].any() and not X2[~written].any()
+
+
+def _paged(x, perm, Bk):
+    """[B, T, Hkv, X] -> page pool [B * ceil(T/Bk), Hkv, Bk, X] (zero tail) and
+    seq_pt [B, ceil(T/Bk)]: block j of sequence b goes to page perm[b*n + j]."""
+    B, T, Hkv, X = x.shape
+    n = (T + Bk - 1) // Bk
+    pad = torch.zeros(B, n * Bk, Hkv, X, dtype=x.dtype)
+    pad[:, :T] = x
+    blocks = pad.view(B, n, Bk, Hkv, X).permute(0, 1, 3, 2, 4).reshape(B * n, Hkv, Bk, X)
+    pool = torch.empty_like(blocks)
+    pool[perm] = blocks
+    return pool, perm.view(B, n).to(torch.int32)
+
+
+@pytest.mark.parametrize("q_pos,S", [((0, 0), 700), ((300, 451), 249), ((128, 64), 64), ((699, 500), 1)])
+def test_chunk_layer_equals_prefill_rows(q_pos, S):
+    """A chunk at positions q_pos[b] + s over shuffled pages gives, bit for bit,
+    the scores, selection and attention of those rows of a prefill of the
+    whole context (contiguous tensors, no pages)."""
+    sh = MSAShape(Hq=12, Hkv=2, HI=3, k=3)
+    wl = PrefillWorkload("pin_chunk", B=2, S=700, shape=sh, seed=91)
+    inp = prefill_inputs(wl)
+    T, Bk = wl.S, sh.Bk
+    perm = torch.randperm(2 * ((T + Bk - 1) // Bk), generator=torch.Generator().manual_seed(5))
+    K_pool, seq_pt = _paged(inp["K"], perm, Bk)
+    V_pool, _ = _paged(inp["V"], perm, Bk)
+    X_pool, _ = _paged(inp["k_idx"], perm, Bk)
+    qp = np.array(q_pos, dtype=np.int64)
+    idx = torch.as_tensor(qp[:, None] + np.arange(S)[None, :])
+    take = lambda t: torch.stack([t[b, idx[b]] for b in range(2)])
+    scale = 1 / math.sqrt(sh.D)
+    r = oracle.chunk_layer(take(inp["Q"]), take(inp["q_idx"]), take(inp["w"]), K_pool, V_pool, X_pool, seq_pt,
+                           torch.as_tensor(qp, dtype=torch.int32), sh.k, scale, Bk)
+    rows = (np.arange(2)[:, None] * T + idx.numpy()).reshape(-1)
+    Cp = oracle.prefill_scores(inp["q_idx"], inp["k_idx"], inp["w"], Bk, rows)
+    nbc = r["C"].shape[-1]
+    assert np.array_equal(r["C"].reshape(-1, sh.Hkv, nbc), Cp[:, :, :nbc])
+    assert np.all(Cp[:, :, nbc:] == -np.inf)
+    own = np.repeat(oracle.own_blocks_prefill(T, Bk, rows), sh.Hkv).reshape(-1, sh.Hkv)
+    sel, cnt, _, _ = oracle.select(Cp, own, sh.k)
+    assert np.array_equal(r["sel"].reshape(sel.shape), sel) and np.array_equal(r["count"].reshape(cnt.shape), cnt)
+    O, LSE = oracle.prefill_attend(inp["Q"], inp["K"], inp["V"], sel, cnt, Bk, scale, rows)
+    assert np.array_equal(r["O"].reshape(O.shape), O) and np.array_equal(r["LSE"].reshape(LSE.shape), LSE)
+
+
+def test_chunk_layer_single_token_equals_decode():
+    """A one-token chunk at position L_b - 1 is a decode step: the decode
+    oracle, which reads the pages itself, gives the same scores, selection and
+    attention."""
+    sh = MSAShape(Hq=12, Hkv=2, k=4)
+    wl = ChunkWorkload("pin_chunk_decode", prefix=(1000, 129, 4000), S=1, shape=sh, seed=92)
+    inp = chunk_inputs(wl)
+    scale = 1 / math.sqrt(sh.D)
+    r = oracle.chunk_layer(inp["Q"], inp["q_idx"], inp["w"], inp["K_pool"], inp["V_pool"], inp["kidx_pool"],
+                           inp["seq_pt"], inp["q_pos"], sh.k, scale, sh.Bk)
+    Cd = oracle.decode_scores(inp["q_idx"][:, 0], inp["w"][:, 0], inp["kidx_pool"], inp["seq_pt"], inp["seq_len"])
+    nbc = r["C"].shape[-1]
+    assert np.allclose(r["C"][:, 0], Cd[:, :, :nbc], rtol=1e-12, atol=0)
+    own = np.repeat(oracle.own_blocks_decode(inp["seq_len"], sh.Bk), sh.Hkv).reshape(wl.B, sh.Hkv)
+    sel, cnt, _, _ = oracle.select(Cd, own, sh.k)
+    assert np.array_equal(r["sel"][:, 0], sel) and np.array_equal(r["count"][:, 0], cnt)
+    O, LSE = oracle.decode_attend(inp["Q"][:, 0], inp["K_pool"], inp["V_pool"], inp["seq_pt"], inp["seq_len"],
+                                  sel, cnt, scale)
+    assert np.allclose(r["O"][:, 0], O, rtol=1e-12, atol=1e-15)
+    assert np.allclose(r["LSE"][:, 0], LSE, rtol=1e-12, atol=0)

@@ -17,6 +17,10 @@ Recipes (all seeded):
   position L_b - 1, is already in the cache) in ceil(L_b / Bk) pages of Bk
   tokens.  Physical page ids are a seeded random permutation of the pool, so
   pages are shuffled.  Ragged batches draw L_b = floor(exp(U(ln lo, ln hi))).
+* Chunk over a paged cache: sequence b has a cached prefix of q_pos[b] tokens
+  and a chunk of S new tokens at positions q_pos[b] .. q_pos[b] + S - 1, all
+  q_pos[b] + S tokens already in shuffled pages as in decode; the chunk's
+  queries are drawn like prefill queries.
 
 Big pools may be drawn directly on a CUDA device with a seeded CUDA generator;
 the oracle then reads host copies of exactly those tensors.  Values therefore
@@ -31,8 +35,8 @@ from typing import Dict, Optional, Sequence, Tuple
 import torch
 
 __all__ = [
-    "MSAShape", "PrefillWorkload", "DecodeWorkload", "WORKLOADS",
-    "prefill_inputs", "decode_inputs", "ragged_lengths", "workload",
+    "MSAShape", "PrefillWorkload", "DecodeWorkload", "ChunkWorkload", "WORKLOADS",
+    "prefill_inputs", "decode_inputs", "chunk_inputs", "ragged_lengths", "workload",
 ]
 
 
@@ -98,6 +102,38 @@ class DecodeWorkload:
         return sum(self.pages_per_seq)
 
 
+@dataclass(frozen=True)
+class ChunkWorkload:
+    """S new tokens per sequence after a cached prefix of prefix[b] tokens."""
+    name: str
+    prefix: Tuple[int, ...]      # q_pos[b]: position of the chunk's first token
+    S: int
+    shape: MSAShape
+    seed: int
+    shuffle_pages: bool = True
+
+    @property
+    def B(self) -> int:
+        return len(self.prefix)
+
+    @property
+    def lengths(self) -> Tuple[int, ...]:
+        return tuple(p + self.S for p in self.prefix)
+
+    @property
+    def pages_per_seq(self) -> Tuple[int, ...]:
+        Bk = self.shape.Bk
+        return tuple((L + Bk - 1) // Bk for L in self.lengths)
+
+    @property
+    def max_pages(self) -> int:
+        return max(self.pages_per_seq)
+
+    @property
+    def num_pages(self) -> int:
+        return sum(self.pages_per_seq)
+
+
 def ragged_lengths(B: int, lo: int, hi: int, seed: int) -> Tuple[int, ...]:
     """L_b = floor(exp(U(ln lo, ln hi))) for b < B, from a seeded CPU generator."""
     g = torch.Generator().manual_seed(seed)
@@ -126,6 +162,11 @@ WORKLOADS: Dict[str, object] = {
     # ragged decode batch of 64 sequences, lengths log-uniform in [4096, 524288]
     "decode_ragged_b64": DecodeWorkload("decode_ragged_b64", lengths=ragged_lengths(64, 4096, 524288, 4),
                                         shape=_SHAPE_MSA, seed=4),
+    # chunked prefill: an 8,192-token chunk after a 60,000-token cached prefix
+    "chunk_b1_p60000_s8192": ChunkWorkload("chunk_b1_p60000_s8192", prefix=(60000,), S=8192, shape=_SHAPE_MSA,
+                                           seed=5),
+    # decode of 4 tokens per sequence (draft verification) at concurrency 8 after 60,000 cached tokens
+    "verify_b8_p60000_s4": ChunkWorkload("verify_b8_p60000_s4", prefix=(60000,) * 8, S=4, shape=_SHAPE_MSA, seed=6),
 }
 
 
@@ -240,5 +281,40 @@ def decode_inputs(wl: DecodeWorkload, device="cpu", pool_pages: Optional[int] = 
         seq_pt[b, :n] = perm[off:off + n].to(torch.int32)
         off += n
     out["seq_pt"] = seq_pt.to(device)
+    out["seq_len"] = torch.tensor(wl.lengths, dtype=torch.int32).to(device)
+    return out
+
+
+def chunk_inputs(wl: ChunkWorkload, device="cpu", pool_pages: Optional[int] = None) -> Dict[str, torch.Tensor]:
+    """Tensors of one chunk over a paged cache.
+
+    Q [B,S,Hq,D], q_idx [B,S,Hkv,HI,dI] (bf16) and w [B,S,Hkv,HI] fp32 for the
+    chunk's queries; page pools K_pool, V_pool [P,Hkv,Bk,D], kidx_pool
+    [P,Hkv,Bk,dI] (bf16) holding every sequence's q_pos[b] + S tokens (the
+    chunk's own keys included); seq_pt [B,max_pages] int32 (-1 past the end),
+    q_pos [B] int32 and seq_len = q_pos + S [B] int32.
+    """
+    device = torch.device(device)
+    sh = wl.shape
+    P = wl.num_pages if pool_pages is None else pool_pages
+    assert P >= wl.num_pages
+    g = _gen(device, wl.seed)
+    out = {
+        "Q": _randn_bf16((wl.B, wl.S, sh.Hq, sh.D), g, 1.0 / math.sqrt(sh.D), device),
+        "q_idx": _randn_bf16((wl.B, wl.S, sh.Hkv, sh.HI, sh.dI), g, 1.0 / math.sqrt(sh.dI), device),
+        "w": _rand_f32((wl.B, wl.S, sh.Hkv, sh.HI), g, device),
+        "kidx_pool": _randn_bf16((P, sh.Hkv, sh.Bk, sh.dI), g, 1.0 / math.sqrt(sh.dI), device),
+        "K_pool": _randn_bf16((P, sh.Hkv, sh.Bk, sh.D), g, 1.0 / math.sqrt(sh.D), device),
+        "V_pool": _randn_bf16((P, sh.Hkv, sh.Bk, sh.D), g, 1.0 / math.sqrt(sh.D), device),
+    }
+    cg = torch.Generator().manual_seed(wl.seed + 1000)
+    perm = torch.randperm(P, generator=cg) if wl.shuffle_pages else torch.arange(P)
+    seq_pt = torch.full((wl.B, wl.max_pages), -1, dtype=torch.int32)
+    off = 0
+    for b, n in enumerate(wl.pages_per_seq):
+        seq_pt[b, :n] = perm[off:off + n].to(torch.int32)
+        off += n
+    out["seq_pt"] = seq_pt.to(device)
+    out["q_pos"] = torch.tensor(wl.prefix, dtype=torch.int32).to(device)
     out["seq_len"] = torch.tensor(wl.lengths, dtype=torch.int32).to(device)
     return out
