@@ -6,9 +6,9 @@ entry point of the same name, and raises ``MSAError`` on a non-OK status.  All
 computation runs in the library's sm_103a kernels; there is no fallback path.
 PyTorch provides device memory and streams only.
 
-The two pipelines at the bottom (``decode_step`` and ``prefill_layer``) call
-the entry points in hot-path order: index score -> top-k -> (decode: page
-table) -> sparse attention (with its log-sum-exp merge).
+The pipelines at the bottom (``decode_step``, ``prefill_layer`` and
+``chunk_layer``) call the entry points in hot-path order: index score -> top-k
+-> (decode: page table) -> sparse attention (with its log-sum-exp merge).
 """
 from __future__ import annotations
 
@@ -19,14 +19,14 @@ import torch
 
 from . import _abi
 from ._abi import (MSA_DEVERR_BAD_LEN, MSA_DEVERR_BAD_PAGE, MSA_DEVERR_BAD_SEL, MSA_DEVERR_TIMEOUT,
-                   MSA_MODE_DECODE, MSA_MODE_PREFILL, MSAError)
+                   MSA_MODE_CHUNK, MSA_MODE_DECODE, MSA_MODE_PREFILL, MSAError)
 
 __all__ = [
     "msa_index_score", "msa_topk_blocks", "msa_build_page_table", "msa_sparse_attn_prefill",
     "msa_sparse_attn_decode", "msa_sparse_attn_decode_noalloc", "msa_lse_merge", "msa_sparse_attn_prefill_workspace_size",
-    "msa_sparse_attn_decode_workspace_size", "msa_cache_append", "decode_step", "prefill_layer", "lib",
-    "MSAError",
-    "MSA_MODE_PREFILL", "MSA_MODE_DECODE", "MSA_DEVERR_TIMEOUT", "MSA_DEVERR_BAD_PAGE",
+    "msa_sparse_attn_decode_workspace_size", "msa_cache_append", "decode_step", "prefill_layer", "chunk_layer",
+    "lib", "MSAError",
+    "MSA_MODE_PREFILL", "MSA_MODE_DECODE", "MSA_MODE_CHUNK", "MSA_DEVERR_TIMEOUT", "MSA_DEVERR_BAD_PAGE",
     "MSA_DEVERR_BAD_SEL", "MSA_DEVERR_BAD_LEN", "Bk", "D", "dI",
 ]
 
@@ -71,10 +71,12 @@ def msa_index_score(mode: int, q_idx: torch.Tensor, w: torch.Tensor, k_idx: torc
                     sel: Optional[torch.Tensor] = None, count: Optional[torch.Tensor] = None,
                     pt: Optional[torch.Tensor] = None, n: Optional[torch.Tensor] = None,
                     last_len: Optional[torch.Tensor] = None, row_scratch: Optional[torch.Tensor] = None,
-                    scratch_zeroed: bool = False) -> None:
+                    scratch_zeroed: bool = False, q_pos: Optional[torch.Tensor] = None) -> None:
     """Block scores of the Index Branch into ``C_out`` (see msa.h, a1).
 
     PREFILL: q_idx [B,S,Hkv,HI,dI], w [B,S,Hkv,HI], k_idx [B,S,Hkv,dI], C_out [B,S,Hkv,nb_stride].
+    CHUNK:   q_idx, w, C_out as PREFILL; k_idx pool [P,Hkv,Bk,dI], seq_pt [B,max_pages] int32,
+             q_pos [B] int32 (position of each sequence's first chunk query).
     DECODE:  q_idx [B,Hkv,HI,dI], w [B,Hkv,HI], k_idx pool [P,Hkv,Bk,dI], C_out [B,Hkv,nb_stride],
              seq_pt [B,max_pages] int32 (contiguous rows), seq_len [B] int32.
     DECODE with ``sel`` given: the same call also selects (a2) into sel/count and,
@@ -89,13 +91,17 @@ def msa_index_score(mode: int, q_idx: torch.Tensor, w: torch.Tensor, k_idx: torc
     a.q_idx, a.w, a.k_idx, a.C = _ptr(q_idx), _ptr(w), _ptr(k_idx), _ptr(C_out)
     a.dev_err = _ptr(dev_err)
     a.nb_stride = C_out.shape[-1]
-    if mode == MSA_MODE_PREFILL:
+    if mode in (MSA_MODE_PREFILL, MSA_MODE_CHUNK):
         B, S, Hkv, HI, di = q_idx.shape
         a.B, a.S, a.Hkv, a.HI, a.dI, a.Bk = B, S, Hkv, HI, di, Bk
         a.q_idx_stride[:] = _strides(q_idx, 4)
         a.w_stride[:] = _strides(w, 3)
         a.k_idx_stride[:] = _strides(k_idx, 3)
         a.C_stride[:] = _strides(C_out, 3)
+        if mode == MSA_MODE_CHUNK:
+            if not (seq_pt.is_contiguous() and q_pos.is_contiguous()):
+                raise ValueError("seq_pt and q_pos must be contiguous")
+            a.num_pages, a.seq_pt, a.max_pages, a.q_pos = k_idx.shape[0], _ptr(seq_pt), seq_pt.shape[1], _ptr(q_pos)
     else:
         B, Hkv, HI, di = q_idx.shape
         a.B, a.S, a.Hkv, a.HI, a.dI, a.Bk = B, 0, Hkv, HI, di, k_idx.shape[2]
@@ -124,10 +130,11 @@ def msa_index_score(mode: int, q_idx: torch.Tensor, w: torch.Tensor, k_idx: torc
 
 def msa_topk_blocks(mode: int, C_in: torch.Tensor, k: int, sel: torch.Tensor, count: torch.Tensor, *,
                     seq_len: Optional[torch.Tensor] = None, dev_err: Optional[torch.Tensor] = None,
-                    stream=None) -> None:
+                    stream=None, q_pos: Optional[torch.Tensor] = None) -> None:
     """Own block + top-(k-1) earlier blocks per row (see msa.h, a2).
 
     PREFILL: C_in [B,S,Hkv,nb], sel [B,S,Hkv,k], count [B,S,Hkv].
+    CHUNK:   as PREFILL, own block (q_pos[b] + s) // Bk.
     DECODE:  C_in [B,Hkv,nb], seq_len [B], sel [B,Hkv,k], count [B,Hkv].
     """
     _inner_contig(C_in, "C")
@@ -137,9 +144,11 @@ def msa_topk_blocks(mode: int, C_in: torch.Tensor, k: int, sel: torch.Tensor, co
     a.mode, a.k, a.Bk = mode, k, Bk
     a.C, a.sel, a.count, a.dev_err = _ptr(C_in), _ptr(sel), _ptr(count), _ptr(dev_err)
     a.nb_stride = C_in.shape[-1]
-    if mode == MSA_MODE_PREFILL:
+    if mode in (MSA_MODE_PREFILL, MSA_MODE_CHUNK):
         a.B, a.S, a.Hkv = C_in.shape[0], C_in.shape[1], C_in.shape[2]
         a.C_stride[:] = _strides(C_in, 3)
+        if mode == MSA_MODE_CHUNK:
+            a.q_pos = _ptr(q_pos)
     else:
         a.B, a.S, a.Hkv = C_in.shape[0], 0, C_in.shape[1]
         a.C_stride[:] = _strides(C_in, 2) + [0]
@@ -171,12 +180,20 @@ def msa_build_page_table(sel: torch.Tensor, count: torch.Tensor, seq_pt: torch.T
 # a4/a5 sparse attention and a6 merge
 # ---------------------------------------------------------------------------
 
-def _prefill_args(Q, K, V, sel, count, O, LSE, softmax_scale, dev_err) -> _abi.PrefillArgs:
+def _prefill_args(Q, K, V, sel, count, O, LSE, softmax_scale, dev_err, seq_pt=None, q_pos=None
+                  ) -> _abi.PrefillArgs:
+    """PREFILL: K, V [B,S,Hkv,D].  CHUNK (seq_pt and q_pos given): K, V page pools [P,Hkv,Bk,D]."""
     for t, nm in ((Q, "Q"), (K, "K"), (V, "V")):
         _inner_contig(t, nm)
     a = _abi.PrefillArgs()
     a.B, a.S, a.Hq, a.D = Q.shape
     a.Hkv = K.shape[2]
+    if seq_pt is not None:
+        if not (seq_pt.is_contiguous() and q_pos.is_contiguous()):
+            raise ValueError("seq_pt and q_pos must be contiguous")
+        a.mode = MSA_MODE_CHUNK
+        a.Hkv = K.shape[1]
+        a.seq_pt, a.max_pages, a.num_pages, a.q_pos = _ptr(seq_pt), seq_pt.shape[1], K.shape[0], _ptr(q_pos)
     a.Bk = Bk
     a.k = sel.shape[-1]
     a.softmax_scale = softmax_scale
@@ -189,19 +206,27 @@ def _prefill_args(Q, K, V, sel, count, O, LSE, softmax_scale, dev_err) -> _abi.P
     return a
 
 
-def msa_sparse_attn_prefill_workspace_size(Q, K, sel, chunk_queries: int) -> int:
+def msa_sparse_attn_prefill_workspace_size(Q, K, sel, chunk_queries: int, max_pages: Optional[int] = None) -> int:
+    """Workspace bytes for chunks of ``chunk_queries`` queries; ``max_pages`` (the
+    page-table width) selects CHUNK mode, where K is a page pool [P,Hkv,Bk,D]."""
     a = _abi.PrefillArgs()
     a.B, a.S, a.Hq, a.D = Q.shape
     a.Hkv, a.Bk, a.k = K.shape[2], Bk, sel.shape[-1]
+    if max_pages is not None:
+        a.mode, a.Hkv, a.max_pages = MSA_MODE_CHUNK, K.shape[1], int(max_pages)
     return int(lib().msa_sparse_attn_prefill_workspace_size(C.byref(a), int(chunk_queries)))
 
 
 def msa_sparse_attn_prefill(Q, K, V, sel, count, O, LSE, ws: torch.Tensor, *, softmax_scale: float = 0.0,
-                            dev_err=None, stream=None) -> None:
-    """KV-block-major causal sparse attention (see msa.h, a3'-a4-a6)."""
+                            dev_err=None, stream=None, seq_pt: Optional[torch.Tensor] = None,
+                            q_pos: Optional[torch.Tensor] = None) -> None:
+    """KV-block-major causal sparse attention (see msa.h, a3'-a4-a6).
+
+    With ``seq_pt`` and ``q_pos`` (CHUNK mode) Q is a chunk of queries at
+    positions q_pos[b] + s and K, V are page pools [P,Hkv,Bk,D] indexed by seq_pt."""
     if not (sel.is_contiguous() and count.is_contiguous() and O.is_contiguous()):
         raise ValueError("sel, count and O must be contiguous")
-    a = _prefill_args(Q, K, V, sel, count, O, LSE, softmax_scale, dev_err)
+    a = _prefill_args(Q, K, V, sel, count, O, LSE, softmax_scale, dev_err, seq_pt, q_pos)
     _abi.check(lib().msa_sparse_attn_prefill(C.byref(a), _ptr(ws), ws.numel() * ws.element_size(),
                                              _stream(stream)), "msa_sparse_attn_prefill")
 
@@ -397,4 +422,44 @@ def prefill_layer(inp: Dict[str, torch.Tensor], k: int, bufs: Optional[Dict[str,
     msa_topk_blocks(MSA_MODE_PREFILL, bufs["C"], k, bufs["sel"], bufs["count"], dev_err=e, stream=stream)
     msa_sparse_attn_prefill(inp["Q"], inp["K"], inp["V"], bufs["sel"], bufs["count"], bufs["O"], bufs["LSE"],
                             bufs["ws"], softmax_scale=softmax_scale, dev_err=e, stream=stream)
+    return bufs
+
+
+def chunk_buffers(B: int, S: int, Hq: int, Hkv: int, k: int, nb: int, device, ws_bytes: int
+                  ) -> Dict[str, torch.Tensor]:
+    """Outputs and scratch of ``chunk_layer`` (score rows of ``nb`` blocks)."""
+    bufs = prefill_buffers(B, S, Hq, Hkv, k, device, ws_bytes)
+    bufs["C"] = torch.empty(B, S, Hkv, nb, dtype=torch.float32, device=torch.device(device))
+    return bufs
+
+
+def chunk_layer(inp: Dict[str, torch.Tensor], k: int, bufs: Optional[Dict[str, torch.Tensor]] = None,
+                ws_bytes: Optional[int] = None, softmax_scale: float = 0.0, stream=None
+                ) -> Dict[str, torch.Tensor]:
+    """One MSA layer over a chunk of S queries per sequence on a paged cache
+    (chunked prefill over a cached prefix, or several decode tokens per
+    sequence): a1 index score -> a2 top-k -> a3'/a4/a6 KV-block-major attention.
+
+    ``inp`` holds Q [B,S,Hq,D], q_idx [B,S,Hkv,HI,dI], w [B,S,Hkv,HI], the page
+    pools K_pool, V_pool [P,Hkv,Bk,D] and kidx_pool [P,Hkv,Bk,dI], seq_pt
+    [B,max_pages] and q_pos [B] int32 (the chunk's own tokens already in the
+    pages).  Score rows span max_pages blocks unless ``bufs`` says otherwise.
+    """
+    B, S, Hq, _ = inp["Q"].shape
+    Hkv = inp["K_pool"].shape[1]
+    max_pages = inp["seq_pt"].shape[1]
+    if bufs is None:
+        if ws_bytes is None:
+            sel_probe = torch.empty(1, 1, 1, k, dtype=torch.int32)
+            ws_bytes = msa_sparse_attn_prefill_workspace_size(inp["Q"], inp["K_pool"], sel_probe,
+                                                              min(S, 8192) * B, max_pages=max_pages)
+        bufs = chunk_buffers(B, S, Hq, Hkv, k, max_pages, inp["Q"].device, ws_bytes)
+    e = bufs["dev_err"]
+    msa_index_score(MSA_MODE_CHUNK, inp["q_idx"], inp["w"], inp["kidx_pool"], bufs["C"], seq_pt=inp["seq_pt"],
+                    q_pos=inp["q_pos"], dev_err=e, stream=stream)
+    msa_topk_blocks(MSA_MODE_CHUNK, bufs["C"], k, bufs["sel"], bufs["count"], q_pos=inp["q_pos"], dev_err=e,
+                    stream=stream)
+    msa_sparse_attn_prefill(inp["Q"], inp["K_pool"], inp["V_pool"], bufs["sel"], bufs["count"], bufs["O"],
+                            bufs["LSE"], bufs["ws"], softmax_scale=softmax_scale, dev_err=e, stream=stream,
+                            seq_pt=inp["seq_pt"], q_pos=inp["q_pos"])
     return bufs

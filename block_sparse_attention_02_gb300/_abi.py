@@ -27,6 +27,7 @@ MSA_DEVERR_BAD_LEN = 0x8
 
 MSA_MODE_PREFILL = 0
 MSA_MODE_DECODE = 1
+MSA_MODE_CHUNK = 2
 
 _p = C.c_void_p
 _i64x2 = C.c_int64 * 2
@@ -46,6 +47,7 @@ class IndexArgs(C.Structure):
         ("dev_err", _p),
         ("k", C.c_int), ("sel", _p), ("count", _p), ("pt", _p), ("n", _p), ("last_len", _p),
         ("row_scratch", _p), ("scratch_zeroed", C.c_int),
+        ("q_pos", _p),
     ]
 
 
@@ -54,6 +56,7 @@ class TopkArgs(C.Structure):
         ("mode", C.c_int), ("B", C.c_int), ("S", C.c_int), ("Hkv", C.c_int), ("Bk", C.c_int), ("k", C.c_int),
         ("C", _p), ("C_stride", _i64x3), ("nb_stride", C.c_int),
         ("seq_len", _p), ("sel", _p), ("count", _p), ("dev_err", _p),
+        ("q_pos", _p),
     ]
 
 
@@ -63,6 +66,7 @@ class PrefillArgs(C.Structure):
         ("k", C.c_int), ("softmax_scale", C.c_float),
         ("Q", _p), ("Q_stride", _i64x3), ("K", _p), ("K_stride", _i64x3), ("V", _p), ("V_stride", _i64x3),
         ("sel", _p), ("count", _p), ("O", _p), ("LSE", _p), ("dev_err", _p),
+        ("mode", C.c_int), ("seq_pt", _p), ("max_pages", C.c_int64), ("num_pages", C.c_int64), ("q_pos", _p),
     ]
 
 

@@ -168,8 +168,8 @@ const char* msa_status_string(msa_status s) {
 msa_status msa_index_score(const msa_index_args* a, msa_stream_t stream) {
   g_last_error.clear();
   MSA_REQUIRE(a != nullptr, MSA_ERR_INVALID_ARG, "args is NULL");
-  MSA_REQUIRE(a->mode == MSA_MODE_PREFILL || a->mode == MSA_MODE_DECODE, MSA_ERR_INVALID_ARG, "bad mode %d",
-              static_cast<int>(a->mode));
+  MSA_REQUIRE(a->mode == MSA_MODE_PREFILL || a->mode == MSA_MODE_DECODE || a->mode == MSA_MODE_CHUNK,
+              MSA_ERR_INVALID_ARG, "bad mode %d", static_cast<int>(a->mode));
   MSA_REQUIRE(a->B >= 0 && a->Hkv >= 1, MSA_ERR_INVALID_ARG, "B = %d, Hkv = %d", a->B, a->Hkv);
   if (msa_status st = check_common_shape(a->Bk, a->dI, kDI, "dI"); st != MSA_OK) return st;
   MSA_REQUIRE(a->HI >= 1 && a->HI <= kMaxHI, MSA_ERR_UNSUPPORTED, "HI = %d, supported 1..%d", a->HI, kMaxHI);
@@ -177,16 +177,27 @@ msa_status msa_index_score(const msa_index_args* a, msa_stream_t stream) {
   MSA_REQUIRE(a->q_idx && a->w && a->k_idx && a->C, MSA_ERR_INVALID_ARG, "q_idx, w, k_idx and C must be non-NULL");
   MSA_REQUIRE(aligned16(a->q_idx) && aligned16(a->k_idx), MSA_ERR_INVALID_ARG,
               "q_idx and k_idx must be 16-byte aligned");
-  if (a->mode == MSA_MODE_PREFILL) {
+  if (a->mode == MSA_MODE_PREFILL || a->mode == MSA_MODE_CHUNK) {
+    const bool chunk = a->mode == MSA_MODE_CHUNK;
     MSA_REQUIRE(a->S >= 0, MSA_ERR_INVALID_ARG, "S = %d", a->S);
     MSA_REQUIRE(a->nb_stride >= (a->S + a->Bk - 1) / a->Bk, MSA_ERR_INVALID_ARG, "nb_stride %d < ceil(S/Bk) = %d",
                 a->nb_stride, (a->S + a->Bk - 1) / a->Bk);
     for (int i = 0; i < 4; ++i)
       MSA_REQUIRE(vec_stride_ok(a->q_idx_stride[i], 2), MSA_ERR_INVALID_ARG,
                   "q_idx_stride[%d] = %" PRId64 " must be a positive multiple of 8 elements", i, a->q_idx_stride[i]);
-    for (int i = 0; i < 3; ++i)   // strides (b, s, g); a group stride of 0: one k_idx for all KV groups
-      MSA_REQUIRE(vec_stride_ok(a->k_idx_stride[i], 2) || (i == 2 && a->k_idx_stride[i] == 0), MSA_ERR_INVALID_ARG,
+    // strides (b, s, g), or (page, g, t) for a chunk's page pool; a group
+    // stride of 0: one index-key tensor for all KV groups
+    const int gi = chunk ? 1 : 2;
+    for (int i = 0; i < 3; ++i)
+      MSA_REQUIRE(vec_stride_ok(a->k_idx_stride[i], 2) || (i == gi && a->k_idx_stride[i] == 0), MSA_ERR_INVALID_ARG,
                   "k_idx_stride[%d] = %" PRId64 " must be a positive multiple of 8 elements", i, a->k_idx_stride[i]);
+    if (chunk) {
+      MSA_REQUIRE(a->seq_pt && a->q_pos, MSA_ERR_INVALID_ARG, "chunk: seq_pt and q_pos must be non-NULL");
+      MSA_REQUIRE(a->num_pages >= 1 && a->num_pages < (int64_t(1) << 31), MSA_ERR_INVALID_ARG,
+                  "num_pages = %" PRId64, a->num_pages);
+      MSA_REQUIRE(a->max_pages >= 1 && a->max_pages < (int64_t(1) << 31) / a->Bk, MSA_ERR_INVALID_ARG,
+                  "max_pages = %" PRId64, a->max_pages);
+    }
     for (int i = 0; i < 3; ++i)
       MSA_REQUIRE(a->w_stride[i] > 0 && a->C_stride[i] > 0, MSA_ERR_INVALID_ARG, "w / C strides must be positive");
     if (static_cast<int64_t>(a->B) * a->S == 0) return MSA_OK;
@@ -224,7 +235,8 @@ msa_status msa_index_score(const msa_index_args* a, msa_stream_t stream) {
 msa_status msa_topk_blocks(const msa_topk_args* a, msa_stream_t stream) {
   g_last_error.clear();
   MSA_REQUIRE(a != nullptr, MSA_ERR_INVALID_ARG, "args is NULL");
-  MSA_REQUIRE(a->mode == MSA_MODE_PREFILL || a->mode == MSA_MODE_DECODE, MSA_ERR_INVALID_ARG, "bad mode");
+  MSA_REQUIRE(a->mode == MSA_MODE_PREFILL || a->mode == MSA_MODE_DECODE || a->mode == MSA_MODE_CHUNK,
+              MSA_ERR_INVALID_ARG, "bad mode");
   MSA_REQUIRE(a->Bk == kBk, MSA_ERR_UNSUPPORTED, "Bk = %d, only %d is supported", a->Bk, kBk);
   MSA_REQUIRE(a->k >= 1 && a->k <= kMaxK, MSA_ERR_UNSUPPORTED, "k = %d, supported 1..%d", a->k, kMaxK);
   MSA_REQUIRE(a->B >= 0 && a->Hkv >= 1 && a->nb_stride >= 1, MSA_ERR_INVALID_ARG, "B = %d, Hkv = %d, nb_stride = %d",
@@ -236,6 +248,10 @@ msa_status msa_topk_blocks(const msa_topk_args* a, msa_stream_t stream) {
     MSA_REQUIRE(a->C_stride[2] > 0, MSA_ERR_INVALID_ARG, "C strides must be positive");
     MSA_REQUIRE(a->nb_stride >= (a->S + a->Bk - 1) / a->Bk, MSA_ERR_INVALID_ARG, "nb_stride < ceil(S/Bk)");
     MSA_REQUIRE((a->S - 1) / a->Bk < 2048, MSA_ERR_UNSUPPORTED, "prefill rows with more than 2048 blocks");
+  } else if (a->mode == MSA_MODE_CHUNK) {
+    MSA_REQUIRE(a->S >= 0, MSA_ERR_INVALID_ARG, "S = %d", a->S);
+    MSA_REQUIRE(a->C_stride[2] > 0, MSA_ERR_INVALID_ARG, "C strides must be positive");
+    MSA_REQUIRE(a->q_pos != nullptr, MSA_ERR_INVALID_ARG, "q_pos must be non-NULL in chunk mode");
   } else {
     MSA_REQUIRE(a->seq_len != nullptr, MSA_ERR_INVALID_ARG, "seq_len must be non-NULL in decode");
   }
@@ -283,6 +299,16 @@ msa_status msa_sparse_attn_decode(const msa_decode_args* a, void* ws, size_t ws_
 // ---------------------------------------------------------------------------
 static msa_status check_prefill(const msa_prefill_args* a) {
   MSA_REQUIRE(a != nullptr, MSA_ERR_INVALID_ARG, "args is NULL");
+  MSA_REQUIRE(a->mode == MSA_MODE_PREFILL || a->mode == MSA_MODE_CHUNK, MSA_ERR_INVALID_ARG,
+              "mode %d: prefill attention takes PREFILL or CHUNK", static_cast<int>(a->mode));
+  if (a->mode == MSA_MODE_CHUNK) {
+    MSA_REQUIRE(a->seq_pt && a->q_pos, MSA_ERR_INVALID_ARG, "chunk: seq_pt and q_pos must be non-NULL");
+    // the page id travels in the tile descriptor above two flag bits
+    MSA_REQUIRE(a->num_pages >= 1 && a->num_pages <= (int64_t(1) << 29), MSA_ERR_INVALID_ARG,
+                "num_pages = %" PRId64 ", supported 1..2^29", a->num_pages);
+    MSA_REQUIRE(a->max_pages >= 1 && a->max_pages < (int64_t(1) << 31) / kBk, MSA_ERR_INVALID_ARG,
+                "max_pages = %" PRId64, a->max_pages);
+  }
   MSA_REQUIRE(a->B >= 0 && a->S >= 0 && a->Hkv >= 1 && a->Hq >= 1, MSA_ERR_INVALID_ARG,
               "B = %d, S = %d, Hq = %d, Hkv = %d", a->B, a->S, a->Hq, a->Hkv);
   MSA_REQUIRE(a->Hq % a->Hkv == 0 && a->Hq / a->Hkv <= kMaxG, MSA_ERR_UNSUPPORTED,
@@ -305,6 +331,7 @@ static msa_status check_prefill(const msa_prefill_args* a) {
 
 size_t msa_sparse_attn_prefill_workspace_size(const msa_prefill_args* a, int64_t chunk_queries) {
   if (a == nullptr || chunk_queries < 1) return 0;
+  if (a->mode == MSA_MODE_CHUNK && a->max_pages < 1) return 0;
   return attn_prefill_workspace_size(*a, chunk_queries);
 }
 

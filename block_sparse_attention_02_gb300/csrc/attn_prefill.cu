@@ -28,6 +28,10 @@
 //   5. merge    per (query, head): the log-sum-exp merge of its k partials,
 //               found through the slot map.
 // Keys of block j seen by query i are t in [j*Bk, (j+1)*Bk) with t <= i.
+// A chunk over a paged cache (MSA_MODE_CHUNK) differs only in where things
+// are: query i of sequence b sits at position q_pos[b] + i (the causal limit),
+// and block j of sequence b is page seq_pt[b][j] of the K/V pools (carried in
+// the tile descriptor, so the producer needs no extra load).
 #include <algorithm>
 
 #include "msa_internal.h"
@@ -52,9 +56,14 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 constexpr int kTileFirst = 1;         // tile_info.w: first tile of its item
 constexpr int kTileLast = 2;          //              last tile of its item
+constexpr int kTilePageShift = 2;     //              page id of the block (chunk) above the flags
 
 struct CsrParams {
   int S, Hkv, Hq, G, k, nb;
+  int chunk;            // 1: queries at q_pos[b] + i, blocks are pages seq_pt[b][j]
+  const int32_t* q_pos;
+  const int32_t* seq_pt;
+  int64_t max_pages, num_pages;
   int64_t q0;           // first flattened query (b*S + i) of the chunk
   int nq;               // queries in the chunk
   const int32_t* sel;
@@ -79,6 +88,7 @@ struct CsrEntry {
   int64_t e;     // index into where[nq, Hkv, k]
   int64_t item;  // (b, g, j) item of the selected block, -1 if the slot is empty
   int64_t bs;    // flattened query b*S + i
+  int page;      // chunk: page of the block
 };
 __device__ __forceinline__ CsrEntry csr_entry(const CsrParams& p, int64_t t, bool report_bad) {
   const int qi = static_cast<int>(t % p.nq);
@@ -88,11 +98,21 @@ __device__ __forceinline__ CsrEntry csr_entry(const CsrParams& p, int64_t t, boo
   x.e = (static_cast<int64_t>(qi) * p.Hkv + g) * p.k + s;
   x.bs = p.q0 + qi;
   x.item = -1;
+  x.page = 0;
   const int b = static_cast<int>(x.bs / p.S), i = static_cast<int>(x.bs % p.S);
   if (s < p.count[x.bs * p.Hkv + g]) {
     const int j = p.sel[(x.bs * p.Hkv + g) * p.k + s];
-    if (j < 0 || j > i / kBk) {
+    const int64_t pos = p.chunk ? static_cast<int64_t>(p.q_pos[b]) + i : i;
+    if (j < 0 || pos < 0 || j > pos / kBk || j >= p.nb) {
       if (report_bad) report(p.dev_err, MSA_DEVERR_BAD_SEL);
+    } else if (p.chunk) {
+      const int page = p.seq_pt[b * p.max_pages + j];
+      if (page < 0 || page >= p.num_pages) {
+        if (report_bad) report(p.dev_err, MSA_DEVERR_BAD_PAGE);
+      } else {
+        x.item = (static_cast<int64_t>(b) * p.Hkv + g) * p.nb + j;
+        x.page = page;
+      }
     } else {
       x.item = (static_cast<int64_t>(b) * p.Hkv + g) * p.nb + j;
     }
@@ -108,7 +128,7 @@ __global__ void csr_count_kernel(const CsrParams p) {
   for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31); base < total;
        base += stride) {
     const int64_t t = base + lane;
-    CsrEntry x{0, -1, 0};
+    CsrEntry x{0, -1, 0, 0};
     if (t < total) x = csr_entry(p, t, true);
     const unsigned grp = __match_any_sync(0xffffffffu, static_cast<int>(x.item));
     if (x.item >= 0 && lane == __ffs(grp) - 1) atomicAdd(&p.cnt[x.item], __popc(grp));
@@ -186,7 +206,7 @@ __global__ void csr_fill_kernel(const CsrParams p) {
   for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31); base < total;
        base += stride) {
     const int64_t t = base + lane;
-    CsrEntry x{0, -1, 0};
+    CsrEntry x{0, -1, 0, 0};
     if (t < total) x = csr_entry(p, t, false);
     const unsigned grp = __match_any_sync(0xffffffffu, static_cast<int>(x.item));
     if (x.item >= 0) {   // no early exit: every lane reaches the next iteration's match together
@@ -202,7 +222,7 @@ __global__ void csr_fill_kernel(const CsrParams p) {
       p.where[x.e] = es * 8;                                              // tile row of head 0
       if (idx % kEntries == 0) {
         const int c = p.off[item + 1] - p.off[item], u = idx / kEntries, nt = tiles_of(c);
-        const int flags = (u == 0 ? kTileFirst : 0) | (u == nt - 1 ? kTileLast : 0);
+        const int flags = (u == 0 ? kTileFirst : 0) | (u == nt - 1 ? kTileLast : 0) | (x.page << kTilePageShift);
         p.tile_info[es / kEntries] = make_int4(static_cast<int>(item), min(kEntries, c - idx), p.ord[item], flags);
       }
     }
@@ -216,6 +236,8 @@ __global__ void csr_fill_kernel(const CsrParams p) {
 
 struct AttnParams {
   int S, Hkv, G, nb;
+  int chunk;                 // 1: K/V are page pools, queries at q_pos[b] + i
+  const int32_t* q_pos;
   int64_t n_items;
   float scale_log2;
   const int32_t* tile_off;   // tile_off[n_items] = number of tiles
@@ -359,11 +381,14 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
             ok = mbar_wait(&bar_kvempty[kvb], ((rel >> 1) & 1) ^ 1, abort_flag, p.dev_err);
             if (ok) {
               uint8_t* kvbuf = s_kv + kvb * kKV;
+              // contiguous K/V: (d, g, token, b); page pools: (d, token, g, page)
+              const int x1 = p.chunk ? 0 : g, x2 = p.chunk ? g : j * kBk;
+              const int x3 = p.chunk ? (ti.w >> kTilePageShift) : b;
               mbar_arrive_expect_tx(&bar_kvfull[kvb], kKV);
-              tma_load_4d(kvbuf + 0 * kHalf, &kmap, &bar_kvfull[kvb], 0, g, j * kBk, b);
-              tma_load_4d(kvbuf + 1 * kHalf, &kmap, &bar_kvfull[kvb], 64, g, j * kBk, b);
-              tma_load_4d(kvbuf + 2 * kHalf, &vmap, &bar_kvfull[kvb], 0, g, j * kBk, b);
-              tma_load_4d(kvbuf + 3 * kHalf, &vmap, &bar_kvfull[kvb], 64, g, j * kBk, b);
+              tma_load_4d(kvbuf + 0 * kHalf, &kmap, &bar_kvfull[kvb], 0, x1, x2, x3);
+              tma_load_4d(kvbuf + 1 * kHalf, &kmap, &bar_kvfull[kvb], 64, x1, x2, x3);
+              tma_load_4d(kvbuf + 2 * kHalf, &vmap, &bar_kvfull[kvb], 0, x1, x2, x3);
+              tma_load_4d(kvbuf + 3 * kHalf, &vmap, &bar_kvfull[kvb], 64, x1, x2, x3);
               last_kv = rel;
             }
           }
@@ -499,8 +524,9 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
       const uint32_t ph = (n >> 1) & 1;
       const int j = static_cast<int>(ti.x % p.nb);
       const bool valid = h < p.G && e < ti.y;
-      // keys of this block visible to the row: t <= i
-      const int nvis = valid ? min(kBk, bs % p.S - j * kBk + 1) : kBk;
+      // keys of this block visible to the row: t <= position of the query
+      const int pos = bs % p.S + (p.chunk && valid ? __ldg(p.q_pos + bs / p.S) : 0);
+      const int nvis = valid ? min(kBk, pos - j * kBk + 1) : kBk;
       const bool ok_s = mbar_wait(&bar_sfull[slot], ph, abort_flag, p.dev_err);
       if (!__all_sync(0xffffffffu, ok_s)) break;     // warp-uniform exit
       tc_fence_after();
@@ -749,8 +775,13 @@ struct WsLayout {
 
 // Tiles of a chunk: sum over items of ceil(entries / 16)
 //   <= entries / 16 + (non-empty items) + 1.
+// Blocks per sequence: those of the prefill, or (chunk) the page-table width.
+int64_t seq_blocks(const msa_prefill_args& a) {
+  return a.mode == MSA_MODE_CHUNK ? a.max_pages : (a.S + kBk - 1) / kBk;
+}
+
 WsLayout ws_layout(const msa_prefill_args& a, int64_t cq) {
-  const int64_t nb = (a.S + kBk - 1) / kBk;
+  const int64_t nb = seq_blocks(a);
   const int64_t n_items = static_cast<int64_t>(a.B) * a.Hkv * nb;
   const int64_t entries = cq * a.Hkv * a.k;
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
@@ -790,7 +821,8 @@ msa_status launch_attn_prefill(const msa_prefill_args& a, void* ws, size_t ws_by
   }
   const int64_t cq = lo;
   const WsLayout L = ws_layout(a, cq);
-  const int64_t nb = (a.S + kBk - 1) / kBk;
+  const int64_t nb = seq_blocks(a);
+  const bool chunk = a.mode == MSA_MODE_CHUNK;
   const int64_t n_items = static_cast<int64_t>(a.B) * a.Hkv * nb;
   const int G = a.Hq / a.Hkv;
   if (L.max_tiles * 128 >= (int64_t(1) << 31) || cq * a.Hkv * a.k >= (int64_t(1) << 31) ||
@@ -812,9 +844,15 @@ msa_status launch_attn_prefill(const msa_prefill_args& a, void* ws, size_t ws_by
         st != MSA_OK)
       return st;
   }
-  const uint64_t dims[4] = {static_cast<uint64_t>(a.D), static_cast<uint64_t>(a.Hkv), static_cast<uint64_t>(a.S),
-                            static_cast<uint64_t>(a.B)};
-  const uint32_t box[4] = {64, 1, 128, 1};
+  // contiguous K/V [B, S, Hkv, D] strides (b, s, g) as (d, g, s, b), box = 128
+  // tokens of one group; page pools [pages, Hkv, Bk, D] strides (page, g, t) as
+  // (d, t, g, page), box = one page of one group.  Both land in shared memory
+  // as 128 rows of 64 columns.
+  const uint64_t dims[4] = {static_cast<uint64_t>(a.D), static_cast<uint64_t>(chunk ? kBk : a.Hkv),
+                            static_cast<uint64_t>(chunk ? a.Hkv : a.S),
+                            static_cast<uint64_t>(chunk ? a.num_pages : a.B)};
+  const uint32_t box[4] = {64, chunk ? 128u : 1u, chunk ? 1u : 128u, 1};
+  // Strides (b, s, g) or (page, g, t): dims 1, 2, 3 take strides 2, 1, 0 either way.
   {
     const uint64_t strides[3] = {static_cast<uint64_t>(a.K_stride[2]) * 2, static_cast<uint64_t>(a.K_stride[1]) * 2,
                                  static_cast<uint64_t>(a.K_stride[0]) * 2};
@@ -842,6 +880,7 @@ msa_status launch_attn_prefill(const msa_prefill_args& a, void* ws, size_t ws_by
     const int nq = static_cast<int>(std::min<int64_t>(cq, total_q - q0));
     CsrParams c;
     c.S = a.S; c.Hkv = a.Hkv; c.Hq = a.Hq; c.G = G; c.k = a.k; c.nb = static_cast<int>(nb);
+    c.chunk = chunk; c.q_pos = a.q_pos; c.seq_pt = a.seq_pt; c.max_pages = a.max_pages; c.num_pages = a.num_pages;
     c.q0 = q0; c.nq = nq;
     c.sel = a.sel; c.count = a.count;
     c.cnt = reinterpret_cast<int32_t*>(w + L.cnt);
@@ -863,6 +902,7 @@ msa_status launch_attn_prefill(const msa_prefill_args& a, void* ws, size_t ws_by
 
     AttnParams p;
     p.S = a.S; p.Hkv = a.Hkv; p.G = G; p.nb = static_cast<int>(nb);
+    p.chunk = chunk; p.q_pos = a.q_pos;
     p.n_items = n_items;
     p.scale_log2 = scale * kLog2e;
     p.tile_off = c.tile_off; p.tile_info = c.tile_info; p.tile_q = c.tile_q;

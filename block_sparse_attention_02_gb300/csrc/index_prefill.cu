@@ -17,6 +17,11 @@
 // passes: thread = token t forms s_t = sum_h w_h ReLU(D[t, (h, q)]) for its
 // queries, the block max over tokens is one `redux.sync.max.f32` per warp and
 // query plus a 4-warp combine in shared memory.
+// A chunk over a paged cache (MSA_MODE_CHUNK) runs the same kernel: query s
+// of sequence b sits at position q_pos[b] + s, key block j is page
+// seq_pt[b][j] of the index-key pool, and an item whose 64 queries straddle a
+// block boundary scores up to the later own block; each query's row then
+// masks its own block to -inf when it is stored.
 // Items pair query block qb with nq-1-qb (constant cost per pair); a persistent
 // CTA per SM takes pairs round-robin and runs two independent item streams
 // ("slots") at once:
@@ -50,6 +55,10 @@ constexpr int kFlush = 32;                          // block scores staged per q
 struct Params {
   int B, S, Hkv, HI, nq, nb_stride;                 // nq = ceil(S / 64)
   int kgroups;                                      // 0: one k_idx shared by all groups (group stride 0)
+  int chunk;                                        // 1: queries at q_pos[b] + s, paged index keys
+  const int32_t* q_pos;                             // chunk: [B]
+  const int32_t* seq_pt;                            // chunk: [B, max_pages]
+  int64_t max_pages, num_pages;
   const float* w;
   int64_t ws0, ws1, ws2;
   float* C;
@@ -59,10 +68,21 @@ struct Params {
 
 struct Item {
   int b, g, qb, own;                                // own = number of key blocks to score
+  int pos0;                                         // position of the sequence's query 0 (0 unless chunk)
 };
 
+// Position of query 0 of sequence b, or -1 when a chunk's q_pos[b] leaves the
+// pages or the score rows (the sequence is then not scored).
+__device__ __forceinline__ int seq_pos0(const Params& p, int b) {
+  if (!p.chunk) return 0;
+  const int64_t q = p.q_pos[b];
+  const int64_t last = q + p.S - 1;
+  return (q < 0 || last >= p.max_pages * kBk || last / kBk >= p.nb_stride) ? -1 : static_cast<int>(q);
+}
+
 // item `which` (0 or 1) of pair `pair`: pairs enumerate (b, g, pp) with qb in
-// {pp, nq-1-pp}; false when the pair has no such item
+// {pp, nq-1-pp}; false when the pair has no such item.  The item scores the
+// blocks before the own block of its last query.
 __device__ __forceinline__ bool pair_item(const Params& p, int64_t pair, int which, Item* it) {
   const int half = (p.nq + 1) / 2;
   const int pp = static_cast<int>(pair % half);
@@ -70,7 +90,10 @@ __device__ __forceinline__ bool pair_item(const Params& p, int64_t pair, int whi
   const int other = p.nq - 1 - pp;
   if (which == 1 && other == pp) return false;
   const int qb = which == 0 ? pp : other;
-  *it = {static_cast<int>(bg / p.Hkv), static_cast<int>(bg % p.Hkv), qb, (qb * kQB) / kBk};
+  const int b = static_cast<int>(bg / p.Hkv);
+  const int pos0 = seq_pos0(p, b);
+  const int own = pos0 < 0 ? 0 : (pos0 + min(qb * kQB + kQB, p.S) - 1) / kBk;
+  *it = {b, static_cast<int>(bg % p.Hkv), qb, own, pos0};
   return true;
 }
 
@@ -303,8 +326,15 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
       }
       if (!__all_sync(0xffffffffu, mbar_wait(&bar_kempty[kr.st], kr.ph ^ 1, abort_flag, p.dev_err))) return false;
       if (leader) {
+        const int gk = p.kgroups ? it.g : 0;
         mbar_arrive_expect_tx(&bar_kfull[kr.st], kKTile);
-        tma_load_4d(s_k + kr.st * kKTile, &kmap, &bar_kfull[kr.st], 0, p.kgroups ? it.g : 0, j * kBk, it.b);
+        if (p.chunk) {   // page of block j; an out-of-range id reads zeros and is reported
+          const int page = p.seq_pt[it.b * p.max_pages + j];
+          if (page < 0 || page >= p.num_pages) report(p.dev_err, MSA_DEVERR_BAD_PAGE);
+          tma_load_4d(s_k + kr.st * kKTile, &kmap, &bar_kfull[kr.st], 0, 0, gk, page);
+        } else {
+          tma_load_4d(s_k + kr.st * kKTile, &kmap, &bar_kfull[kr.st], 0, gk, j * kBk, it.b);
+        }
       }
       kr.next();
       ++n;
@@ -372,6 +402,7 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
     bool ok = true;
     while (ok && !st.done) {
       const Item it = st.it;
+      if (it.pos0 < 0 && tw == 0 && it.qb == 0) report(p.dev_err, MSA_DEVERR_BAD_LEN);
       named_bar_sync(bar_id, 128);                    // the previous item's s_w / s_cst are no longer read
       if (tw < kQW) {
         const int i = it.qb * kQB + q0 + tw;
@@ -456,8 +487,10 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
           for (int rr = 0; rr < kQW / 4; ++rr) {     // warp q4: query rows q0 + 8 q4 .. q0 + 8 q4 + 7
             const int qrow = q0 + q4 * (kQW / 4) + rr;
             const int i = it.qb * kQB + qrow;
+            // a query before the item's last own block has its own block among the passes: -inf
             if (i < p.S && lane < cnt)
-              p.C[it.b * p.cs0 + static_cast<int64_t>(i) * p.cs1 + it.g * p.cs2 + j0 + lane] = s_cst[sl][qrow][lane];
+              p.C[it.b * p.cs0 + static_cast<int64_t>(i) * p.cs1 + it.g * p.cs2 + j0 + lane] =
+                  j0 + lane < (it.pos0 + i) / kBk ? s_cst[sl][qrow][lane] : -INFINITY;
           }
         }
       }
@@ -501,7 +534,22 @@ msa_status launch_index_prefill(const msa_index_args& a, cudaStream_t stream) {
         st != MSA_OK)
       return st;
   }
-  {
+  const bool chunk = a.mode == MSA_MODE_CHUNK;
+  if (chunk) {
+    // index-key pool as 4-D (dI, t, g, page) with strides (page, g, t); box =
+    // one page of one group.  A group stride of 0 becomes a g extent of 1.
+    const bool shared = a.k_idx_stride[1] == 0;
+    const uint64_t dims[4] = {static_cast<uint64_t>(a.dI), static_cast<uint64_t>(kBk),
+                              static_cast<uint64_t>(shared ? 1 : a.Hkv), static_cast<uint64_t>(a.num_pages)};
+    const uint64_t strides[3] = {static_cast<uint64_t>(a.k_idx_stride[2]) * 2,
+                                 static_cast<uint64_t>(shared ? a.k_idx_stride[2] * kBk : a.k_idx_stride[1]) * 2,
+                                 static_cast<uint64_t>(a.k_idx_stride[0]) * 2};
+    const uint32_t box[4] = {64, kBk, 1, 1};
+    if (msa_status st = encode_tiled_map(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, a.k_idx, dims, strides, box,
+                                         CU_TENSOR_MAP_SWIZZLE_128B, "k_idx pool");
+        st != MSA_OK)
+      return st;
+  } else {
     // k_idx as 4-D (dI, g, s, b); box = 128 tokens of one group.  A group
     // stride of 0 (one k_idx for all groups) becomes a g extent of 1.
     // (k_idx_stride is (b, s, g): the group stride is the last one)
@@ -520,7 +568,9 @@ msa_status launch_index_prefill(const msa_index_args& a, cudaStream_t stream) {
   Params p;
   p.B = a.B; p.S = a.S; p.Hkv = a.Hkv; p.HI = a.HI;
   p.nq = (a.S + kQB - 1) / kQB;
-  p.kgroups = a.k_idx_stride[2] != 0;
+  p.kgroups = chunk ? a.k_idx_stride[1] != 0 : a.k_idx_stride[2] != 0;
+  p.chunk = chunk;
+  p.q_pos = a.q_pos; p.seq_pt = a.seq_pt; p.max_pages = a.max_pages; p.num_pages = a.num_pages;
   p.nb_stride = a.nb_stride;
   p.w = a.w; p.ws0 = a.w_stride[0]; p.ws1 = a.w_stride[1]; p.ws2 = a.w_stride[2];
   p.C = a.C; p.cs0 = a.C_stride[0]; p.cs1 = a.C_stride[1]; p.cs2 = a.C_stride[2];

@@ -11,9 +11,10 @@
 // the composite key (key << 32 | ~j) makes every candidate distinct, so the
 // selected set is unique.
 //
-// Short rows (<= 2048 candidates: all prefill rows and short decode rows): one
-// warp per row, the register algorithm of select_warp.cuh.
-// Long decode rows: one 256-thread CTA per row, successive block-wide arg-max.
+// Short rows (<= 2048 candidates: all prefill rows, chunk rows of contexts up
+// to 2049 blocks and short decode rows): one warp per row, the register
+// algorithm of select_warp.cuh.
+// Long rows: one 256-thread CTA per row, successive block-wide arg-max.
 #include "msa_internal.h"
 #include "msa_ptx.cuh"
 #include "select_warp.cuh"
@@ -40,12 +41,14 @@ struct RowInfo {
 
 __device__ __forceinline__ RowInfo row_info(const msa_topk_args& a, int64_t row) {
   RowInfo r;
-  if (a.mode == MSA_MODE_PREFILL) {
+  if (a.mode != MSA_MODE_DECODE) {
     const int64_t g = row % a.Hkv, bs = row / a.Hkv;
     const int64_t s = bs % a.S, b = bs / a.S;
     r.c = a.C + b * a.C_stride[0] + s * a.C_stride[1] + g * a.C_stride[2];
-    r.own = static_cast<int>(s / a.Bk);
-    r.valid = true;
+    // a chunk's query s sits at position q_pos[b] + s
+    const int64_t pos = a.mode == MSA_MODE_CHUNK ? a.q_pos[b] + s : s;
+    r.valid = pos >= 0 && pos / a.Bk < a.nb_stride;
+    r.own = r.valid ? static_cast<int>(pos / a.Bk) : 0;
   } else {
     const int64_t g = row % a.Hkv, b = row / a.Hkv;
     r.c = a.C + b * a.C_stride[0] + g * a.C_stride[1];
@@ -144,11 +147,12 @@ msa_status launch_warp(const msa_topk_args& a, int64_t rows, cudaStream_t stream
 }  // namespace
 
 msa_status launch_topk(const msa_topk_args& a, cudaStream_t stream) {
-  const int64_t rows = (a.mode == MSA_MODE_PREFILL) ? static_cast<int64_t>(a.B) * a.S * a.Hkv
-                                                    : static_cast<int64_t>(a.B) * a.Hkv;
+  const int64_t rows = (a.mode != MSA_MODE_DECODE) ? static_cast<int64_t>(a.B) * a.S * a.Hkv
+                                                   : static_cast<int64_t>(a.B) * a.Hkv;
   if (rows == 0) return MSA_OK;
-  // the largest candidate count of any row
-  const int64_t maxc = (a.mode == MSA_MODE_PREFILL) ? (a.S - 1) / a.Bk : a.nb_stride;
+  // the largest candidate count of any row (a chunk's rows: below nb_stride)
+  const int64_t maxc = a.mode == MSA_MODE_PREFILL ? (a.S - 1) / a.Bk
+                       : a.mode == MSA_MODE_CHUNK ? a.nb_stride - 1 : a.nb_stride;
   msa_status st = MSA_OK;
   if (maxc <= 32) st = launch_warp<1>(a, rows, stream);
   else if (maxc <= 64) st = launch_warp<2>(a, rows, stream);
@@ -156,7 +160,7 @@ msa_status launch_topk(const msa_topk_args& a, cudaStream_t stream) {
   else if (maxc <= 256) st = launch_warp<8>(a, rows, stream);
   else if (maxc <= 512) st = launch_warp<16>(a, rows, stream);
   else if (maxc <= 1024) st = launch_warp<32>(a, rows, stream);
-  else if (maxc <= 2048 && a.mode == MSA_MODE_PREFILL) st = launch_warp<64>(a, rows, stream);
+  else if (maxc <= 2048 && a.mode != MSA_MODE_DECODE) st = launch_warp<64>(a, rows, stream);
   else topk_cta_kernel<<<static_cast<unsigned>(rows), kCtaThreads, 0, stream>>>(a, rows);
   if (st != MSA_OK) return st;
   cudaError_t e = cudaGetLastError();

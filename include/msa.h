@@ -67,11 +67,20 @@ typedef enum msa_status {
 #define MSA_DEVERR_TIMEOUT 0x1   /* a bounded barrier wait ran out */
 #define MSA_DEVERR_BAD_PAGE 0x2  /* a page id outside [0, num_pages) */
 #define MSA_DEVERR_BAD_SEL 0x4   /* a selected block outside the causal range */
-#define MSA_DEVERR_BAD_LEN 0x8   /* seq_len[b] outside [1, max_pages * Bk] or past nb_stride */
+#define MSA_DEVERR_BAD_LEN 0x8   /* seq_len[b] (or a chunk's q_pos[b]) outside the pages or past nb_stride */
 
+/* PREFILL: a causal prefill over contiguous K/V/k_idx tensors.
+ * DECODE:  one query per sequence over a paged cache.
+ * CHUNK:   a chunk of S queries per sequence over a paged cache: query s of
+ *          sequence b sits at absolute position q_pos[b] + s and sees every
+ *          cached token t <= q_pos[b] + s.  This is chunked prefill over a
+ *          cached prefix, and with a small S, decode of several tokens per
+ *          sequence (speculative or multi-token verification).  The chunk's
+ *          own tokens must already be in the pages (msa_cache_append). */
 typedef enum msa_mode {
     MSA_MODE_PREFILL = 0,
-    MSA_MODE_DECODE = 1
+    MSA_MODE_DECODE = 1,
+    MSA_MODE_CHUNK = 2
 } msa_mode;
 
 /* Library version: major * 10000 + minor * 100 + patch. */
@@ -118,6 +127,16 @@ const char *msa_status_string(msa_status s);
  *   MSA_DEVERR_BAD_PAGE is raised.  A sequence whose length is outside
  *   [1, max_pages * Bk], or whose own block is not below nb_stride, is not
  *   scored (its row stays -inf) and raises MSA_DEVERR_BAD_LEN.
+ * CHUNK: queries as in PREFILL (q_idx, w and C with the same shapes and
+ *   strides, S = queries per sequence); index keys in pages as in DECODE
+ *   (k_idx page pool, num_pages, seq_pt, max_pages; group stride 0 allowed).
+ *   q_pos [B] int32: absolute position of query 0 of sequence b.  Query s has
+ *   own block (q_pos[b] + s) / Bk and scores the blocks before it; nb_stride >=
+ *   max over b of ceil((q_pos[b] + S) / Bk).  A sequence with q_pos[b] < 0,
+ *   q_pos[b] + S > max_pages * Bk or a block count past nb_stride is not
+ *   scored (its rows are -inf) and raises MSA_DEVERR_BAD_LEN; a page id
+ *   outside [0, num_pages) raises MSA_DEVERR_BAD_PAGE (that block's scores are
+ *   then unspecified).
  * DECODE, fused selection (optional): when `sel` is non-NULL the same kernel
  *   also performs a2 (exactly what msa_topk_blocks computes with this k) on
  *   each (b, g) row as soon as the row's scores are complete, and when `pt` is
@@ -157,6 +176,7 @@ typedef struct msa_index_args {
     int32_t *last_len;
     int32_t *row_scratch;
     int scratch_zeroed;
+    const int32_t *q_pos;         /* chunk */
 } msa_index_args;
 
 msa_status msa_index_score(const msa_index_args *args, msa_stream_t stream);
@@ -173,6 +193,9 @@ msa_status msa_index_score(const msa_index_args *args, msa_stream_t stream);
  *     sel [B, S, Hkv, k] int32, count [B, S, Hkv] int32 (dense).
  *   DECODE rows (b, g): own block (seq_len[b] - 1) / Bk.  C strides (b, g, -).
  *     sel [B, Hkv, k] int32, count [B, Hkv] int32 (dense).
+ *   CHUNK rows (b, s, g): own block (q_pos[b] + s) / Bk; C, sel and count as
+ *     in PREFILL.  A sequence with q_pos[b] < 0 or an own block not below
+ *     nb_stride gets count 0, all -1 selections and MSA_DEVERR_BAD_LEN.
  * Scores are compared as fp32 (-0 equals +0); NaN scores rank below -inf.
  * A decode row whose length is outside [1, nb_stride * Bk] gets count 0, an
  * all -1 selection and MSA_DEVERR_BAD_LEN.
@@ -187,6 +210,7 @@ typedef struct msa_topk_args {
     int32_t *sel;
     int32_t *count;
     int32_t *dev_err;
+    const int32_t *q_pos;         /* chunk */
 } msa_topk_args;
 
 msa_status msa_topk_blocks(const msa_topk_args *args, msa_stream_t stream);
@@ -226,10 +250,22 @@ msa_status msa_build_page_table(const int32_t *sel, const int32_t *count,
  *     written by msa_topk_blocks);
  *     O [B, S, Hq, D] bf16 (dense), LSE [B, S, Hq] fp32 (dense, natural log,
  *     softmax_scale included).
+ * A selected block outside [0, own block] is ignored and raises
+ * MSA_DEVERR_BAD_SEL.
+ * mode = MSA_MODE_CHUNK (mode 0 = PREFILL; DECODE is not accepted here): the
+ *   queries are a chunk at absolute positions q_pos[b] + s (q_pos [B] int32)
+ *   and K, V are page pools [num_pages, Hkv, Bk, D] bf16 with strides K_stride
+ *   = V_stride = (page, g, t); logical block j of sequence b is page
+ *   seq_pt[b * max_pages + j].  Query s sees the tokens t <= q_pos[b] + s of
+ *   its selected blocks.  A selected block at or past max_pages raises
+ *   MSA_DEVERR_BAD_SEL and a page id outside [0, num_pages) raises
+ *   MSA_DEVERR_BAD_PAGE; either slot is ignored.  Pool slots past a sequence's
+ *   last token must hold finite values (a zero-filled pool does): their
+ *   probabilities are 0, and 0 times a NaN or an infinity is NaN.
  * Workspace: caller-owned device scratch of ws_bytes.  Queries are processed in
  * chunks sized to fit; msa_sparse_attn_prefill_workspace_size(args, q) gives
- * the bytes needed for chunks of q queries (q >= 1); larger workspaces mean
- * fewer passes.  The workspace must stay untouched until the stream has run
+ * the bytes needed for chunks of q queries (q >= 1; in CHUNK mode it reads
+ * mode and max_pages too); larger workspaces mean fewer passes.  The workspace must stay untouched until the stream has run
  * the call.  softmax_scale <= 0 selects 1 / sqrt(D).
  * ------------------------------------------------------------------------ */
 typedef struct msa_prefill_args {
@@ -246,6 +282,11 @@ typedef struct msa_prefill_args {
     void *O;
     float *LSE;
     int32_t *dev_err;
+    msa_mode mode;                /* PREFILL (0) or CHUNK */
+    const int32_t *seq_pt;        /* chunk */
+    int64_t max_pages;            /* chunk */
+    int64_t num_pages;            /* chunk */
+    const int32_t *q_pos;         /* chunk */
 } msa_prefill_args;
 
 size_t msa_sparse_attn_prefill_workspace_size(const msa_prefill_args *args, int64_t chunk_queries);
@@ -275,7 +316,8 @@ msa_status msa_sparse_attn_prefill(const msa_prefill_args *args, void *ws, size_
  * Hkv, k and D) and the memset is skipped.  Either way a call that raises no
  * device error leaves the counters zero; after one that does, zero them again
  * (or pass 0).  Page ids outside [0, num_pages) are skipped
- * (MSA_DEVERR_BAD_PAGE).  softmax_scale <= 0 selects 1/sqrt(D).
+ * (MSA_DEVERR_BAD_PAGE).  softmax_scale <= 0 selects 1/sqrt(D).  Pool slots
+ * past a row's last_len must hold finite values (a zero-filled pool does).
  * ------------------------------------------------------------------------ */
 typedef struct msa_decode_args {
     int B, Hq, Hkv, D, Bk, k;

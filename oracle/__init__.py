@@ -316,6 +316,43 @@ def chunk_rows(q_pos, S: int, T: int):
     return (np.arange(len(qp), dtype=np.int64)[:, None] * T + qp[:, None] + np.arange(S)[None, :]).reshape(-1)
 
 
+def _chunk_context(seq_pt, q_pos, S: int, Bk: int, pools):
+    qp = _i64(q_pos)
+    lengths = qp + S
+    T = int(lengths.max())
+    return qp, T, [gather_pages(x, seq_pt, lengths, Bk) for x in pools]
+
+
+def chunk_scores(q_idx, w, kidx_pool, seq_pt, q_pos, Bk: int = 128):
+    """Block scores C [B, S, Hkv, nbT] (fp64) of a chunk's queries at positions
+    q_pos[b] + s over the paged index keys (nbT = blocks of the longest context)."""
+    qi = _u16(q_idx)
+    B, S = qi.shape[:2]
+    qp, T, (Xd,) = _chunk_context(seq_pt, q_pos, S, Bk, [kidx_pool])
+    rows = chunk_rows(qp, S, T)
+    Cs = prefill_scores(place_chunk(qi, qp, T), Xd, place_chunk(_f32(w), qp, T), Bk, rows)
+    return Cs.reshape(B, S, Cs.shape[1], Cs.shape[2])
+
+
+def chunk_own_blocks(q_pos, S: int, Bk: int = 128):
+    """Own block (q_pos[b] + s) // Bk of each chunk query, [B, S] (index bookkeeping)."""
+    qp = _i64(q_pos)
+    return ((qp[:, None] + np.arange(S)[None, :]) // Bk).astype(np.int32)
+
+
+def chunk_attend(Q, K_pool, V_pool, seq_pt, q_pos, sel, count, scale: float, Bk: int = 128):
+    """Attention of a chunk's queries over the given selection (sel [B,S,Hkv,k],
+    count [B,S,Hkv]).  Returns O [B,S,Hq,D], LSE [B,S,Hq] (fp64)."""
+    q = _u16(Q)
+    B, S = q.shape[:2]
+    qp, T, (Kd, Vd) = _chunk_context(seq_pt, q_pos, S, Bk, [K_pool, V_pool])
+    s, c = _i32(sel), _i32(count)
+    rows = chunk_rows(qp, S, T)
+    O, LSE = prefill_attend(place_chunk(q, qp, T), Kd, Vd, s.reshape(B * S, *s.shape[2:]),
+                            c.reshape(B * S, -1), Bk, scale, rows)
+    return O.reshape(B, S, *O.shape[1:]), LSE.reshape(B, S, -1)
+
+
 def chunk_layer(Q, q_idx, w, K_pool, V_pool, kidx_pool, seq_pt, q_pos, k: int, scale: float, Bk: int = 128):
     """Index scores, selection and attention of a chunk of S queries per
     sequence at positions q_pos[b] + s over a paged cache holding each
@@ -327,21 +364,9 @@ def chunk_layer(Q, q_idx, w, K_pool, V_pool, kidx_pool, seq_pt, q_pos, k: int, s
     count [B,S,Hkv], c_last / c_next (as ``select``), O [B,S,Hq,D] and LSE
     [B,S,Hq] (fp64).
     """
-    qp = _i64(q_pos)
-    B, S = _np(Q).shape[:2]
-    lengths = qp + S
-    T = int(lengths.max())
-    Kd = gather_pages(K_pool, seq_pt, lengths, Bk)
-    Vd = gather_pages(V_pool, seq_pt, lengths, Bk)
-    Xd = gather_pages(kidx_pool, seq_pt, lengths, Bk)
-    Qd, QId, Wd = (place_chunk(_u16(Q), qp, T), place_chunk(_u16(q_idx), qp, T),
-                   place_chunk(_f32(w), qp, T))
-    rows = chunk_rows(qp, S, T)
-    Cs = prefill_scores(QId, Xd, Wd, Bk, rows)
-    own = np.repeat(own_blocks_prefill(T, Bk, rows), Cs.shape[1]).reshape(Cs.shape[:2])
+    Cs = chunk_scores(q_idx, w, kidx_pool, seq_pt, q_pos, Bk)
+    B, S, Hkv = Cs.shape[:3]
+    own = np.repeat(chunk_own_blocks(q_pos, S, Bk)[..., None], Hkv, axis=2)
     sel, cnt, cl, cn = select(Cs, own, k)
-    O, LSE = prefill_attend(Qd, Kd, Vd, sel, cnt, Bk, scale, rows)
-    Hkv, nb = Cs.shape[1], Cs.shape[2]
-    return {"C": Cs.reshape(B, S, Hkv, nb), "sel": sel.reshape(B, S, Hkv, k), "count": cnt.reshape(B, S, Hkv),
-            "c_last": cl.reshape(B, S, Hkv), "c_next": cn.reshape(B, S, Hkv),
-            "O": O.reshape(B, S, -1, O.shape[-1]), "LSE": LSE.reshape(B, S, -1)}
+    O, LSE = chunk_attend(Q, K_pool, V_pool, seq_pt, q_pos, sel, cnt, scale, Bk)
+    return {"C": Cs, "sel": sel, "count": cnt, "c_last": cl, "c_next": cn, "O": O, "LSE": LSE}
