@@ -29,6 +29,9 @@ with "impl": "reference".  Under torchrun only rank 0 runs it.
 
 ``--workload prefill_s131072`` times one prefill layer instead (tokens/s =
 B*S per layer), with the tensor-core roofline of the sparse attention.
+``--workload chunk_b1_p60000_s8192`` (an 8,192-token prefill chunk after a
+60,000-token cached prefix) and ``--workload verify_b8_p60000_s4`` (4 decode
+tokens per sequence at concurrency 8) time one layer over a paged cache.
 """
 from __future__ import annotations
 
@@ -455,10 +458,13 @@ def cpu_decode_baseline(wl, inp_host, budget_s: float, min_steps: int = 1):
 # prefill workload (optional)
 # ---------------------------------------------------------------------------
 
-def prefill_attention_flops(sel, count, S, Bk, G, D):
-    """4*D*G FLOPs per (query, group, key) over the unmasked selected keys (count from the selection)."""
+def prefill_attention_flops(sel, count, S, Bk, G, D, q_pos=None):
+    """4*D*G FLOPs per (query, group, key) over the unmasked selected keys
+    (count from the selection); queries sit at q_pos[b] + i (0 without q_pos)."""
     import torch
     i = torch.arange(S, device=sel.device).view(1, S, 1, 1)
+    if q_pos is not None:
+        i = i + q_pos.long().view(-1, 1, 1, 1)
     s = sel.long()
     keys = torch.where(s < 0, torch.zeros_like(s),
                        torch.clamp(i + 1 - s * Bk, min=0, max=Bk))
@@ -538,6 +544,111 @@ def run_prefill_ours(args, wl, world, rank):
 
 
 # ---------------------------------------------------------------------------
+# chunk over a paged cache (chunked prefill, multi-token decode)
+# ---------------------------------------------------------------------------
+
+def run_chunk_ours(args, wl, world, rank):
+    """One MSA layer over a chunk of S queries per sequence after a cached
+    prefix: tokens/s = B*S per step.  The roofline is that of the dominant
+    kernel: the index score (HBM- or tensor-bound, whichever bound is higher)
+    or the sparse attention (tensor)."""
+    import torch
+    import block_sparse_attention_02_gb300 as msa
+    from workloads import chunk_inputs
+    sh = wl.shape
+    inp = chunk_inputs(wl, device="cuda")
+    ws_q = min(wl.S, args.prefill_chunk) * wl.B
+    sel_probe = torch.empty(1, 1, 1, sh.k, dtype=torch.int32)
+    ws_bytes = msa.msa_sparse_attn_prefill_workspace_size(inp["Q"], inp["K_pool"], sel_probe, ws_q,
+                                                          max_pages=wl.max_pages)
+    bufs = msa.chunk_buffers(wl.B, wl.S, sh.Hq, sh.Hkv, sh.k, wl.max_pages, "cuda", ws_bytes)
+    stream = torch.cuda.current_stream()
+    e = bufs["dev_err"]
+    fns = [
+        lambda: msa.msa_index_score(msa.MSA_MODE_CHUNK, inp["q_idx"], inp["w"], inp["kidx_pool"], bufs["C"],
+                                    seq_pt=inp["seq_pt"], q_pos=inp["q_pos"], dev_err=e),
+        lambda: msa.msa_topk_blocks(msa.MSA_MODE_CHUNK, bufs["C"], sh.k, bufs["sel"], bufs["count"],
+                                    q_pos=inp["q_pos"], dev_err=e),
+        lambda: msa.msa_sparse_attn_prefill(inp["Q"], inp["K_pool"], inp["V_pool"], bufs["sel"], bufs["count"],
+                                            bufs["O"], bufs["LSE"], bufs["ws"], dev_err=e, seq_pt=inp["seq_pt"],
+                                            q_pos=inp["q_pos"]),
+    ]
+    for _ in range(max(1, args.warmup)):
+        for f in fns:
+            f()
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(K):
+        for j, f in enumerate(fns):
+            ev[i][j].record(stream)
+            f()
+        ev[i][3].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    assert int(e.item()) == 0, "device error during the timed steps"
+    total_ms = max_over_ranks(start.elapsed_time(end), world)
+    part_ms = [statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)) for j in range(3)]
+    peaks = load_peaks()
+    # algorithmic work: attention over the unmasked selected keys; index
+    # scores of every earlier block of every query, and its HBM bytes (index
+    # keys of each scored (b, g) block once, q_idx and w read, C written)
+    att_flops = prefill_attention_flops(bufs["sel"], bufs["count"], wl.S, sh.Bk, sh.G, sh.D, inp["q_pos"])
+    own = [[(p + s) // sh.Bk for s in range(wl.S)] for p in wl.prefix]
+    idx_flops = 2.0 * sh.HI * sh.dI * sh.Hkv * sh.Bk * sum(sum(o) for o in own)
+    idx_bytes = (sum(max(o) for o in own) * sh.Hkv * sh.Bk * sh.dI * 2
+                 + wl.B * wl.S * sh.Hkv * (sh.HI * sh.dI * 2 + sh.HI * 4 + wl.max_pages * 4))
+    idx_ms, att_ms = part_ms[0], part_ms[2]
+    t_hbm = idx_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = idx_flops / (peaks["bf16_tflops"] * 1e12)
+    if idx_ms >= att_ms and t_hbm >= t_tc:
+        ach = idx_bytes / (idx_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "kernel": "index score (a1)", "achieved": ach, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "algorithmic_bytes_per_launch": idx_bytes,
+                "launch_ms": idx_ms}
+    elif idx_ms >= att_ms:
+        ach = idx_flops / (idx_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": "index score (a1)", "achieved": ach, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "algorithmic_flops_per_launch": idx_flops,
+                "launch_ms": idx_ms}
+    else:
+        ach = att_flops / (att_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": "sparse attention (a4+a6)", "achieved": ach,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"],
+                "algorithmic_flops_per_launch": att_flops, "launch_ms": att_ms}
+    roof.update({"peak_src": peaks["src"], "traffic": None,
+                 "index_hbm_frac": idx_bytes / (idx_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                 "index_tc_frac": idx_flops / (idx_ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                 "attention_tc_frac": att_flops / (att_ms * 1e-3) / 1e12 / peaks["bf16_tflops"]})
+    step_ms = total_ms / K
+    step_bytes = idx_bytes + 2 * wl.B * wl.S * sh.Hq * sh.D * 2
+    res = {
+        "metric": METRIC, "value": wl.B * wl.S * world / (step_ms * 1e-3), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "batch": wl.B, "chunk": wl.S,
+                   "cached_prefix": wl.prefix[0] if len(set(wl.prefix)) == 1 else list(wl.prefix),
+                   "Hq": sh.Hq, "Hkv": sh.Hkv, "D": sh.D, "HI": sh.HI, "dI": sh.dI, "Bk": sh.Bk, "k": sh.k,
+                   "pages": "128-token, shuffled", "query_chunk": ws_q,
+                   "l2": f"no flush: a step moves more than twice the L2 (>= {step_bytes / 1e6:.0f} MB)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roof,
+        "breakdown_ms": {"index_score": part_ms[0], "topk": part_ms[1], "sparse_attention": part_ms[2]},
+        "gpu_launches": K * (2 + 5 * ((wl.B * wl.S + ws_q - 1) // ws_q)),
+        "clocks": clocks,
+    }
+    return res, None, inp
+
 
 def main():
     ap = argparse.ArgumentParser()
@@ -564,10 +675,11 @@ def main():
         wl = replace(wl, name=f"{wl.name}_s{args.seq}", S=args.seq)
     world, rank, _ = dist_setup()
 
+    from workloads import ChunkWorkload, DecodeWorkload
     if args.impl == "reference":
         if rank != 0:
             return
-        if not hasattr(wl, "lengths"):
+        if not isinstance(wl, DecodeWorkload):
             print(json.dumps({"impl": "reference", "unavailable": "reference arm implemented for decode workloads"}))
             return
         from workloads import decode_inputs
@@ -596,11 +708,13 @@ def main():
         raise SystemExit("bench.py needs a CUDA device for --impl ours")
     from block_sparse_attention_02_gb300 import build as b
     b.build()
-    if hasattr(wl, "lengths"):
+    if isinstance(wl, DecodeWorkload):
         res, host_in, inp = run_decode_ours(args, wl, world, rank)
+    elif isinstance(wl, ChunkWorkload):
+        res, host_in, inp = run_chunk_ours(args, wl, world, rank)
     else:
         res, host_in, inp = run_prefill_ours(args, wl, world, rank)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and hasattr(wl, "lengths"):
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and isinstance(wl, DecodeWorkload):
         h = {n: t.cpu() for n, t in inp.items()}
         res["cpu_baseline"] = cpu_decode_baseline(wl, h, args.cpu_budget_s)
     elif rank == 0:

@@ -22,6 +22,9 @@
 // seq_pt[b][j] of the index-key pool, and an item whose 64 queries straddle a
 // block boundary scores up to the later own block; each query's row then
 // masks its own block to -inf when it is stored.
+// When there are too few items to fill the GPU (short chunks: a few decode
+// tokens per sequence), each item's key blocks are split into nsplit ranges
+// scored by different CTAs (block scores are independent of each other).
 // Items pair query block qb with nq-1-qb (constant cost per pair); a persistent
 // CTA per SM takes pairs round-robin and runs two independent item streams
 // ("slots") at once:
@@ -56,6 +59,7 @@ struct Params {
   int B, S, Hkv, HI, nq, nb_stride;                 // nq = ceil(S / 64)
   int kgroups;                                      // 0: one k_idx shared by all groups (group stride 0)
   int chunk;                                        // 1: queries at q_pos[b] + s, paged index keys
+  int nsplit;                                       // key-block ranges per item
   const int32_t* q_pos;                             // chunk: [B]
   const int32_t* seq_pt;                            // chunk: [B, max_pages]
   int64_t max_pages, num_pages;
@@ -67,49 +71,68 @@ struct Params {
 };
 
 struct Item {
-  int b, g, qb, own;                                // own = number of key blocks to score
-  int pos0;                                         // position of the sequence's query 0 (0 unless chunk)
+  int b, g, qb;
+  int jb, je;                                       // this split's key blocks [jb, je)
+  bool fill;                                        // last split (je = the item's block count): writes
+                                                    // the -inf tail of the rows from je on
 };
+
+// CHUNK (a template parameter of everything below) selects the chunk mode:
+// query positions, paged index keys and split items.  The prefill
+// instantiations see nsplit = 1 and position 0 as constants.
 
 // Position of query 0 of sequence b, or -1 when a chunk's q_pos[b] leaves the
 // pages or the score rows (the sequence is then not scored).
+template <bool CHUNK>
 __device__ __forceinline__ int seq_pos0(const Params& p, int b) {
-  if (!p.chunk) return 0;
-  const int64_t q = p.q_pos[b];
-  const int64_t last = q + p.S - 1;
-  return (q < 0 || last >= p.max_pages * kBk || last / kBk >= p.nb_stride) ? -1 : static_cast<int>(q);
+  if constexpr (!CHUNK) {
+    return 0;
+  } else {
+    const int64_t q = p.q_pos[b];
+    const int64_t last = q + p.S - 1;
+    return (q < 0 || last >= p.max_pages * kBk || last / kBk >= p.nb_stride) ? -1 : static_cast<int>(q);
+  }
 }
 
-// item `which` (0 or 1) of pair `pair`: pairs enumerate (b, g, pp) with qb in
-// {pp, nq-1-pp}; false when the pair has no such item.  The item scores the
-// blocks before the own block of its last query.
-__device__ __forceinline__ bool pair_item(const Params& p, int64_t pair, int which, Item* it) {
+// item `which` (0 or 1) of pair `pair`: pairs enumerate (b, g, pp, split r)
+// with qb in {pp, nq-1-pp}; false when the pair has no such item.  The item
+// scores the blocks before the own block of its last query; split r takes
+// the r-th of nsplit equal ranges of them.
+template <bool CHUNK>
+__device__ __forceinline__ bool pair_item(const Params& p, int pair, int which, Item* it) {
   const int half = (p.nq + 1) / 2;
-  const int pp = static_cast<int>(pair % half);
-  const int64_t bg = pair / half;
+  const int nsplit = CHUNK ? p.nsplit : 1;
+  const int r = pair % nsplit;
+  const int rest = pair / nsplit;
+  const int pp = rest % half;
+  const int bg = rest / half;
   const int other = p.nq - 1 - pp;
   if (which == 1 && other == pp) return false;
   const int qb = which == 0 ? pp : other;
-  const int b = static_cast<int>(bg / p.Hkv);
-  const int pos0 = seq_pos0(p, b);
+  const int b = bg / p.Hkv;
+  const int pos0 = seq_pos0<CHUNK>(p, b);
   const int own = pos0 < 0 ? 0 : (pos0 + min(qb * kQB + kQB, p.S) - 1) / kBk;
-  *it = {b, static_cast<int>(bg % p.Hkv), qb, own, pos0};
+  const int jb = static_cast<int>(static_cast<int64_t>(own) * r / nsplit);
+  const int je = static_cast<int>(static_cast<int64_t>(own) * (r + 1) / nsplit);
+  *it = {b, bg % p.Hkv, qb, jb, je, r == nsplit - 1};
   return true;
 }
 
 // The items of one slot: in the k-th pair of this CTA the slot takes item
 // slot ^ (k & 1), so long and short items alternate between the slots.
 struct Stream {
-  int64_t pr;      // next pair to look at
+  int pr;          // next pair to look at
   int k;           // its ordinal in this CTA
   Item it;         // current item
   int j;           // next key block of the current item
   bool done;
 };
 
-// keep_empty: also stop at items with no key block to score (the epilogue
-// still writes their -inf rows; the producer and the MMA warp skip them)
-__device__ __forceinline__ void stream_advance(const Params& p, Stream& s, int slot, int64_t npairs,
+// keep_empty: also stop at last splits with no key block to score (the
+// epilogue still writes their -inf rows; the producer and the MMA warp skip
+// them)
+template <bool CHUNK>
+__device__ __forceinline__ void stream_advance(const Params& p, Stream& s, int slot, int npairs,
                                                bool keep_empty) {
   for (;;) {
     if (s.pr >= npairs) {
@@ -117,22 +140,23 @@ __device__ __forceinline__ void stream_advance(const Params& p, Stream& s, int s
       return;
     }
     Item it;
-    const bool ok = pair_item(p, s.pr, slot ^ (s.k & 1), &it);
+    const bool ok = pair_item<CHUNK>(p, s.pr, slot ^ (s.k & 1), &it);
     s.pr += gridDim.x;
     ++s.k;
-    if (ok && (keep_empty || it.own > 0)) {
+    if (ok && (it.je > it.jb || (keep_empty && it.fill))) {
       s.it = it;
-      s.j = 0;
+      s.j = it.jb;
       return;
     }
   }
 }
 
-__device__ __forceinline__ void stream_init(const Params& p, Stream& s, int slot, int64_t npairs, bool keep_empty) {
+template <bool CHUNK>
+__device__ __forceinline__ void stream_init(const Params& p, Stream& s, int slot, int npairs, bool keep_empty) {
   s.pr = blockIdx.x;
   s.k = 0;
   s.done = false;
-  stream_advance(p, s, slot, npairs, keep_empty);
+  stream_advance<CHUNK>(p, s, slot, npairs, keep_empty);
 }
 
 template <int N>
@@ -140,12 +164,12 @@ using SlotC = std::integral_constant<int, N>;
 
 // One pass of stream `st` (slot SLOT): hand it to f(SlotC<SLOT>, item, j,
 // first, last) and step the stream.  first/last = first/last pass of the item.
-template <int SLOT, class F>
-__device__ __forceinline__ bool stream_pass(const Params& p, Stream& st, int64_t npairs, F& f) {
+template <bool CHUNK, int SLOT, class F>
+__device__ __forceinline__ bool stream_pass(const Params& p, Stream& st, int npairs, F& f) {
   const Item it = st.it;
   const int j = st.j;
-  if (++st.j == it.own) stream_advance(p, st, SLOT, npairs, false);
-  return f(SlotC<SLOT>{}, it, j, j == 0, j == it.own - 1);
+  if (++st.j == it.je) stream_advance<CHUNK>(p, st, SLOT, npairs, false);
+  return f(SlotC<SLOT>{}, it, j, j == it.jb, j == it.je - 1);
 }
 
 // The merged pass order of the producer and the MMA warp: the two slots'
@@ -153,11 +177,11 @@ __device__ __forceinline__ bool stream_pass(const Params& p, Stream& st, int64_t
 // compile-time constant, so per-slot state and barrier addresses need no
 // runtime selection, and both streams stay in registers.  Stops early when f
 // returns false.
-template <class F>
-__device__ __forceinline__ void for_each_pass(const Params& p, int64_t npairs, F&& f) {
+template <bool CHUNK, class F>
+__device__ __forceinline__ void for_each_pass(const Params& p, int npairs, F&& f) {
   Stream s0, s1;
-  stream_init(p, s0, 0, npairs, false);
-  stream_init(p, s1, 1, npairs, false);
+  stream_init<CHUNK>(p, s0, 0, npairs, false);
+  stream_init<CHUNK>(p, s1, 1, npairs, false);
   bool turn = false;
   for (;;) {
     bool one;
@@ -171,7 +195,7 @@ __device__ __forceinline__ void for_each_pass(const Params& p, int64_t npairs, F
     } else {
       return;
     }
-    if (!(one ? stream_pass<1>(p, s1, npairs, f) : stream_pass<0>(p, s0, npairs, f))) return;
+    if (!(one ? stream_pass<CHUNK, 1>(p, s1, npairs, f) : stream_pass<CHUNK, 0>(p, s0, npairs, f))) return;
   }
 }
 
@@ -270,7 +294,7 @@ __device__ __forceinline__ void regs_after_wait(uint32_t (&r)[8]) {
 constexpr int kCQ = 8;                               // queries per epilogue chunk
 constexpr int kNC = kQW / kCQ;                       // chunks per pass and warp
 
-template <int HI>
+template <int HI, bool CHUNK>
 __global__ void __launch_bounds__(kThreads, 1)
 index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                      const Params p) {
@@ -303,7 +327,7 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   volatile int* abort_flag = &s_abort;
-  const int64_t npairs = static_cast<int64_t>(p.B) * p.Hkv * ((p.nq + 1) / 2);
+  const int npairs = p.B * p.Hkv * ((p.nq + 1) / 2) * (CHUNK ? p.nsplit : 1);   // < 2^31, checked at launch
 
   if (warp == 0) {
     // ===================== TMA producer =====================
@@ -311,7 +335,7 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
     const bool leader = elect_one();
     Ring kr;
     int n = 0, nql[2] = {0, 0};   // k blocks issued; q tiles issued per slot
-    for_each_pass(p, npairs, [&](auto slot_c, const Item& it, int j, bool first, bool) -> bool {
+    for_each_pass<CHUNK>(p, npairs, [&](auto slot_c, const Item& it, int j, bool first, bool) -> bool {
       constexpr int slot = decltype(slot_c)::value;
       if (first) {   // the item's q_idx tile into the slot's buffer, once its previous item is done
         if (!__all_sync(0xffffffffu, mbar_wait(&bar_qempty[slot], (nql[slot] & 1) ^ 1, abort_flag, p.dev_err)))
@@ -328,7 +352,7 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
       if (leader) {
         const int gk = p.kgroups ? it.g : 0;
         mbar_arrive_expect_tx(&bar_kfull[kr.st], kKTile);
-        if (p.chunk) {   // page of block j; an out-of-range id reads zeros and is reported
+        if constexpr (CHUNK) {   // page of block j; an out-of-range id reads zeros and is reported
           const int page = p.seq_pt[it.b * p.max_pages + j];
           if (page < 0 || page >= p.num_pages) report(p.dev_err, MSA_DEVERR_BAD_PAGE);
           tma_load_4d(s_k + kr.st * kKTile, &kmap, &bar_kfull[kr.st], 0, 0, gk, page);
@@ -359,7 +383,7 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
     const uint64_t qdesc0 = sdesc_sw128(smem_u32(s_q), 16, 1024);
     Ring kr;
     uint32_t qph[2] = {0, 0}, tph[2] = {0, 0};   // parities of the slots' qfull / tempty waits
-    for_each_pass(p, npairs, [&](auto slot_c, const Item&, int, bool first, bool last) -> bool {
+    for_each_pass<CHUNK>(p, npairs, [&](auto slot_c, const Item&, int, bool first, bool last) -> bool {
       constexpr int slot = decltype(slot_c)::value;
       if (first) {
         if (!__all_sync(0xffffffffu, mbar_wait(&bar_qfull[slot], qph[slot], abort_flag, p.dev_err))) return false;
@@ -397,12 +421,13 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
     const int bar_id = 1 + wg;
     const uint32_t base = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + sl * kBufCols + q0;
     Stream st;
-    stream_init(p, st, sl, npairs, true);
+    stream_init<CHUNK>(p, st, sl, npairs, true);
     int np = 0;
     bool ok = true;
     while (ok && !st.done) {
       const Item it = st.it;
-      if (it.pos0 < 0 && tw == 0 && it.qb == 0) report(p.dev_err, MSA_DEVERR_BAD_LEN);
+      const int pos0 = seq_pos0<CHUNK>(p, it.b);    // -1: a rejected chunk sequence (no passes)
+      if (pos0 < 0 && tw == 0 && it.qb == 0 && it.fill) report(p.dev_err, MSA_DEVERR_BAD_LEN);
       named_bar_sync(bar_id, 128);                    // the previous item's s_w / s_cst are no longer read
       if (tw < kQW) {
         const int i = it.qb * kQB + q0 + tw;
@@ -412,7 +437,15 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
         for (int h = 0; h < HI; ++h) sw[2 * h] = i < p.S ? wp[h] : 0.f;
       }
       named_bar_sync(bar_id, 128);
-      for (int j = 0; j < it.own; ++j) {
+      // -inf for every entry from the item's block count on (the last split
+      // only; disjoint from the columns the passes below store)
+      for (int rr = 0; rr < kQW / 4 && it.fill; ++rr) {
+        const int i = it.qb * kQB + q0 + q4 * (kQW / 4) + rr;
+        if (i >= p.S) break;
+        float* rowp = p.C + it.b * p.cs0 + static_cast<int64_t>(i) * p.cs1 + it.g * p.cs2;
+        for (int jj = it.je + lane; jj < p.nb_stride; jj += 32) rowp[jj] = -INFINITY;
+      }
+      for (int j = it.jb; j < it.je; ++j) {
         // warp-uniform decision: the TMEM loads below are warp-collective
         const bool got = __all_sync(0xffffffffu, mbar_wait(&bar_tfull[sl], np & 1, abort_flag, p.dev_err));
         if (got) tc_fence_after();
@@ -481,28 +514,22 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
           s_cst[sl][q0 + tw][j % kFlush] = fmaxf(fmaxf(rp[0], rp[kQB]), fmaxf(rp[2 * kQB], rp[3 * kQB]));
         }
         ++np;
-        if (j % kFlush == kFlush - 1 || j == it.own - 1) {
+        if (j % kFlush == kFlush - 1 || j == it.je - 1) {
           named_bar_sync(bar_id, 128);
-          const int j0 = j - j % kFlush, cnt = j % kFlush + 1;
+          // staged blocks j0 .. j (s_cst column = block mod kFlush)
+          const int jal = j - j % kFlush, j0 = max(it.jb, jal), cnt = j - j0 + 1;
           for (int rr = 0; rr < kQW / 4; ++rr) {     // warp q4: query rows q0 + 8 q4 .. q0 + 8 q4 + 7
             const int qrow = q0 + q4 * (kQW / 4) + rr;
             const int i = it.qb * kQB + qrow;
             // a query before the item's last own block has its own block among the passes: -inf
             if (i < p.S && lane < cnt)
               p.C[it.b * p.cs0 + static_cast<int64_t>(i) * p.cs1 + it.g * p.cs2 + j0 + lane] =
-                  j0 + lane < (it.pos0 + i) / kBk ? s_cst[sl][qrow][lane] : -INFINITY;
+                  j0 + lane < (pos0 + i) / kBk ? s_cst[sl][qrow][j0 - jal + lane] : -INFINITY;
           }
         }
       }
       if (!ok) break;
-      // -inf for the own block and every later entry of the item's rows
-      for (int rr = 0; rr < kQW / 4; ++rr) {
-        const int i = it.qb * kQB + q0 + q4 * (kQW / 4) + rr;
-        if (i >= p.S) break;
-        float* rowp = p.C + it.b * p.cs0 + static_cast<int64_t>(i) * p.cs1 + it.g * p.cs2;
-        for (int jj = it.own + lane; jj < p.nb_stride; jj += 32) rowp[jj] = -INFINITY;
-      }
-      stream_advance(p, st, sl, npairs, true);
+      stream_advance<CHUNK>(p, st, sl, npairs, true);
     }
   }
 
@@ -577,12 +604,24 @@ msa_status launch_index_prefill(const msa_index_args& a, cudaStream_t stream) {
   p.dev_err = a.dev_err;
   const size_t smem = 1024 + 2 * static_cast<size_t>(kQTile) + static_cast<size_t>(kKStages) * kKTile;
   if (smem > dev.max_smem_optin) return fail(MSA_ERR_UNSUPPORTED, "prefill index score: not enough shared memory");
-  void (*kern)(const CUtensorMap, const CUtensorMap, const Params) =
-      a.HI == 1 ? index_prefill_kernel<1> : a.HI == 2 ? index_prefill_kernel<2>
-                                          : a.HI == 3 ? index_prefill_kernel<3> : index_prefill_kernel<4>;
+  using Kern = void (*)(const CUtensorMap, const CUtensorMap, const Params);
+  static constexpr Kern kPrefill[4] = {index_prefill_kernel<1, false>, index_prefill_kernel<2, false>,
+                                       index_prefill_kernel<3, false>, index_prefill_kernel<4, false>};
+  static constexpr Kern kChunk[4] = {index_prefill_kernel<1, true>, index_prefill_kernel<2, true>,
+                                     index_prefill_kernel<3, true>, index_prefill_kernel<4, true>};
+  const Kern kern = (chunk ? kChunk : kPrefill)[a.HI - 1];
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(index_prefill)");
-  const int64_t npairs = static_cast<int64_t>(a.B) * a.Hkv * ((p.nq + 1) / 2);
+  // Too few items for two per slot of every CTA: split each item's key
+  // blocks into ranges of at least 16 blocks (the longest row has at most
+  // max_own blocks before its own).
+  const int64_t items = static_cast<int64_t>(a.B) * a.Hkv * p.nq;
+  const int64_t want = 4 * static_cast<int64_t>(dev.num_sms);
+  const int64_t max_own = chunk ? a.max_pages : (a.S - 1) / kBk;
+  p.nsplit = items >= want ? 1 : static_cast<int>(std::max<int64_t>(1, std::min((want + items - 1) / items,
+                                                                                   max_own / 16)));
+  const int64_t npairs = static_cast<int64_t>(a.B) * a.Hkv * ((p.nq + 1) / 2) * p.nsplit;
+  if (npairs >= (int64_t(1) << 31)) return fail(MSA_ERR_UNSUPPORTED, "prefill index score: too many query blocks");
   const int grid = static_cast<int>(std::min<int64_t>(dev.num_sms, std::max<int64_t>(npairs, 1)));
   kern<<<grid, kThreads, smem, stream>>>(qmap, kmap, p);
   e = cudaGetLastError();
