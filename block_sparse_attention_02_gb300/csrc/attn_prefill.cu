@@ -138,61 +138,98 @@ __global__ void csr_count_kernel(const CsrParams p) {
 
 __device__ __forceinline__ int tiles_of(int c) { return (c + kEntries - 1) / kEntries; }
 
-// single CTA: exclusive scans of entries, tiles and non-empty items
-__global__ void __launch_bounds__(1024) csr_scan_kernel(const CsrParams p, int64_t n_items) {
-  __shared__ int64_t s_sum[32][3];
-  const int tid = threadIdx.x;
-  const int64_t per = (n_items + 1023) / 1024;
-  const int64_t i0 = min(n_items, tid * per), i1 = min(n_items, i0 + per);
-  int64_t c = 0, t = 0, z = 0;
-  for (int64_t x = i0; x < i1; ++x) {
-    const int v = p.cnt[x];
-    c += v;
-    t += tiles_of(v);
-    z += v > 0;
-  }
-  // inclusive warp scans, then a scan of the 32 warp totals
-  const int lane = tid & 31, wid = tid >> 5;
-  int64_t ic = c, it = t, iz = z;
+// single CTA: exclusive scans of entries, tiles and non-empty items, one pass
+// over tiles of 4096 items (4 consecutive items per thread, 16-byte loads and
+// stores) with a block-wide scan per tile and a running carry.  Totals fit in
+// int32: entries and tile rows are checked against 2^31 at launch.
+constexpr int kScanThreads = 1024;
+constexpr int kScanPer = 4;
+
+__device__ __forceinline__ void scan_store4(int32_t* a, int64_t x0, int64_t n, const int (&v)[kScanPer]) {
+  if (x0 + kScanPer <= n) {
+    *reinterpret_cast<int4*>(a + x0) = make_int4(v[0], v[1], v[2], v[3]);
+  } else {
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int64_t xc = __shfl_up_sync(0xffffffffu, ic, o);
-    const int64_t xt = __shfl_up_sync(0xffffffffu, it, o);
-    const int64_t xz = __shfl_up_sync(0xffffffffu, iz, o);
-    if (lane >= o) { ic += xc; it += xt; iz += xz; }
+    for (int u = 0; u < kScanPer; ++u)
+      if (x0 + u < n) a[x0 + u] = v[u];
   }
-  if (lane == 31) { s_sum[wid][0] = ic; s_sum[wid][1] = it; s_sum[wid][2] = iz; }
+}
+
+__global__ void __launch_bounds__(kScanThreads) csr_scan_kernel(const CsrParams p, int64_t n_items) {
+  __shared__ int s_sum[32][3];
+  __shared__ int s_carry[3];                     // entries, tiles, non-empty items before this tile
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  if (tid == 0) s_carry[0] = s_carry[1] = s_carry[2] = 0;
   __syncthreads();
-  if (wid == 0) {
-    int64_t wc = s_sum[lane][0], wt = s_sum[lane][1], wz = s_sum[lane][2];
+  for (int64_t base = 0; base < n_items; base += kScanThreads * kScanPer) {
+    const int64_t x0 = base + static_cast<int64_t>(tid) * kScanPer;
+    int v[kScanPer];
+    if (x0 + kScanPer <= n_items) {
+      const int4 q = *reinterpret_cast<const int4*>(p.cnt + x0);
+      v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+    } else {
+#pragma unroll
+      for (int u = 0; u < kScanPer; ++u) v[u] = x0 + u < n_items ? p.cnt[x0 + u] : 0;
+    }
+    int c = 0, t = 0, z = 0;
+#pragma unroll
+    for (int u = 0; u < kScanPer; ++u) {
+      c += v[u];
+      t += tiles_of(v[u]);
+      z += v[u] > 0;
+    }
+    // inclusive scans within the warp, then over the 32 warp totals
+    int ic = c, it = t, iz = z;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int64_t xc = __shfl_up_sync(0xffffffffu, wc, o);
-      const int64_t xt = __shfl_up_sync(0xffffffffu, wt, o);
-      const int64_t xz = __shfl_up_sync(0xffffffffu, wz, o);
-      if (lane >= o) { wc += xc; wt += xt; wz += xz; }
+      const int xc = __shfl_up_sync(0xffffffffu, ic, o);
+      const int xt = __shfl_up_sync(0xffffffffu, it, o);
+      const int xz = __shfl_up_sync(0xffffffffu, iz, o);
+      if (lane >= o) { ic += xc; it += xt; iz += xz; }
     }
-    s_sum[lane][0] = wc;   // inclusive over warps
-    s_sum[lane][1] = wt;
-    s_sum[lane][2] = wz;
-    if (lane == 31) {
-      p.off[n_items] = static_cast<int32_t>(wc);
-      p.tile_off[n_items] = static_cast<int32_t>(wt);
+    if (lane == 31) { s_sum[wid][0] = ic; s_sum[wid][1] = it; s_sum[wid][2] = iz; }
+    __syncthreads();
+    if (wid == 0) {
+      int wc = s_sum[lane][0], wt = s_sum[lane][1], wz = s_sum[lane][2];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int xc = __shfl_up_sync(0xffffffffu, wc, o);
+        const int xt = __shfl_up_sync(0xffffffffu, wt, o);
+        const int xz = __shfl_up_sync(0xffffffffu, wz, o);
+        if (lane >= o) { wc += xc; wt += xt; wz += xz; }
+      }
+      s_sum[lane][0] = wc;   // inclusive over warps
+      s_sum[lane][1] = wt;
+      s_sum[lane][2] = wz;
     }
+    __syncthreads();
+    // exclusive prefixes of this thread's first item
+    int pc = s_carry[0] + ic - c + (wid > 0 ? s_sum[wid - 1][0] : 0);
+    int pt = s_carry[1] + it - t + (wid > 0 ? s_sum[wid - 1][1] : 0);
+    int pz = s_carry[2] + iz - z + (wid > 0 ? s_sum[wid - 1][2] : 0);
+    int o_c[kScanPer], o_t[kScanPer], o_z[kScanPer];
+#pragma unroll
+    for (int u = 0; u < kScanPer; ++u) {
+      o_c[u] = pc; o_t[u] = pt; o_z[u] = pz;
+      pc += v[u];
+      pt += tiles_of(v[u]);
+      pz += v[u] > 0;
+    }
+    scan_store4(p.off, x0, n_items, o_c);
+    scan_store4(p.cursor, x0, n_items, o_c);
+    scan_store4(p.tile_off, x0, n_items, o_t);
+    scan_store4(p.ord, x0, n_items, o_z);
+    __syncthreads();                             // every thread has read s_carry and s_sum
+    if (tid == 0) {
+      s_carry[0] += s_sum[31][0];
+      s_carry[1] += s_sum[31][1];
+      s_carry[2] += s_sum[31][2];
+    }
+    __syncthreads();
   }
-  __syncthreads();
-  c = ic - c + (wid > 0 ? s_sum[wid - 1][0] : 0);   // exclusive prefixes of this thread
-  t = it - t + (wid > 0 ? s_sum[wid - 1][1] : 0);
-  z = iz - z + (wid > 0 ? s_sum[wid - 1][2] : 0);
-  for (int64_t x = i0; x < i1; ++x) {
-    const int v = p.cnt[x];
-    p.off[x] = static_cast<int32_t>(c);
-    p.cursor[x] = static_cast<int32_t>(c);
-    p.tile_off[x] = static_cast<int32_t>(t);
-    p.ord[x] = static_cast<int32_t>(z);
-    c += v;
-    t += tiles_of(v);
-    z += v > 0;
+  if (tid == 0) {
+    p.off[n_items] = s_carry[0];
+    p.tile_off[n_items] = s_carry[1];
   }
 }
 
@@ -897,7 +934,7 @@ msa_status launch_attn_prefill(const msa_prefill_args& a, void* ws, size_t ws_by
     const int64_t work = static_cast<int64_t>(nq) * a.Hkv * a.k;
     const int grid_w = static_cast<int>(std::min<int64_t>((work + 255) / 256, 8 * dev.num_sms));
     csr_count_kernel<<<grid_w, 256, 0, stream>>>(c);
-    csr_scan_kernel<<<1, 1024, 0, stream>>>(c, n_items);
+    csr_scan_kernel<<<1, kScanThreads, 0, stream>>>(c, n_items);
     csr_fill_kernel<<<grid_w, 256, 0, stream>>>(c);
 
     AttnParams p;

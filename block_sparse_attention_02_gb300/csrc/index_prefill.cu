@@ -294,7 +294,10 @@ __device__ __forceinline__ void regs_after_wait(uint32_t (&r)[8]) {
 constexpr int kCQ = 8;                               // queries per epilogue chunk
 constexpr int kNC = kQW / kCQ;                       // chunks per pass and warp
 
-template <int HI, bool CHUNK>
+// FEW: a chunk of at most kCQ queries per sequence (a few decode tokens):
+// only the first 8-query chunk of the first query half holds queries, so the
+// epilogue loads and reduces that chunk alone.
+template <int HI, bool CHUNK, bool FEW>
 __global__ void __launch_bounds__(kThreads, 1)
 index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                      const Params p) {
@@ -488,7 +491,18 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
             dst[1] = make_float4(km[4], km[5], km[6], km[7]);
           }
         };
-        if (got) {
+        if constexpr (FEW) {
+          if (got) {
+            if (q0 == 0) {
+              load(0, va);
+              wait(va);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_tempty[sl]);
+            if (q0 == 0) reduce(0, va);
+          }
+        } else if (got) {
           load(0, va);
           wait(va);
 #pragma unroll
@@ -605,11 +619,13 @@ msa_status launch_index_prefill(const msa_index_args& a, cudaStream_t stream) {
   const size_t smem = 1024 + 2 * static_cast<size_t>(kQTile) + static_cast<size_t>(kKStages) * kKTile;
   if (smem > dev.max_smem_optin) return fail(MSA_ERR_UNSUPPORTED, "prefill index score: not enough shared memory");
   using Kern = void (*)(const CUtensorMap, const CUtensorMap, const Params);
-  static constexpr Kern kPrefill[4] = {index_prefill_kernel<1, false>, index_prefill_kernel<2, false>,
-                                       index_prefill_kernel<3, false>, index_prefill_kernel<4, false>};
-  static constexpr Kern kChunk[4] = {index_prefill_kernel<1, true>, index_prefill_kernel<2, true>,
-                                     index_prefill_kernel<3, true>, index_prefill_kernel<4, true>};
-  const Kern kern = (chunk ? kChunk : kPrefill)[a.HI - 1];
+  static constexpr Kern kPrefill[4] = {index_prefill_kernel<1, false, false>, index_prefill_kernel<2, false, false>,
+                                       index_prefill_kernel<3, false, false>, index_prefill_kernel<4, false, false>};
+  static constexpr Kern kChunk[4] = {index_prefill_kernel<1, true, false>, index_prefill_kernel<2, true, false>,
+                                     index_prefill_kernel<3, true, false>, index_prefill_kernel<4, true, false>};
+  static constexpr Kern kFew[4] = {index_prefill_kernel<1, true, true>, index_prefill_kernel<2, true, true>,
+                                   index_prefill_kernel<3, true, true>, index_prefill_kernel<4, true, true>};
+  const Kern kern = (!chunk ? kPrefill : a.S <= kCQ ? kFew : kChunk)[a.HI - 1];
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(index_prefill)");
   // Too few items for two per slot of every CTA: split each item's key
