@@ -186,3 +186,66 @@ def test_cache_append_rejects(abi):
     assert abi.load().msa_cache_append(C.byref(a), None) == 2
     a.Bk = 128
     assert abi.load().msa_cache_append(C.byref(a), None) == 1   # NULL pointers
+
+
+def _chunk_index_args(abi, **kw):
+    a = abi.IndexArgs()
+    a.mode, a.B, a.S, a.Hkv, a.HI, a.dI, a.Bk = abi.MSA_MODE_CHUNK, 2, 4, 8, 4, 64, 128
+    a.q_idx = a.w = a.k_idx = a.C = a.seq_pt = a.q_pos = FAKE
+    a.q_idx_stride[:] = [8192, 2048, 256, 64]
+    a.w_stride[:] = [128, 32, 4]
+    a.k_idx_stride[:] = [65536, 8192, 64]      # page pool strides (page, g, t)
+    a.C_stride[:] = [4 * 8 * 100, 8 * 100, 100]
+    a.num_pages, a.max_pages, a.nb_stride = 10, 5, 100
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("q_pos", None, 1), ("seq_pt", None, 1), ("num_pages", 0, 1), ("max_pages", 0, 1), ("nb_stride", 0, 1),
+])
+def test_chunk_index_rejects(abi, field, value, status):
+    lib = abi.load()
+    a = _chunk_index_args(abi, **{field: value})
+    assert lib.msa_index_score(C.byref(a), None) == status
+    assert lib.msa_last_error_string()
+
+
+def test_chunk_index_group_stride(abi):
+    """A chunk's index pool may share one group (stride 0 at the pool's group
+    index 1); a zero page or token stride is rejected."""
+    lib = abi.load()
+    a = _chunk_index_args(abi)
+    a.k_idx_stride[1] = 0
+    assert lib.msa_index_score(C.byref(a), None) == abi.MSA_ERR_CUDA      # valid: stops at the missing device
+    a = _chunk_index_args(abi)
+    a.k_idx_stride[2] = 0
+    assert lib.msa_index_score(C.byref(a), None) == abi.MSA_ERR_INVALID_ARG
+
+
+def test_chunk_topk_and_attention_reject(abi):
+    lib = abi.load()
+    t = abi.TopkArgs()
+    t.mode, t.B, t.S, t.Hkv, t.Bk, t.k = abi.MSA_MODE_CHUNK, 1, 4, 8, 128, 16
+    t.C = t.sel = t.count = FAKE
+    t.C_stride[:] = [3200, 800, 100]
+    t.nb_stride = 100
+    assert lib.msa_topk_blocks(C.byref(t), None) == abi.MSA_ERR_INVALID_ARG   # q_pos NULL
+    a = abi.PrefillArgs()
+    a.B, a.S, a.Hq, a.Hkv, a.D, a.Bk, a.k = 1, 4, 48, 8, 128, 128, 16
+    a.Q = a.K = a.V = a.sel = a.count = a.O = FAKE
+    a.Q_stride[:] = [4 * 48 * 128, 48 * 128, 128]
+    a.K_stride[:] = a.V_stride[:] = [8 * 128 * 128, 128 * 128, 128]
+    ws = FAKE
+    a.mode = abi.MSA_MODE_DECODE
+    assert lib.msa_sparse_attn_prefill(C.byref(a), ws, 1 << 30, None) == abi.MSA_ERR_INVALID_ARG
+    a.mode = abi.MSA_MODE_CHUNK
+    assert lib.msa_sparse_attn_prefill(C.byref(a), ws, 1 << 30, None) == abi.MSA_ERR_INVALID_ARG   # no seq_pt
+    a.seq_pt = a.q_pos = FAKE
+    a.max_pages, a.num_pages = 5, (1 << 29) + 1            # page ids must fit the tile descriptor
+    assert lib.msa_sparse_attn_prefill(C.byref(a), ws, 1 << 30, None) == abi.MSA_ERR_INVALID_ARG
+    a.num_pages = 10
+    assert lib.msa_sparse_attn_prefill_workspace_size(C.byref(a), 4) > 0
+    a.max_pages = 0
+    assert lib.msa_sparse_attn_prefill_workspace_size(C.byref(a), 4) == 0
