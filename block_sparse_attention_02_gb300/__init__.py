@@ -305,6 +305,8 @@ def msa_cache_append(K_new: torch.Tensor, V_new: torch.Tensor, kidx_new: torch.T
 
     K_new, V_new [B,Hkv,D], kidx_new [B,Hkv,dI] bf16; K_pool, V_pool [P,Hkv,Bk,D] and
     kidx_pool [P,Hkv,Bk,dI] bf16; seq_pt [B,max_pages] int32 (contiguous rows), seq_len [B].
+    With 4-D K_new, V_new [B,T,Hkv,D] and kidx_new [B,T,Hkv,dI] the T tokens of each
+    sequence go to positions L_b - T .. L_b - 1.
     """
     for t, nm in ((K_new, "K_new"), (V_new, "V_new"), (kidx_new, "kidx_new"), (K_pool, "K_pool"),
                   (V_pool, "V_pool"), (kidx_pool, "kidx_pool")):
@@ -314,12 +316,21 @@ def msa_cache_append(K_new: torch.Tensor, V_new: torch.Tensor, kidx_new: torch.T
     if not seq_pt.is_contiguous():
         raise ValueError("seq_pt must be contiguous")
     a = _abi.AppendArgs()
-    a.B, a.Hkv, a.D = K_new.shape
-    a.dI, a.Bk = kidx_new.shape[2], K_pool.shape[2]
+    if K_new.dim() == 4:   # several tokens per sequence: strides (b, u, g)
+        a.B, a.T, a.Hkv, a.D = K_new.shape
+        a.new_t_stride[:] = [K_new.stride(1), V_new.stride(1), kidx_new.stride(1)]
+        K_new_bg = [K_new.stride(0), K_new.stride(2)]
+        V_new_bg = [V_new.stride(0), V_new.stride(2)]
+        X_new_bg = [kidx_new.stride(0), kidx_new.stride(2)]
+    else:
+        a.B, a.Hkv, a.D = K_new.shape
+        a.T = 1
+        K_new_bg, V_new_bg, X_new_bg = _strides(K_new, 2), _strides(V_new, 2), _strides(kidx_new, 2)
+    a.dI, a.Bk = kidx_new.shape[-1], K_pool.shape[2]
     a.K_new, a.V_new, a.kidx_new = _ptr(K_new), _ptr(V_new), _ptr(kidx_new)
-    a.K_new_stride[:] = _strides(K_new, 2)
-    a.V_new_stride[:] = _strides(V_new, 2)
-    a.kidx_new_stride[:] = _strides(kidx_new, 2)
+    a.K_new_stride[:] = K_new_bg
+    a.V_new_stride[:] = V_new_bg
+    a.kidx_new_stride[:] = X_new_bg
     a.K_pool, a.V_pool, a.kidx_pool = _ptr(K_pool), _ptr(V_pool), _ptr(kidx_pool)
     a.kv_stride[:] = _strides(K_pool, 3)
     a.kidx_stride[:] = _strides(kidx_pool, 3)

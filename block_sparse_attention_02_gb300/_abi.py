@@ -87,6 +87,7 @@ class AppendArgs(C.Structure):
         ("kidx_new", _p), ("kidx_new_stride", _i64x2),
         ("K_pool", _p), ("V_pool", _p), ("kv_stride", _i64x3), ("kidx_pool", _p), ("kidx_stride", _i64x3),
         ("num_pages", C.c_int64), ("seq_pt", _p), ("max_pages", C.c_int64), ("seq_len", _p), ("dev_err", _p),
+        ("T", C.c_int), ("new_t_stride", _i64x3),
     ]
 
 

@@ -378,6 +378,14 @@ msa_status msa_cache_append(const msa_append_args* a, msa_stream_t stream) {
     MSA_REQUIRE(vec_stride_ok(a->K_new_stride[i], 2) && vec_stride_ok(a->V_new_stride[i], 2) &&
                     (vec_stride_ok(a->kidx_new_stride[i], 2) || (i == 1 && a->kidx_new_stride[i] == 0)),
                 MSA_ERR_INVALID_ARG, "new-token strides must be positive multiples of 8 elements");
+  MSA_REQUIRE(a->T >= 0, MSA_ERR_INVALID_ARG, "T = %d", a->T);
+  if (a->T > 1) {
+    MSA_REQUIRE(static_cast<int64_t>(a->B) * a->T * a->Hkv < (int64_t(1) << 33), MSA_ERR_INVALID_ARG,
+                "B*T*Hkv too large");
+    for (int i = 0; i < 3; ++i)
+      MSA_REQUIRE(vec_stride_ok(a->new_t_stride[i], 2), MSA_ERR_INVALID_ARG,
+                  "new_t_stride[%d] = %" PRId64 " must be a positive multiple of 8 elements", i, a->new_t_stride[i]);
+  }
   for (int i = 0; i < 3; ++i)
     MSA_REQUIRE(vec_stride_ok(a->kv_stride[i], 2) &&
                     (vec_stride_ok(a->kidx_stride[i], 2) || (i == 1 && a->kidx_stride[i] == 0)),

@@ -404,6 +404,13 @@ msa_status msa_lse_merge(const float *O_part, const float *LSE_part, int64_t row
  * written.  Pointers and strides must be 16-byte aligned; D and dI multiples of 8.
  * A kidx_pool group stride of 0 (one index-key pool shared by the KV groups,
  * as msa_index_score accepts) stores the index key of group 0 only.
+ * T > 1 appends T tokens per sequence (a prefill chunk, or draft tokens before
+ * a CHUNK-mode call): K_new, V_new [B, T, Hkv, D] and kidx_new [B, T, Hkv, dI]
+ * with the (b, g) strides above and token strides new_t_stride = (K_new,
+ * V_new, kidx_new); token u of sequence b goes to position L_b - T + u.  A
+ * sequence with L_b < T or L_b > max_pages * Bk is not written
+ * (MSA_DEVERR_BAD_LEN); a token whose page id is outside [0, num_pages) is
+ * not written (MSA_DEVERR_BAD_PAGE).  T = 0 means 1.
  * ------------------------------------------------------------------------ */
 typedef struct msa_append_args {
     int B, Hkv, D, dI, Bk;
@@ -423,6 +430,8 @@ typedef struct msa_append_args {
     int64_t max_pages;
     const int32_t *seq_len;
     int32_t *dev_err;
+    int T;                        /* tokens per sequence (0 or 1: one) */
+    int64_t new_t_stride[3];      /* T > 1: token strides of K_new, V_new, kidx_new */
 } msa_append_args;
 
 msa_status msa_cache_append(const msa_append_args *args, msa_stream_t stream);

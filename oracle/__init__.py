@@ -256,30 +256,40 @@ def own_blocks_decode(seq_len, Bk: int):
 
 def cache_append(K_new, V_new, kidx_new, K_pool, V_pool, kidx_pool, seq_pt, seq_len, Bk: int,
                  shared_index: bool = False):
-    """The three pools after token L_b - 1 of every sequence b is written to slot
-    (L_b - 1) % Bk of page seq_pt[b][(L_b - 1) // Bk] (raw 16-bit patterns, copies;
-    the inputs are not modified).  Sequences whose length is outside
-    [1, max_pages * Bk] or whose page id is outside the pool are left out and
-    listed in the returned ``skipped``.  With ``shared_index`` the index-key
-    pool is one pool for all groups and takes group 0's key."""
+    """The three pools after the new tokens of every sequence b are written into
+    their page slots (raw 16-bit patterns, copies; the inputs are not
+    modified).  K_new [B, Hkv, D] is one token per sequence, at position
+    L_b - 1; K_new [B, T, Hkv, D] is T tokens, token u at position L_b - T + u.
+    Position p is slot p % Bk of page seq_pt[b][p // Bk].  A sequence whose
+    length is below T or outside [1, max_pages * Bk] is left out, and so is a
+    token whose page id is outside the pool; ``skipped`` lists the sequences
+    (one token) or the (b, u) tokens (several) left out.  With
+    ``shared_index`` the index-key pool is one pool for all groups and takes
+    group 0's key."""
     K, V, X = _u16(K_pool).copy(), _u16(V_pool).copy(), _u16(kidx_pool).copy()
     kn, vn, xn = _u16(K_new), _u16(V_new), _u16(kidx_new)
+    one = kn.ndim == 3
+    if one:
+        kn, vn, xn = kn[:, None], vn[:, None], xn[:, None]
     pt, sl = _i32(seq_pt), _i32(seq_len)
     P, max_pages = K.shape[0], pt.shape[1]
+    T = kn.shape[1]
     skipped = []
     for b in range(sl.shape[0]):
         L = int(sl[b])
-        if L < 1 or L > max_pages * Bk:
-            skipped.append(b)
+        if L < T or L < 1 or L > max_pages * Bk:
+            skipped += [b] if one else [(b, u) for u in range(T)]
             continue
-        page = int(pt[b, (L - 1) // Bk])
-        if page < 0 or page >= P:
-            skipped.append(b)
-            continue
-        t = (L - 1) % Bk
-        K[page, :, t, :] = kn[b]
-        V[page, :, t, :] = vn[b]
-        X[page, :, t, :] = xn[b] if not shared_index else xn[b, 0]
+        for u in range(T):
+            pos = L - T + u
+            page = int(pt[b, pos // Bk])
+            if page < 0 or page >= P:
+                skipped.append(b if one else (b, u))
+                continue
+            t = pos % Bk
+            K[page, :, t, :] = kn[b, u]
+            V[page, :, t, :] = vn[b, u]
+            X[page, :, t, :] = xn[b, u] if not shared_index else xn[b, u, 0]
     return K, V, X, skipped
 
 

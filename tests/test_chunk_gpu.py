@@ -154,3 +154,66 @@ def test_chunk_rejected_sequence_and_page(msa):
     bufs = run_chunk(msa, bad, wl.shape.k, expect_err=msa.MSA_DEVERR_BAD_PAGE)
     for name in ("count", "sel", "O", "LSE"):
         assert torch.equal(bufs[name][0], good[name][0]) and torch.equal(bufs[name][1], good[name][1]), name
+
+
+def _bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("shared", [False, True], ids=["per_group", "shared_index_pool"])
+def test_chunk_append_then_layer(msa, shared):
+    """The chunk's own tokens, cleared from the pages and appended back with one
+    msa_cache_append call (T = S tokens per sequence, crossing page
+    boundaries), restore the pools bit for bit (the oracle's copies agree), and
+    the layer over them gives the same bits as before."""
+    wl = ChunkWorkload("append", prefix=(300, 1000, 127), S=200, shape=MSAShape(Hq=12, Hkv=2, k=4), seed=71)
+    inp = chunk_inputs(wl, device="cuda")
+    if shared:
+        inp["kidx_pool"] = inp["kidx_pool"][:, :1].expand(-1, wl.shape.Hkv, -1, -1)
+    ref = run_chunk(msa, inp, wl.shape.k)
+    pos = inp["q_pos"].long()[:, None] + torch.arange(wl.S, device="cuda")[None, :]
+    pages = torch.gather(inp["seq_pt"].long(), 1, pos // wl.shape.Bk)
+    slots = pos % wl.shape.Bk
+    names = ("K_pool", "V_pool", "kidx_pool")
+    new = [inp[n][pages, :, slots].contiguous() for n in names]       # [B, S, Hkv, d]
+    cleared = {n: inp[n].clone() if not (shared and n == "kidx_pool") else inp[n][:, :1].clone() for n in names}
+    for n in names:
+        cleared[n][pages, :, slots] = 0
+    if shared:
+        cleared["kidx_pool"] = cleared["kidx_pool"].expand(-1, wl.shape.Hkv, -1, -1)
+    want = oracle.cache_append(*[t.cpu() for t in new], *[cleared[n].cpu() for n in names], inp["seq_pt"].cpu(),
+                               inp["seq_len"].cpu(), wl.shape.Bk, shared_index=shared)
+    assert want[3] == []
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    msa.msa_cache_append(*new, *[cleared[n] for n in names], inp["seq_pt"], inp["seq_len"], dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for n, w in zip(names, want[:3]):
+        assert np.array_equal(_bits(cleared[n]), w), n
+        assert torch.equal(cleared[n], inp[n]), n
+    got = run_chunk(msa, dict(inp, **cleared), wl.shape.k)
+    for name in ("C", "sel", "count", "O", "LSE"):
+        assert torch.equal(got[name], ref[name]), name
+
+
+def test_chunk_append_rejects_short_sequence_and_bad_page(msa):
+    """A sequence shorter than T writes nothing (MSA_DEVERR_BAD_LEN); a token
+    whose page id is outside the pool is skipped alone (MSA_DEVERR_BAD_PAGE);
+    the pools match the oracle's copies bit for bit."""
+    g = torch.Generator(device="cuda").manual_seed(72)
+    P, Hkv, D_, dI_, mp, T = 32, 2, 128, 64, 4, 5
+    seq_len = torch.tensor([3, 130, 300, 129], dtype=torch.int32, device="cuda")
+    B = seq_len.shape[0]
+    pools = [torch.randn(P, Hkv, 128, d, generator=g, device="cuda").to(torch.bfloat16) for d in (D_, D_, dI_)]
+    new = [torch.randn(B, T, Hkv, d, generator=g, device="cuda").to(torch.bfloat16) for d in (D_, D_, dI_)]
+    seq_pt = torch.randperm(P, generator=g, device="cuda")[: B * mp].view(B, mp).to(torch.int32).contiguous()
+    seq_pt[3, 1] = P + 9                                  # position 128 of sequence 3: no such page
+    K2, V2, X2, skipped = oracle.cache_append(*[t.cpu() for t in new], *[t.cpu() for t in pools], seq_pt.cpu(),
+                                              seq_len.cpu(), 128)
+    assert skipped == [(0, u) for u in range(T)] + [(3, 4)]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    msa.msa_cache_append(*new, *pools, seq_pt, seq_len, dev_err=err)
+    torch.cuda.synchronize()
+    for got, want in zip(pools, (K2, V2, X2)):
+        assert np.array_equal(_bits(got), want)
+    assert int(err.item()) == msa.MSA_DEVERR_BAD_LEN | msa.MSA_DEVERR_BAD_PAGE

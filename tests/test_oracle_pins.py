@@ -408,6 +408,39 @@ def test_cache_append_slots_by_hand():
     assert not K2[~written].any() and not V2[~written].any() and not X2[~written].any()
 
 
+def test_cache_append_tokens_by_hand():
+    """T = 3 tokens per sequence land at positions L-3, L-2, L-1: lengths 5, 130
+    and 256 give (page, slot) pairs worked out by hand across page boundaries;
+    a length below T skips the sequence, and a token whose page id is outside
+    the pool is skipped alone."""
+    P, Hkv, Bk, D, dI, T = 8, 2, 128, 16, 8, 3
+    K = np.zeros((P, Hkv, Bk, D), dtype=np.uint16)
+    V = np.zeros((P, Hkv, Bk, D), dtype=np.uint16)
+    X = np.zeros((P, Hkv, Bk, dI), dtype=np.uint16)
+    seq_pt = np.array([[5, 1, 2], [3, 0, 4], [6, 7, 2], [2, 4, 1], [0, 99, 3]], dtype=np.int32)
+    seq_len = np.array([5, 130, 256, 2, 129], dtype=np.int32)
+    B = seq_len.shape[0]
+    kn = (np.arange(B * T * Hkv * D, dtype=np.uint16) + 1).reshape(B, T, Hkv, D)
+    vn = (np.arange(B * T * Hkv * D, dtype=np.uint16) + 3000).reshape(B, T, Hkv, D)
+    xn = (np.arange(B * T * Hkv * dI, dtype=np.uint16) + 7000).reshape(B, T, Hkv, dI)
+    K2, V2, X2, skipped = oracle.cache_append(kn, vn, xn, K, V, X, seq_pt, seq_len, Bk)
+    # b = 3: length 2 < T; b = 4: positions 126, 127 on page 0, position 128 on page 99 (outside)
+    assert skipped == [(3, 0), (3, 1), (3, 2), (4, 2)]
+    expect = {(0, 0): (5, 2), (0, 1): (5, 3), (0, 2): (5, 4),          # positions 2, 3, 4
+              (1, 0): (3, 127), (1, 1): (0, 0), (1, 2): (0, 1),        # positions 127, 128, 129
+              (2, 0): (7, 125), (2, 1): (7, 126), (2, 2): (7, 127),    # positions 253, 254, 255
+              (4, 0): (0, 126), (4, 1): (0, 127)}                      # positions 126, 127
+    for (b, u), (page, t) in expect.items():
+        for g in range(Hkv):
+            assert np.array_equal(K2[page, g, t], kn[b, u, g])
+            assert np.array_equal(V2[page, g, t], vn[b, u, g])
+            assert np.array_equal(X2[page, g, t], xn[b, u, g])
+    written = np.zeros((P, Hkv, Bk), dtype=bool)
+    for page, t in expect.values():
+        written[page, :, t] = True
+    assert not K2[~written].any() and not V2[~written].any() and not X2[~written].any()
+
+
 def _paged(x, perm, Bk):
     """[B, T, Hkv, X] -> page pool [B * ceil(T/Bk), Hkv, Bk, X] (zero tail) and
     seq_pt [B, ceil(T/Bk)]: block j of sequence b goes to page perm[b*n + j]."""
