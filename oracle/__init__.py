@@ -34,12 +34,10 @@ Functions and the passages they follow (page title and passage):
   the serving command's 8,192-token prefill chunks; the serving post's
   measurement paragraph, a 60,000-token cached prefix), and with a small S the
   decode of several tokens per sequence (the M2-report article names
-  multi-token prediction for speculative decoding).  No new arithmetic: the
-  cached tokens are gathered out of the pages (``gather_pages``), the chunk's
-  queries are placed at their positions of the whole context
-  (``place_chunk``), and the prefill step functions above run on the chunk's
-  rows only -- a query at position p sees exactly what query p of a prefill of
-  the whole context sees.
+  multi-token prediction for speculative decoding).  No new arithmetic: a
+  chunk query at position p sees exactly what a decode query of a sequence of
+  length p + 1 sees over the same pages, so query offset s of every sequence
+  is one call of the decode step functions above with lengths q_pos[b] + s + 1.
 """
 from __future__ import annotations
 
@@ -293,55 +291,15 @@ def cache_append(K_new, V_new, kidx_new, K_pool, V_pool, kidx_pool, seq_pt, seq_
     return K, V, X, skipped
 
 
-def gather_pages(pool, seq_pt, lengths, Bk: int):
-    """Dense [B, T, Hkv, X] copy (raw 16-bit patterns) of the first lengths[b]
-    tokens of every sequence b in a page pool [P, Hkv, Bk, X]: token t is slot
-    t % Bk of page seq_pt[b][t // Bk].  T = max length; zeros past a sequence's
-    end.  Data movement only."""
-    pool_, pt, L = _u16(pool), _i32(seq_pt), _i64(lengths)
-    B = pt.shape[0]
-    T = int(L.max()) if B else 0
-    out = np.zeros((B, T) + pool_.shape[1:2] + pool_.shape[3:], dtype=np.uint16)
-    for b in range(B):
-        t = np.arange(int(L[b]))
-        out[b, :len(t)] = pool_[pt[b, t // Bk], :, t % Bk]
-    return out
-
-
-def place_chunk(x, q_pos, T: int):
-    """The chunk tensor x [B, S, ...] copied to rows q_pos[b] .. q_pos[b] + S - 1
-    of a zero [B, T, ...] tensor (same dtype; raw copies)."""
-    a, qp = _np(x), _i64(q_pos)
-    B, S = a.shape[:2]
-    out = np.zeros((B, T) + a.shape[2:], dtype=a.dtype)
-    for b in range(B):
-        out[b, qp[b]:qp[b] + S] = a[b]
-    return out
-
-
-def chunk_rows(q_pos, S: int, T: int):
-    """Flattened context rows b*T + q_pos[b] + s of the chunk's queries, in
-    [B, S] order (index bookkeeping)."""
-    qp = _i64(q_pos)
-    return (np.arange(len(qp), dtype=np.int64)[:, None] * T + qp[:, None] + np.arange(S)[None, :]).reshape(-1)
-
-
-def _chunk_context(seq_pt, q_pos, S: int, Bk: int, pools):
-    qp = _i64(q_pos)
-    lengths = qp + S
-    T = int(lengths.max())
-    return qp, T, [gather_pages(x, seq_pt, lengths, Bk) for x in pools]
-
-
 def chunk_scores(q_idx, w, kidx_pool, seq_pt, q_pos, Bk: int = 128):
     """Block scores C [B, S, Hkv, nbT] (fp64) of a chunk's queries at positions
-    q_pos[b] + s over the paged index keys (nbT = blocks of the longest context)."""
-    qi = _u16(q_idx)
+    q_pos[b] + s over the paged index keys (nbT = blocks of the longest
+    context): offset s is the decode score of a sequence of length q_pos[b] + s + 1."""
+    qi, ww, qp = _u16(q_idx), _f32(w), _i64(q_pos)
     B, S = qi.shape[:2]
-    qp, T, (Xd,) = _chunk_context(seq_pt, q_pos, S, Bk, [kidx_pool])
-    rows = chunk_rows(qp, S, T)
-    Cs = prefill_scores(place_chunk(qi, qp, T), Xd, place_chunk(_f32(w), qp, T), Bk, rows)
-    return Cs.reshape(B, S, Cs.shape[1], Cs.shape[2])
+    nbT = int(((qp + S - 1) // Bk).max()) + 1
+    return np.stack([decode_scores(qi[:, s], ww[:, s], kidx_pool, seq_pt, (qp + s + 1).astype(np.int32), nbT)
+                     for s in range(S)], axis=1)
 
 
 def chunk_own_blocks(q_pos, S: int, Bk: int = 128):
@@ -352,15 +310,13 @@ def chunk_own_blocks(q_pos, S: int, Bk: int = 128):
 
 def chunk_attend(Q, K_pool, V_pool, seq_pt, q_pos, sel, count, scale: float, Bk: int = 128):
     """Attention of a chunk's queries over the given selection (sel [B,S,Hkv,k],
-    count [B,S,Hkv]).  Returns O [B,S,Hq,D], LSE [B,S,Hq] (fp64)."""
-    q = _u16(Q)
-    B, S = q.shape[:2]
-    qp, T, (Kd, Vd) = _chunk_context(seq_pt, q_pos, S, Bk, [K_pool, V_pool])
-    s, c = _i32(sel), _i32(count)
-    rows = chunk_rows(qp, S, T)
-    O, LSE = prefill_attend(place_chunk(q, qp, T), Kd, Vd, s.reshape(B * S, *s.shape[2:]),
-                            c.reshape(B * S, -1), Bk, scale, rows)
-    return O.reshape(B, S, *O.shape[1:]), LSE.reshape(B, S, -1)
+    count [B,S,Hkv]): offset s is the decode attention of a sequence of length
+    q_pos[b] + s + 1.  Returns O [B,S,Hq,D], LSE [B,S,Hq] (fp64)."""
+    q, qp, sl, c = _u16(Q), _i64(q_pos), _i32(sel), _i32(count)
+    S = q.shape[1]
+    outs = [decode_attend(q[:, s], K_pool, V_pool, seq_pt, (qp + s + 1).astype(np.int32), sl[:, s], c[:, s], scale)
+            for s in range(S)]
+    return np.stack([o for o, _ in outs], axis=1), np.stack([l for _, l in outs], axis=1)
 
 
 def chunk_layer(Q, q_idx, w, K_pool, V_pool, kidx_pool, seq_pt, q_pos, k: int, scale: float, Bk: int = 128):

@@ -485,23 +485,38 @@ def test_chunk_layer_equals_prefill_rows(q_pos, S):
     assert np.array_equal(r["O"].reshape(O.shape), O) and np.array_equal(r["LSE"].reshape(LSE.shape), LSE)
 
 
-def test_chunk_layer_single_token_equals_decode():
-    """A one-token chunk at position L_b - 1 is a decode step: the decode
-    oracle, which reads the pages itself, gives the same scores, selection and
-    attention."""
-    sh = MSAShape(Hq=12, Hkv=2, k=4)
-    wl = ChunkWorkload("pin_chunk_decode", prefix=(1000, 129, 4000), S=1, shape=sh, seed=92)
+def test_chunk_layer_brute_force_numpy():
+    """Every block score and the attention of a few chunk queries, written out
+    in numpy from the definitions with explicit page reads (token t of sequence
+    b is slot t % Bk of page seq_pt[b][t // Bk]), against the chunk oracle."""
+    sh = MSAShape(Hq=6, Hkv=2, HI=2, k=3)
+    wl = ChunkWorkload("pin_chunk_numpy", prefix=(130, 5, 383), S=3, shape=sh, seed=93)
     inp = chunk_inputs(wl)
     scale = 1 / math.sqrt(sh.D)
     r = oracle.chunk_layer(inp["Q"], inp["q_idx"], inp["w"], inp["K_pool"], inp["V_pool"], inp["kidx_pool"],
                            inp["seq_pt"], inp["q_pos"], sh.k, scale, sh.Bk)
-    Cd = oracle.decode_scores(inp["q_idx"][:, 0], inp["w"][:, 0], inp["kidx_pool"], inp["seq_pt"], inp["seq_len"])
-    nbc = r["C"].shape[-1]
-    assert np.allclose(r["C"][:, 0], Cd[:, :, :nbc], rtol=1e-12, atol=0)
-    own = np.repeat(oracle.own_blocks_decode(inp["seq_len"], sh.Bk), sh.Hkv).reshape(wl.B, sh.Hkv)
-    sel, cnt, _, _ = oracle.select(Cd, own, sh.k)
-    assert np.array_equal(r["sel"][:, 0], sel) and np.array_equal(r["count"][:, 0], cnt)
-    O, LSE = oracle.decode_attend(inp["Q"][:, 0], inp["K_pool"], inp["V_pool"], inp["seq_pt"], inp["seq_len"],
-                                  sel, cnt, scale)
-    assert np.allclose(r["O"][:, 0], O, rtol=1e-12, atol=1e-15)
-    assert np.allclose(r["LSE"][:, 0], LSE, rtol=1e-12, atol=0)
+    qi, w, Q = f64(inp["q_idx"]), f64(inp["w"]), f64(inp["Q"])
+    Kp, Vp, Xp = f64(inp["K_pool"]), f64(inp["V_pool"]), f64(inp["kidx_pool"])
+    pt = inp["seq_pt"].numpy()
+    for b in range(wl.B):
+        for s in range(wl.S):
+            p = wl.prefix[b] + s
+            own = p // sh.Bk
+            for g in range(sh.Hkv):
+                c = np.full(r["C"].shape[-1], -np.inf)
+                for j in range(own):
+                    keys = Xp[pt[b, j], g]                               # [Bk, dI]
+                    st = sum(w[b, s, g, h] * np.maximum(keys @ qi[b, s, g, h], 0.0) for h in range(sh.HI))
+                    c[j] = st.max()
+                assert np.allclose(r["C"][b, s, g], c, rtol=1e-12, atol=0) and \
+                    np.array_equal(np.isneginf(r["C"][b, s, g]), np.isneginf(c))
+                ts = [t for j in r["sel"][b, s, g] if j >= 0 for t in range(j * sh.Bk, (j + 1) * sh.Bk) if t <= p]
+                Kt = np.stack([Kp[pt[b, t // sh.Bk], g, t % sh.Bk] for t in ts])
+                Vt = np.stack([Vp[pt[b, t // sh.Bk], g, t % sh.Bk] for t in ts])
+                for hh in range(sh.G):
+                    hq = g * sh.G + hh
+                    z = scale * (Kt @ Q[b, s, hq])
+                    m = z.max()
+                    e = np.exp(z - m)
+                    assert np.allclose(r["O"][b, s, hq], e @ Vt / e.sum(), rtol=1e-10, atol=1e-13)
+                    assert abs(r["LSE"][b, s, hq] - (m + math.log(e.sum()))) < 1e-10
