@@ -25,7 +25,9 @@ bounded sample of the same workload on the host cores.
 
 ``--impl reference`` times the oracle itself (the only reference this method
 has: the pages ship no code) on the same workload and prints the same line
-with "impl": "reference".  Under torchrun only rank 0 runs it.
+with "impl": "reference": whole decode steps, or, for the prefill and chunk
+layers, bounded samples of each layer (uniformly drawn query rows; the first
+query offsets of a chunk).  Under torchrun only rank 0 runs it.
 
 ``--workload prefill_s131072`` times one prefill layer instead (tokens/s =
 B*S per layer), with the tensor-core roofline of the sparse attention.
@@ -454,6 +456,50 @@ def cpu_decode_baseline(wl, inp_host, budget_s: float, min_steps: int = 1):
             "sample": f"{steps} full decode step(s) of {wl.name} (B={wl.B}) in {dt:.1f} s"}
 
 
+def cpu_prefill_baseline(wl, inp_host, budget_s: float, seed: int = 0):
+    """The oracle's prefill layer (scores, selection, attention) on query rows
+    drawn uniformly from the layer, 16 at a time, until the time budget is
+    used: tokens/s = rows / time (a uniform sample has the layer's mean cost
+    per query)."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    sh = wl.shape
+    rng = np.random.default_rng(seed)
+    t0 = time.perf_counter()
+    n = 0
+    while n == 0 or time.perf_counter() - t0 < budget_s:
+        rows = np.sort(rng.integers(0, wl.B * wl.S, 16)).astype(np.int64)
+        C = oracle.prefill_scores(inp_host["q_idx"], inp_host["k_idx"], inp_host["w"], sh.Bk, rows)
+        own = np.repeat(oracle.own_blocks_prefill(wl.S, sh.Bk, rows), sh.Hkv).reshape(-1, sh.Hkv)
+        sel, cnt, _, _ = oracle.select(C, own, sh.k)
+        oracle.prefill_attend(inp_host["Q"], inp_host["K"], inp_host["V"], sel, cnt, sh.Bk, 1.0 / math.sqrt(sh.D),
+                              rows)
+        n += len(rows)
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n} query rows of {wl.name} drawn uniformly (all heads and groups) in {dt:.1f} s"}
+
+
+def cpu_chunk_baseline(wl, inp_host, budget_s: float):
+    """The oracle's chunk layer on the chunk's first query offsets (every
+    sequence, one offset at a time) until the time budget is used."""
+    import oracle
+    oracle.build()
+    sh = wl.shape
+    t0 = time.perf_counter()
+    n = 0
+    while n < wl.S and (n == 0 or time.perf_counter() - t0 < budget_s):
+        part = {x: inp_host[x][:, n:n + 1] for x in ("Q", "q_idx", "w")}
+        oracle.chunk_layer(part["Q"], part["q_idx"], part["w"], inp_host["K_pool"], inp_host["V_pool"],
+                           inp_host["kidx_pool"], inp_host["seq_pt"], inp_host["q_pos"] + n, sh.k,
+                           1.0 / math.sqrt(sh.D), sh.Bk)
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": wl.B * n / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"the first {n} of {wl.S} query offsets of {wl.name} (B={wl.B}) in {dt:.1f} s"}
+
+
 # ---------------------------------------------------------------------------
 # prefill workload (optional)
 # ---------------------------------------------------------------------------
@@ -679,27 +725,47 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        if not isinstance(wl, DecodeWorkload):
-            print(json.dumps({"impl": "reference", "unavailable": "reference arm implemented for decode workloads"}))
-            return
-        from workloads import decode_inputs
-        h = decode_inputs(wl, device="cpu")
         import oracle
         oracle.build()
-        for _ in range(args.warmup):
-            oracle_decode_step(h, wl.shape)
-        t0 = time.perf_counter()
-        for _ in range(args.steps):
-            oracle_decode_step(h, wl.shape)
-        dt = time.perf_counter() - t0
-        val = wl.B * args.steps / dt
+        if isinstance(wl, DecodeWorkload):
+            from workloads import decode_inputs
+            h = decode_inputs(wl, device="cpu")
+            for _ in range(args.warmup):
+                oracle_decode_step(h, wl.shape)
+            t0 = time.perf_counter()
+            for _ in range(args.steps):
+                oracle_decode_step(h, wl.shape)
+            dt = time.perf_counter() - t0
+            val = wl.B * args.steps / dt
+            cfg = {"workload": wl.name, "batch": wl.B, "context": wl.lengths[0]}
+            base = {"value": val, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                    "sample": f"{args.steps} full decode steps of {wl.name}"}
+            ms = dt / args.steps * 1e3
+        else:
+            # prefill and chunk layers: each step is a bounded sample of the layer
+            budget = args.cpu_budget_s / max(1, args.steps + args.warmup)
+            if isinstance(wl, ChunkWorkload):
+                from workloads import chunk_inputs
+                h = chunk_inputs(wl, device="cpu")
+                run = lambda: cpu_chunk_baseline(wl, h, budget)
+                cfg = {"workload": wl.name, "batch": wl.B, "chunk": wl.S, "cached_prefix": wl.prefix[0]}
+            else:
+                from workloads import prefill_inputs
+                h = prefill_inputs(wl, device="cpu")
+                run = lambda: cpu_prefill_baseline(wl, h, budget)
+                cfg = {"workload": wl.name, "batch": wl.B, "seq_len": wl.S}
+            for _ in range(args.warmup):
+                run()
+            samples = [run() for _ in range(args.steps)]
+            val = statistics.mean(x["value"] for x in samples)
+            base = dict(samples[-1], value=val)
+            base["sample"] = f"{args.steps} steps, each: " + samples[-1]["sample"]
+            ms = wl.B * wl.S / val * 1e3
         print(json.dumps({
             "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "batch": wl.B, "context": wl.lengths[0]},
-            "cpu_baseline": {"value": val, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-                             "sample": f"{args.steps} full decode steps of {wl.name}"},
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+            "cpu_baseline": base,
             "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         }))
         return
@@ -714,9 +780,14 @@ def main():
         res, host_in, inp = run_chunk_ours(args, wl, world, rank)
     else:
         res, host_in, inp = run_prefill_ours(args, wl, world, rank)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and isinstance(wl, DecodeWorkload):
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         h = {n: t.cpu() for n, t in inp.items()}
-        res["cpu_baseline"] = cpu_decode_baseline(wl, h, args.cpu_budget_s)
+        if isinstance(wl, DecodeWorkload):
+            res["cpu_baseline"] = cpu_decode_baseline(wl, h, args.cpu_budget_s)
+        elif isinstance(wl, ChunkWorkload):
+            res["cpu_baseline"] = cpu_chunk_baseline(wl, h, args.cpu_budget_s)
+        else:
+            res["cpu_baseline"] = cpu_prefill_baseline(wl, h, args.cpu_budget_s)
     elif rank == 0:
         res["cpu_baseline"] = None
     if rank == 0:
