@@ -13,7 +13,8 @@ Functions and the passages they follow (page title and passage):
 
 * ``prefill_scores`` / ``decode_scores`` -- block scores of the Index Branch
   ("MiniMax M3: Como la atencion dispersa hace practicos a los agentes de largo
-  alcance", MSA paragraph and figure caption); formula fixed by this build:
+  alcance", MSA paragraph and figure caption); the pages print no formula, the
+  library and this oracle both take:
   s_t = sum_h w_h ReLU(q_idx_h . k_idx_t), c_j = max over block j.
 * ``select`` -- own block + top-(k-1) earlier blocks by (score desc, index asc)
   (same page, bullet "Costo predecible": Bk = 128, k = 16).

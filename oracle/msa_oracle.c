@@ -23,7 +23,7 @@
  *
  *   1. index score.  A light Index Branch scores the context in blocks
  *      ([agents], MSA paragraph and caption).  The pages never print the
- *      formula; this build fixes it once for both paths:
+ *      formula; the library and this oracle both take:
  *          s_t = sum_h w_h * ReLU(q_idx_h . k_idx_t)
  *          c_j = max over the tokens t of block j of s_t
  *      Only blocks strictly before the query's own block are scored; the own
