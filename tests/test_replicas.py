@@ -3,8 +3,9 @@
 The MSA hot path shards by sequence (decode) or by KV group with no collective
 in the data path; bench.py runs one replica per GPU and only aggregates timings
 (barrier + max over ranks).  Here two gloo processes check that aggregation and
-that a decode batch split by sequence across ranks gives exactly the results of
-the unsplit batch (computed with the oracle, all-gathered only for the check).
+that a decode batch and a chunk batch (several queries per sequence over the
+paged cache) split by sequence across ranks give exactly the results of the
+unsplit batches (computed with the oracle, all-gathered only for the check).
 """
 import math
 import os
@@ -34,7 +35,7 @@ def _worker(rank, world, port, out_dir):
     dist.init_process_group("gloo", rank=rank, world_size=world)
     import bench
     import oracle
-    from workloads import DecodeWorkload, MSAShape, decode_inputs
+    from workloads import ChunkWorkload, DecodeWorkload, MSAShape, chunk_inputs, decode_inputs
 
     # timing aggregation: every rank sees the max
     mx = bench.max_over_ranks(float(10 + rank), world)
@@ -51,12 +52,25 @@ def _worker(rank, world, port, out_dir):
                                 1.0 / math.sqrt(wl.shape.D))
     gathered = [None] * world
     dist.all_gather_object(gathered, (mine, O))
+    # chunk batch sharded the same way
+    cw = ChunkWorkload("replica_chunk", prefix=(300, 1000, 129, 40), S=3, shape=MSAShape(Hq=12, Hkv=2, k=4), seed=72)
+    cin = chunk_inputs(cw)
+    cmine = list(range(rank, cw.B, world))
+    r = oracle.chunk_layer(cin["Q"][cmine], cin["q_idx"][cmine], cin["w"][cmine], cin["K_pool"], cin["V_pool"],
+                           cin["kidx_pool"], cin["seq_pt"][cmine], cin["q_pos"][cmine], cw.shape.k,
+                           1.0 / math.sqrt(cw.shape.D), cw.shape.Bk)
+    cgathered = [None] * world
+    dist.all_gather_object(cgathered, (cmine, r["O"]))
     if rank == 0:
         np.save(os.path.join(out_dir, "max.npy"), np.array([mx]))
         full = np.zeros((wl.B,) + O.shape[1:])
         for idx, o in gathered:
             full[idx] = o
         np.save(os.path.join(out_dir, "sharded.npy"), full)
+        cfull = np.zeros((cw.B,) + r["O"].shape[1:])
+        for idx, o in cgathered:
+            cfull[idx] = o
+        np.save(os.path.join(out_dir, "sharded_chunk.npy"), cfull)
     dist.barrier()
     dist.destroy_process_group()
 
@@ -67,7 +81,7 @@ def test_two_rank_replicas(tmp_path):
     assert float(np.load(tmp_path / "max.npy")[0]) == 11.0
     sys.path.insert(0, ROOT)
     import oracle
-    from workloads import DecodeWorkload, MSAShape, decode_inputs
+    from workloads import ChunkWorkload, DecodeWorkload, MSAShape, chunk_inputs, decode_inputs
     wl = DecodeWorkload("replica", lengths=(300, 1000, 2049, 129), shape=MSAShape(Hq=12, Hkv=2, k=4), seed=71)
     inp = decode_inputs(wl)
     C = oracle.decode_scores(inp["q_idx"], inp["w"], inp["kidx_pool"], inp["seq_pt"], inp["seq_len"])
@@ -76,3 +90,8 @@ def test_two_rank_replicas(tmp_path):
     O, _ = oracle.decode_attend(inp["Q"], inp["K_pool"], inp["V_pool"], inp["seq_pt"], inp["seq_len"], sel, cnt,
                                 1.0 / math.sqrt(wl.shape.D))
     np.testing.assert_array_equal(np.load(tmp_path / "sharded.npy"), O)
+    cw = ChunkWorkload("replica_chunk", prefix=(300, 1000, 129, 40), S=3, shape=MSAShape(Hq=12, Hkv=2, k=4), seed=72)
+    cin = chunk_inputs(cw)
+    r = oracle.chunk_layer(cin["Q"], cin["q_idx"], cin["w"], cin["K_pool"], cin["V_pool"], cin["kidx_pool"],
+                           cin["seq_pt"], cin["q_pos"], cw.shape.k, 1.0 / math.sqrt(cw.shape.D), cw.shape.Bk)
+    np.testing.assert_array_equal(np.load(tmp_path / "sharded_chunk.npy"), r["O"])
