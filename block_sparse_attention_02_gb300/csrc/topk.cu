@@ -45,9 +45,12 @@ __device__ __forceinline__ RowInfo row_info(const msa_topk_args& a, int64_t row)
     const int64_t g = row % a.Hkv, bs = row / a.Hkv;
     const int64_t s = bs % a.S, b = bs / a.S;
     r.c = a.C + b * a.C_stride[0] + s * a.C_stride[1] + g * a.C_stride[2];
-    // a chunk's query s sits at position q_pos[b] + s
-    const int64_t pos = a.mode == MSA_MODE_CHUNK ? a.q_pos[b] + s : s;
-    r.valid = pos >= 0 && pos / a.Bk < a.nb_stride;
+    // a chunk's query s sits at position q_pos[b] + s; a chunk sequence is
+    // rejected as a whole (as the index score does) when it starts before 0 or
+    // its last query's own block is not below nb_stride
+    const int64_t q0 = a.mode == MSA_MODE_CHUNK ? a.q_pos[b] : 0;
+    const int64_t pos = q0 + s;
+    r.valid = q0 >= 0 && (q0 + a.S - 1) / a.Bk < a.nb_stride;
     r.own = r.valid ? static_cast<int>(pos / a.Bk) : 0;
   } else {
     const int64_t g = row % a.Hkv, b = row / a.Hkv;

@@ -194,8 +194,9 @@ msa_status msa_index_score(const msa_index_args *args, msa_stream_t stream);
  *   DECODE rows (b, g): own block (seq_len[b] - 1) / Bk.  C strides (b, g, -).
  *     sel [B, Hkv, k] int32, count [B, Hkv] int32 (dense).
  *   CHUNK rows (b, s, g): own block (q_pos[b] + s) / Bk; C, sel and count as
- *     in PREFILL.  A sequence with q_pos[b] < 0 or an own block not below
- *     nb_stride gets count 0, all -1 selections and MSA_DEVERR_BAD_LEN.
+ *     in PREFILL.  A sequence with q_pos[b] < 0, or whose last query's own
+ *     block (q_pos[b] + S - 1) / Bk is not below nb_stride, gets count 0 and
+ *     all -1 selections in every row, and MSA_DEVERR_BAD_LEN.
  * Scores are compared as fp32 (-0 equals +0); NaN scores rank below -inf.
  * A decode row whose length is outside [1, nb_stride * Bk] gets count 0, an
  * all -1 selection and MSA_DEVERR_BAD_LEN.
