@@ -197,6 +197,11 @@ msa_status msa_index_score(const msa_index_args* a, msa_stream_t stream) {
                   "num_pages = %" PRId64, a->num_pages);
       MSA_REQUIRE(a->max_pages >= 1 && a->max_pages < (int64_t(1) << 31) / a->Bk, MSA_ERR_INVALID_ARG,
                   "max_pages = %" PRId64, a->max_pages);
+      // no block lies past the page table, and with this bound the index score
+      // and the top-k reject exactly the same sequences (a last own block at
+      // or past nb_stride)
+      MSA_REQUIRE(a->nb_stride <= a->max_pages, MSA_ERR_INVALID_ARG,
+                  "chunk: nb_stride = %d exceeds max_pages = %" PRId64, a->nb_stride, a->max_pages);
     }
     for (int i = 0; i < 3; ++i)
       MSA_REQUIRE(a->w_stride[i] > 0 && a->C_stride[i] > 0, MSA_ERR_INVALID_ARG, "w / C strides must be positive");

@@ -354,12 +354,20 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
       if (!__all_sync(0xffffffffu, mbar_wait(&bar_kempty[kr.st], kr.ph ^ 1, abort_flag, p.dev_err))) return false;
       if (leader) {
         const int gk = p.kgroups ? it.g : 0;
-        mbar_arrive_expect_tx(&bar_kfull[kr.st], kKTile);
-        if constexpr (CHUNK) {   // page of block j; an out-of-range id reads zeros and is reported
+        if constexpr (CHUNK) {
+          // page of block j.  An id outside the pool is reported and not
+          // loaded: the stage completes with a plain arrive, the MMA runs on
+          // whatever the stage held, and the epilogue stores -inf for the block.
           const int page = p.seq_pt[it.b * p.max_pages + j];
-          if (page < 0 || page >= p.num_pages) report(p.dev_err, MSA_DEVERR_BAD_PAGE);
-          tma_load_4d(s_k + kr.st * kKTile, &kmap, &bar_kfull[kr.st], 0, 0, gk, page);
+          if (page < 0 || page >= p.num_pages) {
+            report(p.dev_err, MSA_DEVERR_BAD_PAGE);
+            mbar_arrive(&bar_kfull[kr.st]);
+          } else {
+            mbar_arrive_expect_tx(&bar_kfull[kr.st], kKTile);
+            tma_load_4d(s_k + kr.st * kKTile, &kmap, &bar_kfull[kr.st], 0, 0, gk, page);
+          }
         } else {
+          mbar_arrive_expect_tx(&bar_kfull[kr.st], kKTile);
           tma_load_4d(s_k + kr.st * kKTile, &kmap, &bar_kfull[kr.st], 0, gk, j * kBk, it.b);
         }
       }
@@ -532,13 +540,21 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
           named_bar_sync(bar_id, 128);
           // staged blocks j0 .. j (s_cst column = block mod kFlush)
           const int jal = j - j % kFlush, j0 = max(it.jb, jal), cnt = j - j0 + 1;
+          // a chunk's block whose page id is outside the pool was not loaded: -inf
+          bool badpg = false;
+          if constexpr (CHUNK) {
+            if (lane < cnt) {
+              const int pg = p.seq_pt[it.b * p.max_pages + j0 + lane];
+              badpg = pg < 0 || pg >= p.num_pages;
+            }
+          }
           for (int rr = 0; rr < kQW / 4; ++rr) {     // warp q4: query rows q0 + 8 q4 .. q0 + 8 q4 + 7
             const int qrow = q0 + q4 * (kQW / 4) + rr;
             const int i = it.qb * kQB + qrow;
             // a query before the item's last own block has its own block among the passes: -inf
             if (i < p.S && lane < cnt)
               p.C[it.b * p.cs0 + static_cast<int64_t>(i) * p.cs1 + it.g * p.cs2 + j0 + lane] =
-                  j0 + lane < (pos0 + i) / kBk ? s_cst[sl][qrow][j0 - jal + lane] : -INFINITY;
+                  (j0 + lane < (pos0 + i) / kBk && !badpg) ? s_cst[sl][qrow][j0 - jal + lane] : -INFINITY;
           }
         }
       }

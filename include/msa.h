@@ -131,12 +131,14 @@ const char *msa_status_string(msa_status s);
  *   strides, S = queries per sequence); index keys in pages as in DECODE
  *   (k_idx page pool, num_pages, seq_pt, max_pages; group stride 0 allowed).
  *   q_pos [B] int32: absolute position of query 0 of sequence b.  Query s has
- *   own block (q_pos[b] + s) / Bk and scores the blocks before it; nb_stride >=
- *   max over b of ceil((q_pos[b] + S) / Bk).  A sequence with q_pos[b] < 0,
- *   q_pos[b] + S > max_pages * Bk or a block count past nb_stride is not
- *   scored (its rows are -inf) and raises MSA_DEVERR_BAD_LEN; a page id
- *   outside [0, num_pages) raises MSA_DEVERR_BAD_PAGE (that block's scores are
- *   then unspecified).
+ *   own block (q_pos[b] + s) / Bk and scores the blocks before it;
+ *   max over b of ceil((q_pos[b] + S) / Bk) <= nb_stride <= max_pages (a
+ *   larger nb_stride is rejected on the host).  A sequence with q_pos[b] < 0
+ *   or whose last query's own block (q_pos[b] + S - 1) / Bk is not below
+ *   nb_stride is not scored (its rows are -inf) and raises
+ *   MSA_DEVERR_BAD_LEN; msa_topk_blocks with the same nb_stride rejects the
+ *   same sequences.  A page id outside [0, num_pages) is not read: that
+ *   block's scores are -inf in every row and MSA_DEVERR_BAD_PAGE is raised.
  * DECODE, fused selection (optional): when `sel` is non-NULL the same kernel
  *   also performs a2 (exactly what msa_topk_blocks computes with this k) on
  *   each (b, g) row as soon as the row's scores are complete, and when `pt` is
@@ -358,7 +360,10 @@ msa_status msa_sparse_attn_decode(const msa_decode_args *args, void *ws, size_t 
  *     rejected with MSA_ERR_WORKSPACE and a message; use msa_sparse_attn_decode
  *     with a workspace for those.
  *   - The first call on a device looks up the array's device address with that
- *     device current; make that first call before any stream capture.
+ *     device current, and so does the first call after the device's context
+ *     was destroyed and created again (cudaDeviceReset); make such a call
+ *     before any stream capture.  A lookup that fails returns MSA_ERR_CUDA
+ *     and is tried again by the next call.
  *   - All calls share the array, which keeps the last call's contents.  Calls
  *     whose kernels overlap on the GPU (other streams, other host threads)
  *     race on it: serialise them.  Each call clears the per-row counters it

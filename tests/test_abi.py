@@ -196,7 +196,7 @@ def _chunk_index_args(abi, **kw):
     a.w_stride[:] = [128, 32, 4]
     a.k_idx_stride[:] = [65536, 8192, 64]      # page pool strides (page, g, t)
     a.C_stride[:] = [4 * 8 * 100, 8 * 100, 100]
-    a.num_pages, a.max_pages, a.nb_stride = 10, 5, 100
+    a.num_pages, a.max_pages, a.nb_stride = 10, 100, 100
     for k, v in kw.items():
         setattr(a, k, v)
     return a
@@ -210,6 +210,15 @@ def test_chunk_index_rejects(abi, field, value, status):
     a = _chunk_index_args(abi, **{field: value})
     assert lib.msa_index_score(C.byref(a), None) == status
     assert lib.msa_last_error_string()
+
+
+def test_chunk_index_rejects_rows_wider_than_the_page_table(abi):
+    """nb_stride > max_pages would let the index score and the top-k disagree
+    on which sequences they reject, so it is refused on the host."""
+    lib = abi.load()
+    a = _chunk_index_args(abi, max_pages=99)
+    assert lib.msa_index_score(C.byref(a), None) == abi.MSA_ERR_INVALID_ARG
+    assert b"max_pages" in lib.msa_last_error_string()
 
 
 def test_chunk_index_group_stride(abi):

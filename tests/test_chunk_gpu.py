@@ -154,6 +154,27 @@ def test_chunk_rejected_sequence_and_page(msa):
     bufs = run_chunk(msa, bad, wl.shape.k, expect_err=msa.MSA_DEVERR_BAD_PAGE)
     for name in ("count", "sel", "O", "LSE"):
         assert torch.equal(bufs[name][0], good[name][0]) and torch.equal(bufs[name][1], good[name][1]), name
+    # the block on the missing page is not loaded: -inf in every row of that sequence
+    assert torch.isneginf(bufs["C"][2, :, :, 0]).all()
+    assert torch.equal(bufs["C"][2, :, :, 1:], good["C"][2, :, :, 1:])
+
+
+def test_chunk_rejects_a_sequence_whose_last_query_leaves_the_pages(msa):
+    """The first query of sequence 1 is inside the page table and the last is
+    not: index score and top-k reject the sequence as a whole (count 0, zero
+    output, LSE -inf, MSA_DEVERR_BAD_LEN); the other sequences are unchanged."""
+    wl = ChunkWorkload("bad_tail", prefix=(1000, 600, 300), S=100, shape=MSAShape(Hq=12, Hkv=2, k=4), seed=73)
+    inp = chunk_inputs(wl, device="cuda")
+    good = run_chunk(msa, inp, wl.shape.k)
+    bad = dict(inp)
+    bad["q_pos"] = inp["q_pos"].clone()
+    bad["q_pos"][1] = wl.max_pages * wl.shape.Bk - wl.S // 2
+    bufs = run_chunk(msa, bad, wl.shape.k, expect_err=msa.MSA_DEVERR_BAD_LEN)
+    assert torch.isneginf(bufs["C"][1]).all()
+    assert int(bufs["count"][1].abs().sum().item()) == 0 and torch.all(bufs["sel"][1] == -1)
+    assert torch.all(bufs["O"][1] == 0) and torch.all(bufs["LSE"][1] == -math.inf)
+    for name in ("C", "count", "sel", "O", "LSE"):
+        assert torch.equal(bufs[name][0], good[name][0]) and torch.equal(bufs[name][2], good[name][2]), name
 
 
 def _bits(t):
