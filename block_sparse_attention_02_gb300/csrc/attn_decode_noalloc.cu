@@ -16,6 +16,8 @@
 // threads) race on it and must be serialised by the caller.  Each call clears
 // the per-row counters it uses (cudaMemsetAsync) and writes every partial that
 // the merge reads before reading it.
+#include <cuda.h>
+
 #include <cstdio>
 #include <mutex>
 
@@ -28,26 +30,70 @@ constexpr size_t kNoallocScratchBytes = MSA_NOALLOC_SCRATCH_BYTES;
 
 static __device__ __align__(256) unsigned char g_decode_scratch[kNoallocScratchBytes];
 
-// Device address of the array, looked up once per device with that device
-// current.  In host code the symbol itself is only a host-side handle.
+// Device address of the array.  In host code the symbol itself is only a
+// host-side handle; the device address comes from cudaGetSymbolAddress with
+// the device current, and belongs to that device's current context.  It is
+// looked up once per context: the cache entry of a device remembers the
+// unique id of the context it was taken in (cuCtxGetId), so a context that was
+// destroyed and created again (cudaDeviceReset) gets a fresh lookup instead of
+// a stale address.  A failed lookup is not remembered: the next call tries
+// again.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
 constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices] = {};
-cudaError_t g_scratch_err[kMaxDevices] = {};
-std::once_flag g_scratch_once[kMaxDevices];
+struct ScratchEntry {
+  unsigned long long ctx_id = 0;   // 0: nothing cached
+  void* ptr = nullptr;
+};
+ScratchEntry g_scratch[kMaxDevices];
+std::mutex g_scratch_mu;
+
+CtxGetCurrentFn g_ctx_current = nullptr;
+CtxGetIdFn g_ctx_id = nullptr;
+std::once_flag g_ctx_fn_once;
+
+// Unique id of the calling thread's current context, or 0 when there is none
+// yet or the driver cannot say.
+unsigned long long current_context_id() {
+  std::call_once(g_ctx_fn_once, []() {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_id = reinterpret_cast<CtxGetIdFn>(f);
+  });
+  if (g_ctx_current == nullptr || g_ctx_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (g_ctx_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 msa_status scratch_address(void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return fail(MSA_ERR_UNSUPPORTED, "device ordinal out of range");
-  std::call_once(g_scratch_once[dev], [dev]() {
-    void* p = nullptr;
-    g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_decode_scratch);
-    g_scratch_ptr[dev] = p;
-  });
-  if (g_scratch_err[dev] != cudaSuccess) return cuda_fail(g_scratch_err[dev], "cudaGetSymbolAddress(decode scratch)");
-  if (g_scratch_ptr[dev] == nullptr) return fail(MSA_ERR_CUDA, "decode scratch has no device address");
-  *out = g_scratch_ptr[dev];
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  const unsigned long long id = current_context_id();
+  if (id != 0 && g_scratch[dev].ctx_id == id) {
+    *out = g_scratch[dev].ptr;
+    return MSA_OK;
+  }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_decode_scratch);   // initialises the context if needed
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(decode scratch)");
+  if (p == nullptr) return fail(MSA_ERR_CUDA, "decode scratch has no device address");
+  // the context the address belongs to (now current, if the lookup created it)
+  g_scratch[dev].ctx_id = current_context_id();
+  g_scratch[dev].ptr = p;
+  *out = p;
   return MSA_OK;
 }
 
