@@ -1,11 +1,16 @@
-"""The N > 1 path on CPU with two gloo ranks.
+"""The N > 1 host logic on CPU with two gloo ranks.
 
 The MSA hot path shards by sequence (decode) or by KV group with no collective
 in the data path; bench.py runs one replica per GPU and only aggregates timings
-(barrier + max over ranks).  Here two gloo processes check that aggregation and
-that a decode batch and a chunk batch (several queries per sequence over the
-paged cache) split by sequence across ranks give exactly the results of the
-unsplit batches (computed with the oracle, all-gathered only for the check).
+(barrier + max over ranks).  Here two gloo processes check bench.py's
+aggregation (max over ranks) and that the computation is separable the way the
+replicas split it: a decode batch and a chunk batch (several queries per
+sequence over the paged cache) split by sequence across ranks give exactly the
+results of the unsplit batches.  The per-rank results come from the oracle
+(all-gathered only for the check), so this covers the sharding and the bench's
+aggregation, not the CUDA library; the library's per-sequence independence is
+covered by the GPU tests (a sequence's outputs do not change when other
+sequences of the batch are rejected or change).
 """
 import math
 import os
