@@ -6,7 +6,14 @@ Bk = 128, k = 16, shuffled 128-token pages).  A step runs the whole hot path:
 index score -> top-k -> page table -> paged sparse attention -> LSE merge.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--no-cpu-baseline]
+                    [--workload NAME] [--also NAMES] [--no-cpu-baseline]
+
+The default run also times the other full-size workloads of the metric, one
+after the other, each with its own warm-up, timed steps, roofline, clocks and
+oracle baseline: one 131,072-token prefill layer (``prefill_s131072``), the
+1M-token decode step (``decode_b1_l1048576``) and the ragged decode batch of
+64 sequences (``decode_ragged_b64``).  They appear under "workloads" in the
+same JSON line; the top-level ``value`` stays the concurrency-8 decode step.
 
 Prints one JSON line (rank 0).  ``value`` is decode tokens/s (sequences
 advanced by one token per second, all ranks), timed with CUDA events on the
@@ -478,7 +485,9 @@ def cpu_prefill_baseline(wl, inp_host, budget_s: float, seed: int = 0):
         n += len(rows)
     dt = time.perf_counter() - t0
     return {"value": n / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{n} query rows of {wl.name} drawn uniformly (all heads and groups) in {dt:.1f} s"}
+            "sample": f"{n} query rows of {wl.name} drawn uniformly (all heads and groups) in {dt:.1f} s",
+            "extrapolated": True,
+            "full_layer_s_extrapolated": wl.B * wl.S / (n / dt)}
 
 
 def cpu_chunk_baseline(wl, inp_host, budget_s: float):
@@ -696,13 +705,51 @@ def run_chunk_ours(args, wl, world, rank):
     return res, None, inp
 
 
+DEFAULT_WORKLOAD = "decode_b8_l60001"
+# the other full-size workloads of the metric (prefill, the 1M-token decode,
+# the ragged decode batch), timed after the headline one in the default run
+EXTRA_WORKLOADS = ("prefill_s131072", "decode_b1_l1048576", "decode_ragged_b64")
+SUB_KEYS = ("value", "unit", "ms_per_step", "steps", "warmup", "config", "roofline", "breakdown_ms", "e2e",
+            "gpu_launches", "clocks", "cpu_baseline")
+
+
+def run_workload(args, wl, world, rank):
+    """Times one workload; returns its JSON record (with cpu_baseline on rank 0 at N = 1)."""
+    import torch
+    from workloads import ChunkWorkload, DecodeWorkload
+    if isinstance(wl, DecodeWorkload):
+        res, host_in, inp = run_decode_ours(args, wl, world, rank)
+    elif isinstance(wl, ChunkWorkload):
+        res, host_in, inp = run_chunk_ours(args, wl, world, rank)
+    else:
+        res, host_in, inp = run_prefill_ours(args, wl, world, rank)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        h = {n: t.cpu() for n, t in inp.items()}
+        if isinstance(wl, DecodeWorkload):
+            res["cpu_baseline"] = cpu_decode_baseline(wl, h, args.cpu_budget_s)
+        elif isinstance(wl, ChunkWorkload):
+            res["cpu_baseline"] = cpu_chunk_baseline(wl, h, args.cpu_budget_s)
+        else:
+            res["cpu_baseline"] = cpu_prefill_baseline(wl, h, args.cpu_budget_s)
+        del h
+    elif rank == 0:
+        res["cpu_baseline"] = None
+    del inp, host_in
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="decode_b8_l60001")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--also", default=",".join(EXTRA_WORKLOADS),
+                    help="with the default workload: further workloads timed in the same run and reported as "
+                         "sub-records under 'workloads' (empty: none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--prefill-chunk", type=int, default=8192)
@@ -774,22 +821,14 @@ def main():
         raise SystemExit("bench.py needs a CUDA device for --impl ours")
     from block_sparse_attention_02_gb300 import build as b
     b.build()
-    if isinstance(wl, DecodeWorkload):
-        res, host_in, inp = run_decode_ours(args, wl, world, rank)
-    elif isinstance(wl, ChunkWorkload):
-        res, host_in, inp = run_chunk_ours(args, wl, world, rank)
-    else:
-        res, host_in, inp = run_prefill_ours(args, wl, world, rank)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        h = {n: t.cpu() for n, t in inp.items()}
-        if isinstance(wl, DecodeWorkload):
-            res["cpu_baseline"] = cpu_decode_baseline(wl, h, args.cpu_budget_s)
-        elif isinstance(wl, ChunkWorkload):
-            res["cpu_baseline"] = cpu_chunk_baseline(wl, h, args.cpu_budget_s)
-        else:
-            res["cpu_baseline"] = cpu_prefill_baseline(wl, h, args.cpu_budget_s)
-    elif rank == 0:
-        res["cpu_baseline"] = None
+    res = run_workload(args, wl, world, rank)
+    extra = [x for x in args.also.split(",") if x] if args.workload == DEFAULT_WORKLOAD and args.seq is None else []
+    if extra:
+        subs = {}
+        for name in extra:
+            sub = run_workload(args, workload(name), world, rank)
+            subs[name] = {k: sub[k] for k in SUB_KEYS if k in sub}
+        res["workloads"] = subs
     if rank == 0:
         print(json.dumps(res))
     if world > 1:
