@@ -12,8 +12,13 @@ The default run also times the other full-size workloads of the metric, one
 after the other, each with its own warm-up, timed steps, roofline, clocks and
 oracle baseline: one 131,072-token prefill layer (``prefill_s131072``), the
 1M-token decode step (``decode_b1_l1048576``) and the ragged decode batch of
-64 sequences (``decode_ragged_b64``).  They appear under "workloads" in the
-same JSON line; the top-level ``value`` stays the concurrency-8 decode step.
+64 sequences (``decode_ragged_b64``).  Then the dense comparator (attention
+over every token, no index branch: the baseline the pages quote MSA's
+speedups against) on the concurrency-8 and 1M decode inputs and the
+131,072-token prefill inputs ("dense:<workload>"), and "msa_vs_dense" holds
+the same-box ratios of MSA tokens/s to dense tokens/s.  They appear under
+"workloads" in the same JSON line; the top-level ``value`` stays the
+concurrency-8 decode step.
 
 Prints one JSON line (rank 0).  ``value`` is decode tokens/s (sequences
 advanced by one token per second, all ranks), timed with CUDA events on the
@@ -705,10 +710,85 @@ def run_chunk_ours(args, wl, world, rank):
     return res, None, inp
 
 
+# ---------------------------------------------------------------------------
+# dense comparator (attention over every token, no index branch)
+# ---------------------------------------------------------------------------
+
+def dense_decode_bytes(wl):
+    """Algorithmic HBM bytes of a dense decode step: every cached K and V token once, Q read, O written."""
+    sh = wl.shape
+    return sum(wl.lengths) * sh.Hkv * sh.D * 2 * 2 + wl.B * sh.Hq * sh.D * 2 * 2
+
+
+def dense_prefill_flops(wl):
+    """4*D FLOPs per (query head, visible key) of a causal prefill: sum_i (i + 1) keys per head."""
+    sh = wl.shape
+    return 4.0 * sh.D * sh.Hq * wl.B * (wl.S * (wl.S + 1) / 2)
+
+
+def run_dense_ours(args, wl, world, rank):
+    """Times the dense comparator on a workload's inputs: a decode step (HBM
+    roofline) or a prefill layer (tensor-core roofline)."""
+    import torch
+    import block_sparse_attention_02_gb300 as msa
+    from workloads import DecodeWorkload, decode_inputs, prefill_inputs
+    peaks = load_peaks()
+    stream = torch.cuda.current_stream()
+    decode = isinstance(wl, DecodeWorkload)
+    if decode:
+        inp = decode_inputs(wl, device="cuda")
+        bufs = msa.dense_decode_buffers(wl.B, wl.shape.Hq, wl.shape.Hkv, inp["seq_pt"].shape[1], "cuda")
+        fn = lambda: msa.dense_decode_step(inp, bufs, scratch_zeroed=True)
+    else:
+        inp = prefill_inputs(wl, device="cuda")
+        bufs = None
+        out = msa.dense_prefill_layer(inp)
+        fn = lambda: msa.dense_prefill_layer(inp, out)
+        bufs = out
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    assert int(bufs["dev_err"].item()) == 0, "device error during the dense warm-up"
+    K = args.steps
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    work = dense_decode_bytes(wl) if decode else dense_prefill_flops(wl)
+    l2 = L2Flush(decode and work < 2 * L2_BYTES)
+    total = l2.time(fn, K, stream)
+    barrier(world)
+    clocks = sampler.stop()
+    assert int(bufs["dev_err"].item()) == 0, "device error during the dense steps"
+    step_ms = max_over_ranks(total, world) / K
+    tokens = wl.B if decode else wl.B * wl.S
+    if decode:
+        ach = work / (step_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "kernel": "dense_decode_kernel", "achieved": ach, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "algorithmic_bytes_per_launch": work}
+    else:
+        ach = work / (step_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": "dense_prefill_kernel", "achieved": ach, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "algorithmic_flops_per_launch": work}
+    roof.update({"peak_src": peaks["src"], "traffic": None, "launch_ms": step_ms})
+    res = {"value": tokens * world / (step_ms * 1e-3), "unit": UNIT, "ms_per_step": step_ms, "steps": K,
+           "warmup": args.warmup,
+           "config": {"workload": wl.name, "comparator": "dense attention over every token (no index branch)",
+                      "l2": "flushed before every timed step" if l2.enabled else "no flush: inputs larger than L2"},
+           "roofline": roof, "gpu_launches": K, "clocks": clocks, "cpu_baseline": None}
+    del inp, bufs
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
 DEFAULT_WORKLOAD = "decode_b8_l60001"
 # the other full-size workloads of the metric (prefill, the 1M-token decode,
-# the ragged decode batch), timed after the headline one in the default run
-EXTRA_WORKLOADS = ("prefill_s131072", "decode_b1_l1048576", "decode_ragged_b64")
+# the ragged decode batch), timed after the headline one in the default run,
+# then the dense comparator on the same inputs ("dense:" + workload)
+EXTRA_WORKLOADS = ("prefill_s131072", "decode_b1_l1048576", "decode_ragged_b64", "dense:decode_b8_l60001",
+                   "dense:decode_b1_l1048576", "dense:prefill_s131072")
 SUB_KEYS = ("value", "unit", "ms_per_step", "steps", "warmup", "config", "roofline", "breakdown_ms", "e2e",
             "gpu_launches", "clocks", "cpu_baseline")
 
@@ -826,9 +906,16 @@ def main():
     if extra:
         subs = {}
         for name in extra:
-            sub = run_workload(args, workload(name), world, rank)
+            if name.startswith("dense:"):
+                sub = run_dense_ours(args, workload(name[len("dense:"):]), world, rank)
+            else:
+                sub = run_workload(args, workload(name), world, rank)
             subs[name] = {k: sub[k] for k in SUB_KEYS if k in sub}
         res["workloads"] = subs
+        # the same-box speedup of MSA over the dense comparator, per workload
+        msa_values = dict(subs, **{args.workload: res})
+        res["msa_vs_dense"] = {n[len("dense:"):]: msa_values[n[len("dense:"):]]["value"] / subs[n]["value"]
+                               for n in subs if n.startswith("dense:") and n[len("dense:"):] in msa_values}
     if rank == 0:
         print(json.dumps(res))
     if world > 1:

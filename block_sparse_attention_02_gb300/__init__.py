@@ -25,6 +25,8 @@ __all__ = [
     "msa_index_score", "msa_topk_blocks", "msa_build_page_table", "msa_sparse_attn_prefill",
     "msa_sparse_attn_decode", "msa_sparse_attn_decode_noalloc", "msa_lse_merge", "msa_sparse_attn_prefill_workspace_size",
     "msa_sparse_attn_decode_workspace_size", "msa_cache_append", "decode_step", "prefill_layer", "chunk_layer",
+    "msa_dense_attn_decode", "msa_dense_attn_decode_workspace_size", "dense_decode_buffers", "dense_decode_step",
+    "msa_dense_attn_prefill", "dense_prefill_layer",
     "lib", "MSAError",
     "MSA_MODE_PREFILL", "MSA_MODE_DECODE", "MSA_MODE_CHUNK", "MSA_DEVERR_TIMEOUT", "MSA_DEVERR_BAD_PAGE",
     "MSA_DEVERR_BAD_SEL", "MSA_DEVERR_BAD_LEN", "Bk", "D", "dI",
@@ -292,6 +294,108 @@ def msa_lse_merge(O_part: torch.Tensor, LSE_part: torch.Tensor, O: torch.Tensor,
             raise ValueError(f"{nm} must be contiguous")
     _abi.check(lib().msa_lse_merge(_ptr(O_part), _ptr(LSE_part), rows, parts, d, _ptr(O), _ptr(LSE),
                                    _ptr(dev_err), _stream(stream)), "msa_lse_merge")
+
+
+# ---------------------------------------------------------------------------
+# dense comparator (no index branch, no selection)
+# ---------------------------------------------------------------------------
+
+def _dense_decode_args(Q, K_pool, V_pool, seq_pt, seq_len, O, LSE, softmax_scale, dev_err) -> _abi.DenseDecodeArgs:
+    for t, nm in ((Q, "Q"), (K_pool, "K_pool"), (V_pool, "V_pool")):
+        _inner_contig(t, nm)
+    if K_pool.stride() != V_pool.stride():
+        raise ValueError("K_pool and V_pool must share strides")
+    if not seq_pt.is_contiguous():
+        raise ValueError("seq_pt must be contiguous")
+    a = _abi.DenseDecodeArgs()
+    a.B, a.Hq, a.D = Q.shape
+    a.Hkv, a.Bk = K_pool.shape[1], K_pool.shape[2]
+    a.softmax_scale = softmax_scale
+    a.Q = _ptr(Q)
+    a.Q_stride[:] = _strides(Q, 2)
+    a.K_pool, a.V_pool = _ptr(K_pool), _ptr(V_pool)
+    a.kv_stride[:] = _strides(K_pool, 3)
+    a.num_pages = K_pool.shape[0]
+    a.seq_pt, a.max_pages, a.seq_len = _ptr(seq_pt), seq_pt.shape[1], _ptr(seq_len)
+    a.O, a.LSE, a.dev_err = _ptr(O), _ptr(LSE), _ptr(dev_err)
+    return a
+
+
+def msa_dense_attn_decode_workspace_size(B: int, Hq: int, Hkv: int, max_pages: int) -> int:
+    a = _abi.DenseDecodeArgs()
+    a.B, a.Hq, a.Hkv, a.D, a.Bk, a.max_pages = B, Hq, Hkv, D, Bk, max_pages
+    return int(lib().msa_dense_attn_decode_workspace_size(C.byref(a)))
+
+
+def msa_dense_attn_decode(Q, K_pool, V_pool, seq_pt, seq_len, O, LSE, ws: torch.Tensor, *,
+                          softmax_scale: float = 0.0, dev_err=None, stream=None, scratch_zeroed: bool = False) -> None:
+    """Dense comparator of a decode step: every cached token of each sequence (see msa.h)."""
+    if not O.is_contiguous():
+        raise ValueError("O must be contiguous")
+    a = _dense_decode_args(Q, K_pool, V_pool, seq_pt, seq_len, O, LSE, softmax_scale, dev_err)
+    a.scratch_zeroed = int(bool(scratch_zeroed))
+    _abi.check(lib().msa_dense_attn_decode(C.byref(a), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+               "msa_dense_attn_decode")
+
+
+def dense_decode_buffers(B: int, Hq: int, Hkv: int, max_pages: int, device) -> Dict[str, torch.Tensor]:
+    """Outputs and zero-filled scratch of ``dense_decode_step``."""
+    dev = torch.device(device)
+    return {
+        "O": torch.empty(B, Hq, D, dtype=torch.bfloat16, device=dev),
+        "LSE": torch.empty(B, Hq, dtype=torch.float32, device=dev),
+        "ws": torch.zeros(msa_dense_attn_decode_workspace_size(B, Hq, Hkv, max_pages) // 4 + 64, dtype=torch.float32,
+                          device=dev),
+        "dev_err": torch.zeros(1, dtype=torch.int32, device=dev),
+    }
+
+
+def dense_decode_step(inp: Dict[str, torch.Tensor], bufs: Optional[Dict[str, torch.Tensor]] = None,
+                      softmax_scale: float = 0.0, stream=None, scratch_zeroed: bool = False
+                      ) -> Dict[str, torch.Tensor]:
+    """The dense comparator of ``decode_step``: attention over every cached token (no index branch)."""
+    B, Hq, _ = inp["Q"].shape
+    Hkv = inp["K_pool"].shape[1]
+    if bufs is None:
+        bufs = dense_decode_buffers(B, Hq, Hkv, inp["seq_pt"].shape[1], inp["Q"].device)
+    msa_dense_attn_decode(inp["Q"], inp["K_pool"], inp["V_pool"], inp["seq_pt"], inp["seq_len"], bufs["O"],
+                          bufs["LSE"], bufs["ws"], softmax_scale=softmax_scale, dev_err=bufs["dev_err"],
+                          stream=stream, scratch_zeroed=scratch_zeroed)
+    return bufs
+
+
+def msa_dense_attn_prefill(Q, K, V, O, LSE, *, softmax_scale: float = 0.0, dev_err=None, stream=None) -> None:
+    """Dense comparator of a prefill layer: causal GQA attention over every earlier token (see msa.h).
+
+    Q [B,S,Hq,D], K, V [B,S,Hkv,D] bf16; O [B,S,Hq,D] bf16 and LSE [B,S,Hq] fp32 (dense)."""
+    for t, nm in ((Q, "Q"), (K, "K"), (V, "V")):
+        _inner_contig(t, nm)
+    if not O.is_contiguous() or (LSE is not None and not LSE.is_contiguous()):
+        raise ValueError("O and LSE must be contiguous")
+    a = _abi.DensePrefillArgs()
+    a.B, a.S, a.Hq, a.D = Q.shape
+    a.Hkv = K.shape[2]
+    a.softmax_scale = softmax_scale
+    a.Q, a.K, a.V = _ptr(Q), _ptr(K), _ptr(V)
+    a.Q_stride[:] = _strides(Q, 3)
+    a.K_stride[:] = _strides(K, 3)
+    a.V_stride[:] = _strides(V, 3)
+    a.O, a.LSE, a.dev_err = _ptr(O), _ptr(LSE), _ptr(dev_err)
+    _abi.check(lib().msa_dense_attn_prefill(C.byref(a), _stream(stream)), "msa_dense_attn_prefill")
+
+
+def dense_prefill_layer(inp: Dict[str, torch.Tensor], bufs: Optional[Dict[str, torch.Tensor]] = None,
+                        softmax_scale: float = 0.0, stream=None) -> Dict[str, torch.Tensor]:
+    """The dense comparator of ``prefill_layer``: causal attention over every earlier token (no index branch)."""
+    B, S, Hq, _ = inp["Q"].shape
+    if bufs is None:
+        dev = inp["Q"].device
+        bufs = {"O": torch.empty(B, S, Hq, D, dtype=torch.bfloat16, device=dev),
+                "LSE": torch.empty(B, S, Hq, dtype=torch.float32, device=dev),
+                "dev_err": torch.zeros(1, dtype=torch.int32, device=dev)}
+    msa_dense_attn_prefill(inp["Q"], inp["K"], inp["V"], bufs["O"], bufs["LSE"], softmax_scale=softmax_scale,
+                           dev_err=bufs["dev_err"], stream=stream)
+    return bufs
 
 
 # ---------------------------------------------------------------------------

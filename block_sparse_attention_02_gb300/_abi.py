@@ -91,6 +91,25 @@ class AppendArgs(C.Structure):
     ]
 
 
+class DenseDecodeArgs(C.Structure):
+    _fields_ = [
+        ("B", C.c_int), ("Hq", C.c_int), ("Hkv", C.c_int), ("D", C.c_int), ("Bk", C.c_int),
+        ("softmax_scale", C.c_float),
+        ("Q", _p), ("Q_stride", _i64x2), ("K_pool", _p), ("V_pool", _p), ("kv_stride", _i64x3),
+        ("num_pages", C.c_int64), ("seq_pt", _p), ("max_pages", C.c_int64), ("seq_len", _p),
+        ("O", _p), ("LSE", _p), ("dev_err", _p), ("scratch_zeroed", C.c_int),
+    ]
+
+
+class DensePrefillArgs(C.Structure):
+    _fields_ = [
+        ("B", C.c_int), ("S", C.c_int), ("Hq", C.c_int), ("Hkv", C.c_int), ("D", C.c_int),
+        ("softmax_scale", C.c_float),
+        ("Q", _p), ("Q_stride", _i64x3), ("K", _p), ("K_stride", _i64x3), ("V", _p), ("V_stride", _i64x3),
+        ("O", _p), ("LSE", _p), ("dev_err", _p),
+    ]
+
+
 # exported function name -> (restype, argtypes)
 SIGNATURES = {
     "msa_version": (C.c_int, []),
@@ -107,6 +126,9 @@ SIGNATURES = {
     "msa_sparse_attn_decode_noalloc": (C.c_int, [C.POINTER(DecodeArgs), _p]),
     "msa_lse_merge": (C.c_int, [_p, _p, C.c_int64, C.c_int, C.c_int, _p, _p, _p, _p]),
     "msa_cache_append": (C.c_int, [C.POINTER(AppendArgs), _p]),
+    "msa_dense_attn_decode_workspace_size": (C.c_size_t, [C.POINTER(DenseDecodeArgs)]),
+    "msa_dense_attn_decode": (C.c_int, [C.POINTER(DenseDecodeArgs), _p, C.c_size_t, _p]),
+    "msa_dense_attn_prefill": (C.c_int, [C.POINTER(DensePrefillArgs), _p]),
 }
 
 _lock = threading.Lock()

@@ -352,6 +352,65 @@ msa_status msa_sparse_attn_prefill(const msa_prefill_args* a, void* ws, size_t w
 }
 
 // ---------------------------------------------------------------------------
+static msa_status check_dense_decode(const msa_dense_decode_args* a) {
+  MSA_REQUIRE(a != nullptr, MSA_ERR_INVALID_ARG, "args is NULL");
+  MSA_REQUIRE(a->B >= 0 && a->B <= kDenseMaxBatch && a->Hkv >= 1 && a->Hq >= 1, MSA_ERR_INVALID_ARG,
+              "B = %d (at most %d), Hq = %d, Hkv = %d", a->B, kDenseMaxBatch, a->Hq, a->Hkv);
+  MSA_REQUIRE(a->Hq % a->Hkv == 0 && a->Hq / a->Hkv <= kMaxG, MSA_ERR_UNSUPPORTED,
+              "GQA ratio Hq/Hkv = %d/%d not in 1..%d", a->Hq, a->Hkv, kMaxG);
+  if (msa_status st = check_common_shape(a->Bk, a->D, kD, "D"); st != MSA_OK) return st;
+  MSA_REQUIRE(a->Q && a->K_pool && a->V_pool && a->seq_pt && a->seq_len && a->O, MSA_ERR_INVALID_ARG,
+              "Q, K_pool, V_pool, seq_pt, seq_len and O must be non-NULL");
+  MSA_REQUIRE(aligned16(a->Q) && aligned16(a->K_pool) && aligned16(a->V_pool) && aligned16(a->O), MSA_ERR_INVALID_ARG,
+              "Q, K_pool, V_pool and O must be 16-byte aligned");
+  MSA_REQUIRE(a->num_pages >= 1 && a->num_pages < (int64_t(1) << 31), MSA_ERR_INVALID_ARG, "num_pages = %" PRId64,
+              a->num_pages);
+  MSA_REQUIRE(a->max_pages >= 1 && static_cast<int64_t>(a->B) * a->Hkv * a->max_pages < (int64_t(1) << 30),
+              MSA_ERR_INVALID_ARG, "max_pages = %" PRId64 ": B * Hkv * max_pages must be below 2^30", a->max_pages);
+  for (int i = 0; i < 2; ++i)
+    MSA_REQUIRE(vec_stride_ok(a->Q_stride[i], 2), MSA_ERR_INVALID_ARG,
+                "Q_stride[%d] = %" PRId64 " must be a positive multiple of 8 elements", i, a->Q_stride[i]);
+  for (int i = 0; i < 3; ++i)
+    MSA_REQUIRE(vec_stride_ok(a->kv_stride[i], 2), MSA_ERR_INVALID_ARG,
+                "kv_stride[%d] = %" PRId64 " must be a positive multiple of 8 elements", i, a->kv_stride[i]);
+  return MSA_OK;
+}
+
+size_t msa_dense_attn_decode_workspace_size(const msa_dense_decode_args* a) {
+  if (a == nullptr || a->B < 0 || a->Hq < 1 || a->Hkv < 1 || a->max_pages < 1) return 0;
+  return dense_decode_workspace_size(*a);
+}
+
+msa_status msa_dense_attn_decode(const msa_dense_decode_args* a, void* ws, size_t ws_bytes, msa_stream_t stream) {
+  g_last_error.clear();
+  if (msa_status st = check_dense_decode(a); st != MSA_OK) return st;
+  const size_t need = dense_decode_workspace_size(*a);
+  MSA_REQUIRE(ws != nullptr && ws_bytes >= need, MSA_ERR_WORKSPACE, "workspace %zu bytes, need %zu", ws_bytes, need);
+  MSA_REQUIRE(aligned16(ws), MSA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  if (a->B == 0) return MSA_OK;
+  return launch_dense_decode(*a, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+msa_status msa_dense_attn_prefill(const msa_dense_prefill_args* a, msa_stream_t stream) {
+  g_last_error.clear();
+  MSA_REQUIRE(a != nullptr, MSA_ERR_INVALID_ARG, "args is NULL");
+  MSA_REQUIRE(a->B >= 0 && a->S >= 0 && a->Hkv >= 1 && a->Hq >= 1, MSA_ERR_INVALID_ARG,
+              "B = %d, S = %d, Hq = %d, Hkv = %d", a->B, a->S, a->Hq, a->Hkv);
+  MSA_REQUIRE(a->Hq % a->Hkv == 0 && a->Hq / a->Hkv <= kMaxG, MSA_ERR_UNSUPPORTED,
+              "GQA ratio Hq/Hkv = %d/%d not in 1..%d", a->Hq, a->Hkv, kMaxG);
+  MSA_REQUIRE(a->D == kD, MSA_ERR_UNSUPPORTED, "D = %d, only %d is supported", a->D, kD);
+  MSA_REQUIRE(a->Q && a->K && a->V && a->O, MSA_ERR_INVALID_ARG, "Q, K, V and O must be non-NULL");
+  MSA_REQUIRE(aligned16(a->Q) && aligned16(a->K) && aligned16(a->V) && aligned16(a->O), MSA_ERR_INVALID_ARG,
+              "Q, K, V and O must be 16-byte aligned");
+  for (int i = 0; i < 3; ++i)
+    MSA_REQUIRE(vec_stride_ok(a->Q_stride[i], 2) && vec_stride_ok(a->K_stride[i], 2) && vec_stride_ok(a->V_stride[i], 2),
+                MSA_ERR_INVALID_ARG, "Q/K/V strides must be positive multiples of 8 elements");
+  MSA_REQUIRE(static_cast<int64_t>(a->B) * a->S < (int64_t(1) << 31), MSA_ERR_UNSUPPORTED, "B*S too large");
+  if (static_cast<int64_t>(a->B) * a->S == 0) return MSA_OK;
+  return launch_dense_prefill(*a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------------------
 msa_status msa_lse_merge(const float* O_part, const float* LSE_part, int64_t rows, int parts, int D, void* O,
                          float* LSE, int32_t* dev_err, msa_stream_t stream) {
   g_last_error.clear();

@@ -47,6 +47,9 @@ msa_status launch_lse_merge_bf16(const __nv_bfloat16* o_part, const float* lse_p
                                  __nv_bfloat16* O, float* LSE, cudaStream_t stream);
 msa_status launch_attn_prefill(const msa_prefill_args& a, void* ws, size_t ws_bytes, cudaStream_t stream);
 msa_status launch_cache_append(const msa_append_args& a, cudaStream_t stream);
+msa_status launch_dense_decode(const msa_dense_decode_args& a, void* ws, size_t ws_bytes, cudaStream_t stream);
+size_t dense_decode_workspace_size(const msa_dense_decode_args& a);
+msa_status launch_dense_prefill(const msa_dense_prefill_args& a, cudaStream_t stream);
 // Host-side argument checks of msa_sparse_attn_decode (no CUDA call).
 msa_status check_decode_args(const msa_decode_args* a);
 size_t attn_prefill_workspace_size(const msa_prefill_args& a, int64_t chunk_queries);
@@ -58,5 +61,7 @@ constexpr int kMaxK = 64;
 constexpr int kMaxHI = 4;
 constexpr int kMaxG = 8;
 constexpr int kMaxDecodeBatch = 4096;
+constexpr int kDenseMaxBatch = 1024;   // dense comparator: sequences per call
+constexpr int kDenseMaxGrid = 256;     // dense decode: CTAs per launch (at most)
 
 }  // namespace msa

@@ -375,6 +375,84 @@ msa_status msa_sparse_attn_decode(const msa_decode_args *args, void *ws, size_t 
 msa_status msa_sparse_attn_decode_noalloc(const msa_decode_args *args, msa_stream_t stream);
 
 /* --------------------------------------------------------------------------
+ * Dense comparator: paged decode over every cached token
+ *
+ * The pages quote MSA's speed only against dense attention ("MiniMax M3: Como
+ * la atencion dispersa hace practicos a los agentes de largo alcance", bullet
+ * "Rapido en produccion": 14.2x prefill and 7.6x decode on H800; the M2-report
+ * article, section "MiniMax Sparse Attention (MSA) y escalado subcuadratico
+ * entrante": 9.7x / 15.6x at 1M tokens).  This call is that baseline for a
+ * decode step, on the same inputs and layouts as the MSA decode step but with
+ * no index branch and no selection: each query attends to all L_b tokens of
+ * its sequence, what MSA computes when k covers every block.
+ *     O[b, h] = sum_{t < L_b} softmax_t(scale * Q[b, h] . K[b, g, t]) V[b, g, t],
+ *     g = h / G, logical block j of sequence b in page seq_pt[b][j];
+ *     LSE[b, h] = ln sum_t exp(scale * Q[b, h] . K[b, g, t]).
+ *     Q [B, Hq, D] bf16 strides (b, h); K_pool, V_pool [num_pages, Hkv, Bk, D]
+ *     bf16 with common strides kv_stride = (page, g, t); seq_pt [B, max_pages]
+ *     and seq_len [B] int32; O [B, Hq, D] bf16 (dense), LSE [B, Hq] fp32
+ *     (dense, may be NULL).
+ * Workspace: msa_dense_attn_decode_workspace_size(args) bytes of caller
+ * scratch (per-split partials and one page counter per (b, g) row, the
+ * counters last).  scratch_zeroed works as in msa_sparse_attn_decode.
+ * A sequence whose length is outside [1, max_pages * Bk] gets O = 0 and
+ * LSE = -inf and raises MSA_DEVERR_BAD_LEN; a page id outside [0, num_pages)
+ * is not read (MSA_DEVERR_BAD_PAGE) and its tokens are left out.  Pool slots
+ * past a sequence's last token must hold finite values.  B <= 1024 and
+ * B * Hkv * max_pages < 2^30.
+ * ------------------------------------------------------------------------ */
+typedef struct msa_dense_decode_args {
+    int B, Hq, Hkv, D, Bk;
+    float softmax_scale;
+    const void *Q;
+    int64_t Q_stride[2];
+    const void *K_pool;
+    const void *V_pool;
+    int64_t kv_stride[3];
+    int64_t num_pages;
+    const int32_t *seq_pt;
+    int64_t max_pages;
+    const int32_t *seq_len;
+    void *O;
+    float *LSE;
+    int32_t *dev_err;
+    int scratch_zeroed;
+} msa_dense_decode_args;
+
+size_t msa_dense_attn_decode_workspace_size(const msa_dense_decode_args *args);
+msa_status msa_dense_attn_decode(const msa_dense_decode_args *args, void *ws, size_t ws_bytes,
+                                 msa_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * Dense comparator: causal prefill over every earlier token
+ *
+ * The prefill half of the same baseline (pages and passages as for
+ * msa_dense_attn_decode): exact causal GQA attention with no index branch and
+ * no selection, what MSA computes when k covers every block.
+ *     O[b, i, h] = sum_{t <= i} softmax_t(scale * Q[b, i, h] . K[b, t, g]) V[b, t, g],
+ *     LSE[b, i, h] = ln sum_{t <= i} exp(scale * Q[b, i, h] . K[b, t, g]),  g = h / G.
+ *     Q [B, S, Hq, D] bf16 strides (b, s, h); K, V [B, S, Hkv, D] bf16 strides
+ *     (b, s, g); O [B, S, Hq, D] bf16 (dense), LSE [B, S, Hq] fp32 (dense, may
+ *     be NULL).
+ * No workspace.  softmax_scale <= 0 selects 1 / sqrt(D).  B * S < 2^31.
+ * ------------------------------------------------------------------------ */
+typedef struct msa_dense_prefill_args {
+    int B, S, Hq, Hkv, D;
+    float softmax_scale;
+    const void *Q;
+    int64_t Q_stride[3];
+    const void *K;
+    int64_t K_stride[3];
+    const void *V;
+    int64_t V_stride[3];
+    void *O;
+    float *LSE;
+    int32_t *dev_err;
+} msa_dense_prefill_args;
+
+msa_status msa_dense_attn_prefill(const msa_dense_prefill_args *args, msa_stream_t stream);
+
+/* --------------------------------------------------------------------------
  * a6. Log-sum-exp merge of partial softmax results
  *
  * Partial outputs over blocks recombined by a final log-sum-exp reduction

@@ -43,7 +43,8 @@ def test_exports_every_declared_symbol(abi):
 def test_struct_layout_matches_header(abi, tmp_path):
     structs = {"msa_index_args": abi.IndexArgs, "msa_topk_args": abi.TopkArgs,
                "msa_prefill_args": abi.PrefillArgs, "msa_decode_args": abi.DecodeArgs,
-               "msa_append_args": abi.AppendArgs}
+               "msa_append_args": abi.AppendArgs, "msa_dense_decode_args": abi.DenseDecodeArgs,
+               "msa_dense_prefill_args": abi.DensePrefillArgs}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "msa.h"', "int main(void) {"]
     for cname, py in structs.items():
         lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
@@ -258,3 +259,54 @@ def test_chunk_topk_and_attention_reject(abi):
     assert lib.msa_sparse_attn_prefill_workspace_size(C.byref(a), 4) > 0
     a.max_pages = 0
     assert lib.msa_sparse_attn_prefill_workspace_size(C.byref(a), 4) == 0
+
+
+def _dense_decode_args(abi, **kw):
+    a = abi.DenseDecodeArgs()
+    a.B, a.Hq, a.Hkv, a.D, a.Bk = 2, 48, 8, 128, 128
+    a.Q = a.K_pool = a.V_pool = a.seq_pt = a.seq_len = a.O = FAKE
+    a.Q_stride[:] = [48 * 128, 128]
+    a.kv_stride[:] = [8 * 128 * 128, 128 * 128, 128]
+    a.num_pages, a.max_pages = 10, 5
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("Hq", 47, 2), ("D", 64, 2), ("Bk", 64, 2), ("B", 1025, 1), ("seq_pt", None, 1), ("max_pages", 0, 1),
+    ("max_pages", 1 << 27, 1), ("num_pages", 0, 1), ("Q", FAKE + 4, 1),
+])
+def test_dense_decode_rejects(abi, field, value, status):
+    lib = abi.load()
+    ws = lib.msa_dense_attn_decode_workspace_size(C.byref(_dense_decode_args(abi)))
+    assert ws >= 2 * 48 * 2 * 129 * 4
+    a = _dense_decode_args(abi, **{field: value})
+    assert lib.msa_dense_attn_decode(C.byref(a), FAKE, ws, None) == status
+    assert lib.msa_last_error_string()
+
+
+def test_dense_decode_rejects_small_workspace(abi):
+    lib = abi.load()
+    a = _dense_decode_args(abi)
+    ws = lib.msa_dense_attn_decode_workspace_size(C.byref(a))
+    assert lib.msa_dense_attn_decode(C.byref(a), FAKE, ws - 1, None) == abi.MSA_ERR_WORKSPACE
+    assert lib.msa_dense_attn_decode(C.byref(a), None, ws, None) == abi.MSA_ERR_WORKSPACE
+
+
+def test_dense_prefill_rejects(abi):
+    lib = abi.load()
+    a = abi.DensePrefillArgs()
+    a.B, a.S, a.Hq, a.Hkv, a.D = 1, 256, 48, 8, 128
+    a.Q = a.K = a.V = a.O = FAKE
+    a.Q_stride[:] = [256 * 48 * 128, 48 * 128, 128]
+    a.K_stride[:] = a.V_stride[:] = [256 * 8 * 128, 8 * 128, 128]
+    a.D = 64
+    assert lib.msa_dense_attn_prefill(C.byref(a), None) == abi.MSA_ERR_UNSUPPORTED
+    a.D, a.Hq = 128, 80                                  # G = 10
+    assert lib.msa_dense_attn_prefill(C.byref(a), None) == abi.MSA_ERR_UNSUPPORTED
+    a.Hq, a.V = 48, None
+    assert lib.msa_dense_attn_prefill(C.byref(a), None) == abi.MSA_ERR_INVALID_ARG
+    a.V = FAKE
+    a.K_stride[1] = 100                                  # not a multiple of 8 elements
+    assert lib.msa_dense_attn_prefill(C.byref(a), None) == abi.MSA_ERR_INVALID_ARG
