@@ -454,8 +454,20 @@ def oracle_decode_step(h, sh):
                                 1.0 / math.sqrt(sh.D))
 
 
+def one_thread(fn):
+    """Runs fn() with the oracle on one host thread; returns its result."""
+    import oracle
+    n = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        return fn()
+    finally:
+        oracle.set_num_threads(n)
+
+
 def cpu_decode_baseline(wl, inp_host, budget_s: float, min_steps: int = 1):
-    """Oracle decode steps on the host cores until the time budget is used."""
+    """Oracle decode steps on the host cores until the time budget is used;
+    then one step on a single thread."""
     import oracle
     oracle.build()
     t0 = time.perf_counter()
@@ -464,8 +476,15 @@ def cpu_decode_baseline(wl, inp_host, budget_s: float, min_steps: int = 1):
         oracle_decode_step(inp_host, wl.shape)
         steps += 1
     dt = time.perf_counter() - t0
+
+    def single():
+        t1 = time.perf_counter()
+        oracle_decode_step(inp_host, wl.shape)
+        return time.perf_counter() - t1
+    dt1 = one_thread(single)
     return {"value": wl.B * steps / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{steps} full decode step(s) of {wl.name} (B={wl.B}) in {dt:.1f} s"}
+            "sample": f"{steps} full decode step(s) of {wl.name} (B={wl.B}) in {dt:.1f} s",
+            "value_1_thread": wl.B / dt1, "sample_1_thread": f"one full decode step in {dt1:.1f} s"}
 
 
 def cpu_prefill_baseline(wl, inp_host, budget_s: float, seed: int = 0):
@@ -489,10 +508,21 @@ def cpu_prefill_baseline(wl, inp_host, budget_s: float, seed: int = 0):
                               rows)
         n += len(rows)
     dt = time.perf_counter() - t0
+
+    def single():
+        r = np.sort(rng.integers(0, wl.B * wl.S, 16)).astype(np.int64)
+        t1 = time.perf_counter()
+        C1 = oracle.prefill_scores(inp_host["q_idx"], inp_host["k_idx"], inp_host["w"], sh.Bk, r)
+        o1 = np.repeat(oracle.own_blocks_prefill(wl.S, sh.Bk, r), sh.Hkv).reshape(-1, sh.Hkv)
+        s1, c1, _, _ = oracle.select(C1, o1, sh.k)
+        oracle.prefill_attend(inp_host["Q"], inp_host["K"], inp_host["V"], s1, c1, sh.Bk, 1.0 / math.sqrt(sh.D), r)
+        return time.perf_counter() - t1
+    dt1 = one_thread(single)
     return {"value": n / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{n} query rows of {wl.name} drawn uniformly (all heads and groups) in {dt:.1f} s",
             "extrapolated": True,
-            "full_layer_s_extrapolated": wl.B * wl.S / (n / dt)}
+            "full_layer_s_extrapolated": wl.B * wl.S / (n / dt),
+            "value_1_thread": 16 / dt1, "sample_1_thread": f"16 uniformly drawn query rows in {dt1:.1f} s"}
 
 
 def cpu_chunk_baseline(wl, inp_host, budget_s: float):
@@ -704,7 +734,8 @@ def run_chunk_ours(args, wl, world, rank):
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,
         "breakdown_ms": {"index_score": part_ms[0], "topk": part_ms[1], "sparse_attention": part_ms[2]},
-        "gpu_launches": K * (2 + 5 * ((wl.B * wl.S + ws_q - 1) // ws_q)),
+        # a few queries per sequence: page table + decode attention (2 launches); else 5 per query chunk
+        "gpu_launches": K * (2 + (2 if wl.S <= 8 else 5 * ((wl.B * wl.S + ws_q - 1) // ws_q))),
         "clocks": clocks,
     }
     return res, None, inp

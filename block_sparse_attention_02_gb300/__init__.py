@@ -214,6 +214,9 @@ def msa_sparse_attn_prefill_workspace_size(Q, K, sel, chunk_queries: int, max_pa
     a = _abi.PrefillArgs()
     a.B, a.S, a.Hq, a.D = Q.shape
     a.Hkv, a.Bk, a.k = K.shape[2], Bk, sel.shape[-1]
+    a.Q_stride[:] = _strides(Q, 3)
+    a.K_stride[:] = _strides(K, 3)
+    a.V_stride[:] = _strides(K, 3)      # V is taken to share K's strides
     if max_pages is not None:
         a.mode, a.Hkv, a.max_pages = MSA_MODE_CHUNK, K.shape[1], int(max_pages)
     return int(lib().msa_sparse_attn_prefill_workspace_size(C.byref(a), int(chunk_queries)))

@@ -840,13 +840,72 @@ WsLayout ws_layout(const msa_prefill_args& a, int64_t cq) {
   return L;
 }
 
+// A chunk of at most kChunkDecodeMaxS queries per sequence (a few decode
+// tokens: draft verification) runs through the decode attention kernel
+// instead: the rows (b, s, g), each with its own selected pages and last-page
+// length, are a decode batch of B * S sequences, served in one launch after
+// the page table (versus the per-chunk inversion, attention and merge of the
+// KV-block-major path).  It needs Q dense over (b, s) and K, V with one set of
+// strides; otherwise the KV-block-major path runs.
+bool chunk_decode_path(const msa_prefill_args& a) {
+  return a.mode == MSA_MODE_CHUNK && a.S <= kChunkDecodeMaxS && a.Q_stride[0] == a.S * a.Q_stride[1] &&
+         a.K_stride[0] == a.V_stride[0] && a.K_stride[1] == a.V_stride[1] && a.K_stride[2] == a.V_stride[2];
+}
+
+struct ChunkDecodeWs {
+  size_t pt, n, last_len, o_part, lse_part, counter, total;
+};
+ChunkDecodeWs chunk_decode_ws(const msa_prefill_args& a) {
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t rows = static_cast<size_t>(a.B) * a.S * a.Hkv;
+  const size_t parts = static_cast<size_t>(a.B) * a.S * a.Hq * a.k;
+  ChunkDecodeWs L;
+  size_t o = 0;
+  L.pt = o; o = al(o + rows * a.k * 4);
+  L.n = o; o = al(o + rows * 4);
+  L.last_len = o; o = al(o + rows * 4);
+  L.o_part = o; o = al(o + parts * kD * 4);
+  L.lse_part = o; o = al(o + parts * 4);
+  L.counter = o; o = al(o + rows * 4);
+  L.total = o + 256;
+  return L;
+}
+
+msa_status launch_chunk_decode(const msa_prefill_args& a, void* ws, cudaStream_t stream) {
+  const ChunkDecodeWs L = chunk_decode_ws(a);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int32_t* pt = reinterpret_cast<int32_t*>(w + L.pt);
+  int32_t* n = reinterpret_cast<int32_t*>(w + L.n);
+  int32_t* last_len = reinterpret_cast<int32_t*>(w + L.last_len);
+  if (msa_status st = launch_page_table(a.sel, a.count, a.seq_pt, a.max_pages, nullptr, a.B, a.Hkv, a.k, kBk, pt, n,
+                                        last_len, a.dev_err, stream, a.S, a.q_pos);
+      st != MSA_OK)
+    return st;
+  msa_decode_args d{};
+  d.B = a.B * a.S; d.Hq = a.Hq; d.Hkv = a.Hkv; d.D = a.D; d.Bk = a.Bk; d.k = a.k;
+  d.softmax_scale = a.softmax_scale;
+  d.Q = a.Q;
+  d.Q_stride[0] = a.Q_stride[1];   // row (b, s) = b * S + s: Q is dense over (b, s)
+  d.Q_stride[1] = a.Q_stride[2];
+  d.K_pool = a.K; d.V_pool = a.V;
+  for (int i = 0; i < 3; ++i) d.kv_stride[i] = a.K_stride[i];
+  d.num_pages = a.num_pages;
+  d.pt = pt; d.n = n; d.last_len = last_len;
+  d.O = a.O; d.LSE = a.LSE; d.dev_err = a.dev_err;
+  d.scratch_zeroed = 0;
+  return launch_attn_decode(d, reinterpret_cast<float*>(w + L.o_part), reinterpret_cast<float*>(w + L.lse_part),
+                            reinterpret_cast<int32_t*>(w + L.counter), stream);
+}
+
 }  // namespace
 
 size_t attn_prefill_workspace_size(const msa_prefill_args& a, int64_t chunk_queries) {
+  if (chunk_decode_path(a)) return chunk_decode_ws(a).total;
   return ws_layout(a, chunk_queries).total;
 }
 
 msa_status launch_attn_prefill(const msa_prefill_args& a, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (chunk_decode_path(a)) return launch_chunk_decode(a, ws, stream);
   DeviceInfo dev;
   if (msa_status st = current_device(&dev); st != MSA_OK) return st;
   const int64_t total_q = static_cast<int64_t>(a.B) * a.S;

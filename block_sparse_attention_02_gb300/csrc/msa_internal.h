@@ -38,7 +38,7 @@ msa_status launch_topk(const msa_topk_args& a, cudaStream_t stream);
 msa_status launch_page_table(const int32_t* sel, const int32_t* count, const int32_t* seq_pt,
                              int64_t max_pages, const int32_t* seq_len, int B, int Hkv, int k, int Bk,
                              int32_t* pt, int32_t* n, int32_t* last_len, int32_t* dev_err,
-                             cudaStream_t stream);
+                             cudaStream_t stream, int S = 1, const int32_t* q_pos = nullptr);
 msa_status launch_attn_decode(const msa_decode_args& a, float* o_part, float* lse_part, int32_t* counter,
                               cudaStream_t stream);
 msa_status launch_lse_merge(const float* o_part, const float* lse_part, int64_t rows, int parts, int D,
@@ -61,6 +61,7 @@ constexpr int kMaxK = 64;
 constexpr int kMaxHI = 4;
 constexpr int kMaxG = 8;
 constexpr int kMaxDecodeBatch = 4096;
+constexpr int kChunkDecodeMaxS = 8;   // chunk attention through the decode kernel for S <= this
 constexpr int kDenseMaxBatch = 1024;   // dense comparator: sequences per call
 constexpr int kDenseMaxGrid = 256;     // dense decode: CTAs per launch (at most)
 

@@ -265,10 +265,18 @@ msa_status msa_build_page_table(const int32_t *sel, const int32_t *count,
  *   MSA_DEVERR_BAD_PAGE; either slot is ignored.  Pool slots past a sequence's
  *   last token must hold finite values (a zero-filled pool does): their
  *   probabilities are 0, and 0 times a NaN or an infinity is NaN.
+ *   With S <= 8 queries per sequence (a few decode tokens, e.g. draft
+ *   verification), Q dense over (b, s) (Q_stride[0] = S * Q_stride[1]) and K,
+ *   V with equal strides, the rows (b, s, g) run as a decode batch of B * S
+ *   sequences through the paged decode attention (a page table of each row's
+ *   selected pages, then one attention launch with the merge fused); the
+ *   workspace then holds that path's page table and partials and does not
+ *   depend on chunk_queries.
  * Workspace: caller-owned device scratch of ws_bytes.  Queries are processed in
  * chunks sized to fit; msa_sparse_attn_prefill_workspace_size(args, q) gives
  * the bytes needed for chunks of q queries (q >= 1; in CHUNK mode it reads
- * mode and max_pages too); larger workspaces mean fewer passes.  The workspace must stay untouched until the stream has run
+ * mode, max_pages and the Q, K and V strides too); larger workspaces mean
+ * fewer passes.  The workspace must stay untouched until the stream has run
  * the call.  softmax_scale <= 0 selects 1 / sqrt(D).
  * ------------------------------------------------------------------------ */
 typedef struct msa_prefill_args {

@@ -51,3 +51,22 @@ def test_oracle_baselines_on_small_workloads():
     r = bench.cpu_chunk_baseline(cw, chunk_inputs(cw), budget_s=0.05)
     assert r["value"] > 0 and "query offsets" in r["sample"]
     assert math.isfinite(r["value"])
+
+
+def test_dense_comparator_work_by_hand():
+    """Dense decode reads every cached K and V token once (plus Q, O); a dense
+    causal prefill does 4*D FLOPs per (query head, visible key), S(S+1)/2 keys
+    per head."""
+    sh = MSAShape(Hq=4, Hkv=2, HI=4, k=2)
+    wl = DecodeWorkload("t", lengths=(129, 300), shape=sh, seed=0)
+    assert bench.dense_decode_bytes(wl) == (129 + 300) * 2 * 128 * 2 * 2 + 2 * 4 * 128 * 2 * 2
+    pw = PrefillWorkload("p", B=2, S=3, shape=sh, seed=0)
+    assert bench.dense_prefill_flops(pw) == 4 * 128 * 4 * 2 * (1 + 2 + 3)
+
+
+def test_decode_baseline_reports_one_thread_rate():
+    sh = MSAShape(Hq=4, Hkv=1, HI=2, k=4)
+    wl = DecodeWorkload("d", lengths=(300, 129), shape=sh, seed=3)
+    from workloads import decode_inputs
+    r = bench.cpu_decode_baseline(wl, decode_inputs(wl), budget_s=0.05)
+    assert r["value"] > 0 and r["value_1_thread"] > 0 and "single" not in r["sample"]

@@ -133,11 +133,13 @@ def test_chunk_small_workspace_is_bit_identical(msa):
         assert torch.equal(a[name], b[name]), name
 
 
-def test_chunk_rejected_sequence_and_page(msa):
+@pytest.mark.parametrize("S", [100, 4], ids=["kv_block_major", "decode_path"])
+def test_chunk_rejected_sequence_and_page(msa, S):
     """A sequence whose chunk leaves the pages gets count 0, zero output and
     LSE -inf (MSA_DEVERR_BAD_LEN); a page id outside the pool is reported
-    (MSA_DEVERR_BAD_PAGE) and the other sequences are unaffected."""
-    wl = ChunkWorkload("bad", prefix=(1000, 600, 300), S=100, shape=MSAShape(Hq=12, Hkv=2, k=4), seed=70)
+    (MSA_DEVERR_BAD_PAGE) and the other sequences are unaffected.  S = 4 runs
+    the attention through the decode kernel."""
+    wl = ChunkWorkload("bad", prefix=(1000, 600, 300), S=S, shape=MSAShape(Hq=12, Hkv=2, k=4), seed=70)
     inp = chunk_inputs(wl, device="cuda")
     good = run_chunk(msa, inp, wl.shape.k)
     bad = dict(inp)
@@ -157,6 +159,27 @@ def test_chunk_rejected_sequence_and_page(msa):
     # the block on the missing page is not loaded: -inf in every row of that sequence
     assert torch.isneginf(bufs["C"][2, :, :, 0]).all()
     assert torch.equal(bufs["C"][2, :, :, 1:], good["C"][2, :, :, 1:])
+
+
+def test_chunk_few_queries_run_through_the_decode_kernel(msa):
+    """S <= 8 with a dense Q: the workspace is that of the decode path (page
+    table and fp32 partials of B*S*Hq*k parts) whatever the query chunk, and
+    the outputs match the oracle (checked in the verify cases above); here a
+    4-token verification at the MSA shape also agrees with four one-token
+    chunk calls at consecutive positions, which take the same path."""
+    wl = ChunkWorkload("few", prefix=(5000, 777), S=4, shape=MSAShape(), seed=74)
+    inp = chunk_inputs(wl, device="cuda")
+    sel_probe = torch.empty(1, 1, 1, wl.shape.k, dtype=torch.int32)
+    a = msa.msa_sparse_attn_prefill_workspace_size(inp["Q"], inp["K_pool"], sel_probe, 1, max_pages=wl.max_pages)
+    b = msa.msa_sparse_attn_prefill_workspace_size(inp["Q"], inp["K_pool"], sel_probe, 8, max_pages=wl.max_pages)
+    assert a == b >= wl.B * wl.S * wl.shape.Hq * wl.shape.k * (wl.shape.D + 1) * 4
+    whole = run_chunk(msa, inp, wl.shape.k)
+    for s in range(wl.S):
+        one = dict(inp, Q=inp["Q"][:, s:s + 1].contiguous(), q_idx=inp["q_idx"][:, s:s + 1].contiguous(),
+                   w=inp["w"][:, s:s + 1].contiguous(), q_pos=inp["q_pos"] + s)
+        got = run_chunk(msa, one, wl.shape.k)
+        for name in ("sel", "count", "O", "LSE"):
+            assert torch.equal(got[name][:, 0], whole[name][:, s]), (name, s)
 
 
 def test_chunk_rejects_a_sequence_whose_last_query_leaves_the_pages(msa):

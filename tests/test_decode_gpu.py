@@ -285,6 +285,8 @@ def test_cache_append_matches_oracle(msa, bad, shared):
 SHARED_INDEX = [
     DecodeWorkload("shared_edges", lengths=(1, 2, 127, 128, 129, 257, 1000, 2049, 5000), shape=MSAShape(), seed=62),
     DecodeWorkload("shared_hkv4", lengths=(3000, 20000, 640), shape=MSAShape(Hq=24, Hkv=4, k=16), seed=63),
+    # rows of more than 2048 blocks: a sequence's 8 group rows complete together and are selected side by side
+    DecodeWorkload("shared_long", lengths=(300000, 270000, 1000), shape=MSAShape(), seed=64),
 ]
 
 
