@@ -184,7 +184,7 @@ def read_profile_traffic(name: str, kernel_files):
     if kv.get("source_sha256_16") != source_hash(kernel_files):
         return None, "kernel changed since the capture"
     try:
-        return float(kv["dram_bytes_per_launch"]), p
+        return float(kv["dram_bytes_per_launch"]), os.path.relpath(p, ROOT)
     except (KeyError, ValueError):
         return None, "no dram bytes in profile"
 
@@ -867,6 +867,8 @@ def main():
     ap.add_argument("--shared-index", action="store_true",
                     help="decode with one index-key pool for all KV groups (k_idx group stride 0)")
     ap.add_argument("--seq", type=int, default=None, help="override the prefill sequence length (profiling)")
+    ap.add_argument("--dense", action="store_true",
+                    help="time only the dense comparator on the workload's inputs (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -932,6 +934,13 @@ def main():
         raise SystemExit("bench.py needs a CUDA device for --impl ours")
     from block_sparse_attention_02_gb300 import build as b
     b.build()
+    if args.dense:
+        res = run_dense_ours(args, wl, world, rank)
+        res.update({"metric": METRIC, "n_gpus": world, "higher_is_better": True, "scaling": "weak",
+                    "vs_baseline": None, "dtype": "bf16", "data": "synthetic"})
+        if rank == 0:
+            print(json.dumps(res))
+        return
     res = run_workload(args, wl, world, rank)
     extra = [x for x in args.also.split(",") if x] if args.workload == DEFAULT_WORKLOAD and args.seq is None else []
     if extra:
