@@ -259,7 +259,7 @@ def pack_tensors(ts, device):
     for n, t in ts.items():
         offs[n] = total
         total += (t.numel() * t.element_size() + 255) // 256 * 256
-    pack = torch.empty(total, dtype=torch.uint8, device=device)
+    pack = torch.zeros(total, dtype=torch.uint8, device=device)   # alignment padding stays zero
     views = {}
     for n, t in ts.items():
         nbytes = t.numel() * t.element_size()
@@ -288,21 +288,26 @@ def run_decode_ours(args, wl, world, rank):
     out_pack, out_views = pack_tensors({n: bufs[n] for n in ("O", "LSE")}, "cuda")
     bufs.update(out_views)
 
-    def index_part():
-        # a1 index score with a2 selection and a3 page table fused into the same kernel
-        msa.msa_index_score(msa.MSA_MODE_DECODE, inp["q_idx"], inp["w"], inp["kidx_pool"], bufs["C"],
-                            seq_pt=inp["seq_pt"], seq_len=inp["seq_len"], dev_err=bufs["dev_err"], k=sh.k,
-                            sel=bufs["sel"], count=bufs["count"], pt=bufs["pt"], n=bufs["n"],
-                            last_len=bufs["last_len"], row_scratch=bufs["row_scratch"], scratch_zeroed=True)
+    def make_parts(inp, bufs):
+        def index_part():
+            # a1 index score with a2 selection and a3 page table fused into the same kernel
+            msa.msa_index_score(msa.MSA_MODE_DECODE, inp["q_idx"], inp["w"], inp["kidx_pool"], bufs["C"],
+                                seq_pt=inp["seq_pt"], seq_len=inp["seq_len"], dev_err=bufs["dev_err"], k=sh.k,
+                                sel=bufs["sel"], count=bufs["count"], pt=bufs["pt"], n=bufs["n"],
+                                last_len=bufs["last_len"], row_scratch=bufs["row_scratch"], scratch_zeroed=True)
 
-    def rest_part():
-        e = bufs["dev_err"]
-        msa.msa_sparse_attn_decode(inp["Q"], inp["K_pool"], inp["V_pool"], bufs["pt"], bufs["n"], bufs["last_len"],
-                                   bufs["O"], bufs["LSE"], bufs["ws"], dev_err=e, scratch_zeroed=True)
+        def rest_part():
+            e = bufs["dev_err"]
+            msa.msa_sparse_attn_decode(inp["Q"], inp["K_pool"], inp["V_pool"], bufs["pt"], bufs["n"],
+                                       bufs["last_len"], bufs["O"], bufs["LSE"], bufs["ws"], dev_err=e,
+                                       scratch_zeroed=True)
 
-    def step():
-        index_part()
-        rest_part()
+        def step():
+            index_part()
+            rest_part()
+        return index_part, rest_part, step
+
+    index_part, rest_part, step = make_parts(inp, bufs)
 
     # warm up eagerly (sets kernel attributes), then capture the whole step in one CUDA graph
     for _ in range(max(1, args.warmup)):
@@ -388,23 +393,80 @@ def run_decode_ours(args, wl, world, rank):
     rest_ms = per_call["attention+merge"]
 
     # ---- end to end through the C ABI with host buffers ----
-    host_in = in_pack.cpu().pin_memory()          # the step inputs, packed as on the device
-    host_out = torch.empty_like(out_pack, device="cpu").pin_memory()
-    h2d = host_in.numel()
-    d2h = host_out.numel()
+    # Every step copies its inputs in from pinned host memory and its O and
+    # LSE out.  Without an L2 flush the copies are pipelined: two sets of
+    # device packs (and a graph per set) alternate between steps, the copy in
+    # of step i+1 runs on one copy stream while step i computes, and the copy
+    # out of step i on another while step i+1 computes.  With a flush between
+    # steps each step runs copy in -> step -> copy out on one stream.
+    host_in = [in_pack.cpu().pin_memory(), in_pack.cpu().pin_memory()]   # the step inputs, packed
+    host_out = [torch.empty_like(out_pack, device="cpu").pin_memory() for _ in range(2)]
+    h2d = host_in[0].numel()
+    d2h = host_out[0].numel()
+    pipelined = graphs and not l2.enabled
+    if pipelined:
+        inp2, bufs2 = dict(inp), dict(bufs)
+        in_pack2, in_views2 = pack_tensors({n: inp[n] for n in step_in}, "cuda")
+        inp2.update(in_views2)
+        out_pack2, out_views2 = pack_tensors({n: bufs[n] for n in ("O", "LSE")}, "cuda")
+        bufs2.update(out_views2)
+        step2 = make_parts(inp2, bufs2)[2]
+        step2()
+        torch.cuda.synchronize()
+        g_step2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_step2):
+            step2()
+        packs_in, packs_out, runs = [in_pack, in_pack2], [out_pack, out_pack2], [run_step, g_step2.replay]
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_comp = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        in_pack.copy_(host_in, non_blocking=True)
-        run_step()
-        host_out.copy_(out_pack, non_blocking=True)
+        def e2e_steps(nsteps):
+            """nsteps pipelined steps; returns their device milliseconds (copy in of the first to copy out of the last)."""
+            t_a, t_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t_a.record(stream)
+            s_in.wait_event(t_a)
+            s_out.wait_event(t_a)
+            for i in range(nsteps):
+                x = i & 1
+                with torch.cuda.stream(s_in):
+                    if i >= 2:
+                        s_in.wait_event(ev_comp[x])        # step i-2 has read this input pack
+                    packs_in[x].copy_(host_in[x], non_blocking=True)
+                    ev_in[x].record(s_in)
+                stream.wait_event(ev_in[x])
+                if i >= 2:
+                    stream.wait_event(ev_out[x])            # step i-2's outputs have left this pack
+                runs[x]()
+                ev_comp[x].record(stream)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(ev_comp[x])
+                    host_out[x].copy_(packs_out[x], non_blocking=True)
+                    ev_out[x].record(s_out)
+            stream.wait_event(ev_out[(nsteps - 1) & 1])
+            t_b.record(stream)
+            torch.cuda.synchronize()
+            return t_a.elapsed_time(t_b)
 
-    for _ in range(args.warmup):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    e2e_total = l2.time(e2e_step, K, stream)
-    barrier(world)
+        e2e_steps(args.warmup)
+        barrier(world)
+        e2e_total = e2e_steps(K)
+        barrier(world)
+    else:
+        def e2e_step():
+            in_pack.copy_(host_in[0], non_blocking=True)
+            run_step()
+            host_out[0].copy_(out_pack, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_total = l2.time(e2e_step, K, stream)
+        barrier(world)
     e2e_ms = max_over_ranks(e2e_total, world)
+    assert torch.equal(host_out[0], host_out[1]) or not pipelined, "the two output packs differ"
 
     peaks = load_peaks()
     achieved = alg["index_kernel"] / (idx_ms * 1e-3) / 1e9
@@ -438,11 +500,13 @@ def run_decode_ours(args, wl, world, rank):
         "breakdown_ms": {"index_score+topk+page_table": idx_ms, "attention+merge": rest_ms,
                          "per_call_graphs": per_call},
         "e2e": {"value": tokens_per_step / (e2e_ms / K * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "copies": ("pipelined: copy in and copy out on two streams, overlapping the neighbouring steps"
+                           if pipelined else "serial: copy in, step, copy out on one stream")},
         "gpu_launches": 2 * K,
         "clocks": clocks,
     }
-    return res, host_in, inp
+    return res, host_in[0], inp
 
 
 def oracle_decode_step(h, sh):
