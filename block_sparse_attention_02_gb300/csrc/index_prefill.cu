@@ -644,14 +644,19 @@ msa_status launch_index_prefill(const msa_index_args& a, cudaStream_t stream) {
   const Kern kern = (!chunk ? kPrefill : a.S <= kCQ ? kFew : kChunk)[a.HI - 1];
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(index_prefill)");
-  // Too few items for two per slot of every CTA: split each item's key
+  // Too few items for many per slot of every CTA: split each item's key
   // blocks into ranges of at least 16 blocks (the longest row has at most
-  // max_own blocks before its own).
+  // max_own blocks before its own).  A chunk's items all have about the same
+  // length (the cached prefix), so a few per slot leave the CTAs unevenly
+  // loaded (3 or 4 pairs a CTA for an 8,192-query chunk of 8 KV groups);
+  // about sixteen items per CTA keep the spread small.  (Prefill items, long and short
+  // paired, are not split.)
   const int64_t items = static_cast<int64_t>(a.B) * a.Hkv * p.nq;
-  const int64_t want = 4 * static_cast<int64_t>(dev.num_sms);
-  const int64_t max_own = chunk ? a.max_pages : (a.S - 1) / kBk;
-  p.nsplit = items >= want ? 1 : static_cast<int>(std::max<int64_t>(1, std::min((want + items - 1) / items,
-                                                                                   max_own / 16)));
+  const int64_t want = 16 * static_cast<int64_t>(dev.num_sms);
+  const int64_t max_own = a.max_pages;
+  p.nsplit = !chunk || items >= want
+                  ? 1
+                  : static_cast<int>(std::max<int64_t>(1, std::min((want + items - 1) / items, max_own / 16)));
   const int64_t npairs = static_cast<int64_t>(a.B) * a.Hkv * ((p.nq + 1) / 2) * p.nsplit;
   if (npairs >= (int64_t(1) << 31)) return fail(MSA_ERR_UNSUPPORTED, "prefill index score: too many query blocks");
   const int grid = static_cast<int>(std::min<int64_t>(dev.num_sms, std::max<int64_t>(npairs, 1)));
