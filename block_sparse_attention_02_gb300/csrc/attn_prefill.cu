@@ -464,10 +464,11 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
     // S(n) and O(n) are issued as soon as their inputs are ready, O first:
     //   O(n) needs P(n) (pready); the warpgroup that arrives there has already
     //   read O(n-2) out of the slot's accumulator;
-    //   S(n) needs Q(n), K_j, and O(n-2) complete: it overwrites the slot's S/P
-    //   columns, from which O(n-2) reads P (waiting for the completion barrier
-    //   rather than relying on issue order between an MMA's TMEM operand read
-    //   and a later MMA's TMEM write).
+    //   S(n) needs Q(n), K_j, and O(n-2) issued: it overwrites the slot's S/P
+    //   columns, from which O(n-2) reads P.  The MMAs of this one thread run
+    //   in issue order, so O(n-2) has read its P operand before S(n) writes
+    //   there, and S(n)'s commit (sfull) also covers O(n-2): the softmax
+    //   warpgroup writes P(n) only after both.
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_o = idesc_bf16(128, 128, false, true);
@@ -495,8 +496,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
         }
         if (ns < ntiles && ns < no + 2) {
           const int st = ns % kQStages, slot = ns & 1;
-          if ((ns < 2 || mbar_test_wait(&bar_ofull[slot], ((ns - 2) >> 1) & 1)) &&
-              mbar_test_wait(&bar_qfull[st], (ns / kQStages) & 1)) {
+          if (mbar_test_wait(&bar_qfull[st], (ns / kQStages) & 1)) {
             const int kv = s_kvinfo[st];
             if (!(kv & 2) || mbar_test_wait(&bar_kvfull[kv & 1], (kv >> 3) & 1)) {
               tc_fence_after();
