@@ -659,6 +659,13 @@ msa_status launch_index_decode(const msa_index_args& a, cudaStream_t stream) {
   p.dev_err = a.dev_err;
   p.k = a.k; p.sel = a.sel; p.count = a.count; p.pt = a.pt; p.n_out = a.n; p.last_len = a.last_len;
   p.counter = a.row_scratch;
+  // With one pool for all groups every group row of a sequence is completed
+  // by the same CTA, which would select them one after another; rows of more
+  // than 2048 blocks are therefore selected by the top-k kernel instead (one
+  // CTA per row, all rows at once) and mapped by the page-table kernel: the
+  // same outputs, two more launches.
+  const bool select_after = shared && a.sel != nullptr && a.nb_stride > 2048;
+  if (select_after) p.sel = nullptr;
 
   const size_t qtile = static_cast<size_t>(shared ? kSharedRows : 16) * kDI * 2;
   const size_t smem = 1024 + kStages * kStageBytes + 2 * qtile + (2 * static_cast<size_t>(a.B) + 1) * 4;
@@ -666,7 +673,7 @@ msa_status launch_index_decode(const msa_index_args& a, cudaStream_t stream) {
   auto kern = shared ? index_decode_kernel<true> : index_decode_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(index_decode)");
-  if (p.sel != nullptr && !a.scratch_zeroed) {   // otherwise zero by contract
+  if (p.sel != nullptr && !a.scratch_zeroed) {   // otherwise zero by contract (and unused without p.sel)
     e = cudaMemsetAsync(p.counter, 0, static_cast<size_t>(a.B) * a.Hkv * sizeof(int32_t), stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(index row counters)");
   }
@@ -674,7 +681,17 @@ msa_status launch_index_decode(const msa_index_args& a, cudaStream_t stream) {
   kern<<<grid, kThreads, smem, stream>>>(kmap, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "index_decode_kernel launch");
-  return MSA_OK;
+  if (!select_after) return MSA_OK;
+  msa_topk_args t{};
+  t.mode = MSA_MODE_DECODE;
+  t.B = a.B; t.S = 1; t.Hkv = a.Hkv; t.Bk = a.Bk; t.k = a.k;
+  t.C = a.C; t.C_stride[0] = a.C_stride[0]; t.C_stride[1] = a.C_stride[1]; t.C_stride[2] = 0;
+  t.nb_stride = a.nb_stride; t.seq_len = a.seq_len;
+  t.sel = a.sel; t.count = a.count; t.dev_err = a.dev_err; t.q_pos = nullptr;
+  if (msa_status st = launch_topk(t, stream); st != MSA_OK) return st;
+  if (a.pt == nullptr) return MSA_OK;
+  return launch_page_table(a.sel, a.count, a.seq_pt, a.max_pages, a.seq_len, a.B, a.Hkv, a.k, a.Bk, a.pt, a.n,
+                           a.last_len, a.dev_err, stream);
 }
 
 }  // namespace msa

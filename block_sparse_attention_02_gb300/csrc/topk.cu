@@ -14,7 +14,8 @@
 // Short rows (<= 2048 candidates: all prefill rows, chunk rows of contexts up
 // to 2049 blocks and short decode rows): one warp per row, the register
 // algorithm of select_warp.cuh.
-// Long rows: one 256-thread CTA per row, successive block-wide arg-max.
+// Long rows: one 256-thread CTA per row; its warps select the best blocks of
+// slices of the row, then the slices' picks are ranked together.
 #include "msa_internal.h"
 #include "msa_ptx.cuh"
 #include "select_warp.cuh"
@@ -92,9 +93,22 @@ topk_warp_kernel(const msa_topk_args a, int64_t rows) {
   if (lane == 0) *r.cnt = m + 1;
 }
 
-// One CTA per long row: m rounds of block-wide arg-max below the previous pick.
-__global__ void __launch_bounds__(kCtaThreads)
+// One CTA per long row, in two phases: the row is cut into at most kMaxSlices
+// slices (of at most 1024 blocks when that leaves no more than one slice per
+// warp, else 2048); each warp selects the best m of its slices with the
+// register warp select into a pool (slot slice * m + y; 0 = empty, below every
+// real key); then the pool's keys are ranked exactly and the m best are the
+// picks.  The row's best m blocks are all in the pool: a block outside its
+// slice's best m has m better blocks in that slice.  Rows of more than
+// kMaxSlices * 2048 blocks take m rounds of block-wide arg-max below the
+// previous pick instead.
+constexpr int kMaxSlices = 32;
+__global__ void __launch_bounds__(kCtaThreads, 1)
 topk_cta_kernel(const msa_topk_args a, int64_t rows) {
+  __shared__ uint64_t s_surv[kWarpsPerCta][kSelCap];
+  __shared__ int s_wpick[kWarpsPerCta][kMaxK];
+  __shared__ int s_wout[kWarpsPerCta][kMaxK];
+  __shared__ uint64_t s_pool[kMaxSlices * (kMaxK - 1)];
   __shared__ uint64_t s_wmax[kCtaThreads / 32];
   __shared__ uint64_t s_best;
   __shared__ int s_pick[kMaxK];
@@ -109,23 +123,53 @@ topk_cta_kernel(const msa_topk_args a, int64_t rows) {
     write_all(r, a.k, tid, kCtaThreads);
     return;
   }
-  uint64_t prev = ~0ull;
-  for (int t = 0; t < m; ++t) {
-    uint64_t best = 0;
-    for (int j = tid; j < n; j += kCtaThreads) {
-      const uint64_t K = comp_key(order_key(r.c[j]), j);
-      if (K < prev && K > best) best = K;
+  if (n <= kMaxSlices * 2048) {
+    const int nslices = n <= kWarpsPerCta * 1024 ? (n + 1023) / 1024 : (n + 2047) / 2048;
+    const int ssz = (n + nslices - 1) / nslices;     // <= 2048
+    for (int sl = wid; sl < nslices; sl += kWarpsPerCta) {
+      const int lo = sl * ssz, cnt = min(ssz, n - lo);
+      int* out = s_wout[wid];
+      int npick = m;
+      if (cnt <= m) {
+        for (int y = lane; y < cnt; y += 32) out[y] = y;
+        npick = cnt;
+      } else {
+        warp_select_any(r.c + lo, cnt, m, s_surv[wid], s_wpick[wid], out);
+      }
+      __syncwarp();
+      for (int y = lane; y < m; y += 32)
+        s_pool[sl * m + y] = y < npick ? comp_key(order_key(r.c[lo + out[y]]), lo + out[y]) : 0ull;
+      __syncwarp();
     }
-    best = warp_max_u64(best);
-    if (lane == 0) s_wmax[wid] = best;
     __syncthreads();
-    if (wid == 0) {
-      uint64_t v = lane < kCtaThreads / 32 ? s_wmax[lane] : 0ull;
-      v = warp_max_u64(v);
-      if (lane == 0) { s_pick[t] = comp_index(v); s_best = v; }
+    const int npool = nslices * m;
+    for (int x = tid; x < npool; x += kCtaThreads) {
+      const uint64_t kx = s_pool[x];
+      if (kx == 0ull) continue;
+      int rank = 0;
+      for (int y = 0; y < npool; ++y) rank += s_pool[y] > kx;
+      if (rank < m) s_pick[rank] = comp_index(kx);
     }
     __syncthreads();
-    prev = s_best;
+  } else {
+    uint64_t prev = ~0ull;
+    for (int t = 0; t < m; ++t) {
+      uint64_t best = 0;
+      for (int j = tid; j < n; j += kCtaThreads) {
+        const uint64_t K = comp_key(order_key(r.c[j]), j);
+        if (K < prev && K > best) best = K;
+      }
+      best = warp_max_u64(best);
+      if (lane == 0) s_wmax[wid] = best;
+      __syncthreads();
+      if (wid == 0) {
+        uint64_t v = lane < kCtaThreads / 32 ? s_wmax[lane] : 0ull;
+        v = warp_max_u64(v);
+        if (lane == 0) { s_pick[t] = comp_index(v); s_best = v; }
+      }
+      __syncthreads();
+      prev = s_best;
+    }
   }
   for (int t = tid; t < m; t += kCtaThreads) {
     const int jt = s_pick[t];

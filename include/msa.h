@@ -143,7 +143,10 @@ const char *msa_status_string(msa_status s);
  *   also performs a2 (exactly what msa_topk_blocks computes with this k) on
  *   each (b, g) row as soon as the row's scores are complete, and when `pt` is
  *   also non-NULL a3 (exactly what msa_build_page_table computes).  This saves
- *   two launches per decode step.  `row_scratch` is then required: B*Hkv int32
+ *   two launches per decode step.  With one index-key pool for all groups
+ *   (group stride 0) and nb_stride > 2048 the call instead launches the
+ *   top-k and page-table kernels after the scores (a sequence's group rows
+ *   would otherwise all be selected by one CTA); the outputs are the same.  `row_scratch` is then required: B*Hkv int32
  *   of caller scratch (one completion counter per row).  Outputs are those of
  *   a2 / a3: sel [B,Hkv,k], count [B,Hkv], pt [B*Hkv,k], n and last_len [B*Hkv].
  *   scratch_zeroed = 0: the call clears row_scratch first (one memset on the

@@ -245,6 +245,39 @@ def test_standalone_topk_and_page_table_match_oracle(msa, wl):
     assert np.array_equal(u["last_len"].numpy(), ll_o)
 
 
+LONG_ROWS = (2049, 5000, 8191, 8192, 8193, 20000, 65536, 70000)
+
+
+@pytest.mark.parametrize("k", [16, 64])
+@pytest.mark.parametrize("ties", [False, True], ids=["distinct", "few_values"])
+def test_topk_long_rows_match_oracle(msa, k, ties):
+    """msa_topk_blocks on decode rows of more than 2048 blocks (one CTA per
+    row: its warps select the best of slices of 1024 or 2048 blocks, the
+    slices' picks are ranked together; past 65,536 blocks successive
+    arg-max), against oracle.select on the same fp32 scores.  Own-block
+    counts sit on both sides of each switch; k = 64 makes the warp select keep
+    every candidate of a slice; rows of a few distinct values put thousands
+    of ties at the threshold (broken by block index)."""
+    g = torch.Generator().manual_seed(71 + k + int(ties))
+    own = torch.tensor(LONG_ROWS, dtype=torch.int64)
+    B, Hkv = len(LONG_ROWS), 2
+    nb = int(own.max()) + 1
+    C = torch.randn(B, Hkv, nb, generator=g)
+    if ties:
+        C = torch.round(C * 2) / 2
+    seq_len = (own * 128 + 1 + torch.arange(B) * 13 % 128).to(torch.int32)   # own block (L - 1) // 128
+    assert torch.equal((seq_len.long() - 1) // 128, own)
+    sel = torch.empty(B, Hkv, k, dtype=torch.int32, device="cuda")
+    count = torch.empty(B, Hkv, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    msa.msa_topk_blocks(msa.MSA_MODE_DECODE, C.cuda(), k, sel, count, seq_len=seq_len.cuda(), dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    sel_o, cnt_o, _, _ = oracle.select(C.double().numpy(), np.repeat(own.numpy(), Hkv).reshape(B, Hkv), k)
+    assert np.array_equal(count.cpu().numpy(), cnt_o)
+    assert np.array_equal(sel.cpu().numpy(), sel_o)
+
+
 def _bits(t):
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
@@ -285,7 +318,8 @@ def test_cache_append_matches_oracle(msa, bad, shared):
 SHARED_INDEX = [
     DecodeWorkload("shared_edges", lengths=(1, 2, 127, 128, 129, 257, 1000, 2049, 5000), shape=MSAShape(), seed=62),
     DecodeWorkload("shared_hkv4", lengths=(3000, 20000, 640), shape=MSAShape(Hq=24, Hkv=4, k=16), seed=63),
-    # rows of more than 2048 blocks: a sequence's 8 group rows complete together and are selected side by side
+    # rows of more than 2048 blocks: a sequence's 8 group rows complete together and are selected by the
+    # top-k kernel after the scores (one CTA per row)
     DecodeWorkload("shared_long", lengths=(300000, 270000, 1000), shape=MSAShape(), seed=64),
 ]
 
