@@ -516,23 +516,30 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
         wmax[0] = redux_max_u32(float_order_key(sg));
       }
       // cross-warp max without a barrier: the last of the four warps to arrive
-      // combines the partial maxima and stores the block score(s).
+      // combines the partial maxima and stores the block score(s), lane g
+      // taking group g.
+      const int rb = n % kRedBufs;
+      int last = 0;
       if (lane == 0) {
-        const int rb = n % kRedBufs;
 #pragma unroll
         for (int g = 0; g < NG; ++g) s_red[rb][q][g] = wmax[g];
         __threadfence_block();
-        if (atomicAdd(&s_cnt[rb], 1) == 3) {
+        last = atomicAdd(&s_cnt[rb], 1) == 3;
+        if (last) {
           __threadfence_block();
           s_cnt[rb] = 0;
-          const bool bad = page_cur < 0 || page_cur >= p.num_pages;
-          if (bad) report(p.dev_err, MSA_DEVERR_BAD_PAGE);
-          const int ng = SHARED ? p.Hkv : 1;
-          for (int g = 0; g < ng; ++g) {
-            const uint32_t mk = max(max(s_red[rb][0][g], s_red[rb][1][g]), max(s_red[rb][2][g], s_red[rb][3][g]));
-            const int gg = SHARED ? g : it.g;
-            p.C[it.b * p.cs0 + gg * p.cs1 + it.j] = bad ? -INFINITY : float_from_order_key(mk);
-          }
+        }
+      }
+      __syncwarp();
+      if (__shfl_sync(0xffffffffu, last, 0)) {
+        const bool bad = page_cur < 0 || page_cur >= p.num_pages;
+        if (bad && lane == 0) report(p.dev_err, MSA_DEVERR_BAD_PAGE);
+        const int ng = SHARED ? p.Hkv : 1;
+        if (lane < ng) {
+          const int g = SHARED ? lane : 0;
+          const uint32_t mk = max(max(s_red[rb][0][g], s_red[rb][1][g]), max(s_red[rb][2][g], s_red[rb][3][g]));
+          const int gg = SHARED ? g : it.g;
+          p.C[it.b * p.cs0 + gg * p.cs1 + it.j] = bad ? -INFINITY : float_from_order_key(mk);
         }
       }
       it = nxt;
