@@ -556,16 +556,24 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
 
   // ---- fused selection: the CTA whose scores complete a (b, g) row selects it ----
   if (p.sel != nullptr && !*abort_flag && count > 0) {
-    __shared__ int s_rows[kThreads], s_long[kThreads];
     __shared__ int s_nrows, s_nlong;
-    __shared__ uint64_t s_w[kThreads / 32 + 1];
-    __shared__ int s_picks[kThreads / 32][kMaxK];
-    __shared__ int s_out[kThreads / 32][kMaxK];
-    __shared__ int s_final[kMaxK];
-    uint8_t* ring = s_stage;                          // the TMA ring is idle now
+    // The TMA ring is idle now and holds the selection's scratch (static
+    // shared memory would keep two CTAs of the shared-index variant from
+    // fitting on one SM): survivors per warp at the start, the small arrays
+    // at the end, staged keys in between.
+    constexpr int kWarps = kThreads / 32;
+    constexpr int kSmallBytes = 8 * (kWarps + 2) + 2 * kWarps * kMaxK * 4 + kMaxK * 4 + 2 * kThreads * 4;
+    uint8_t* ring = s_stage;
     uint64_t* s_surv = reinterpret_cast<uint64_t*>(ring);                  // [warps][kSelCap]
-    uint64_t* s_keys = reinterpret_cast<uint64_t*>(ring + (kThreads / 32) * kSelCap * 8);
-    const int key_cap = (kStages * kStageBytes - (kThreads / 32) * kSelCap * 8) / 8;
+    uint8_t* small = ring + kStages * kStageBytes - kSmallBytes;
+    uint64_t* s_w = reinterpret_cast<uint64_t*>(small);                     // [warps + 1]
+    int (*s_picks)[kMaxK] = reinterpret_cast<int (*)[kMaxK]>(small + 8 * (kWarps + 2));
+    int (*s_out)[kMaxK] = s_picks + kWarps;
+    int* s_final = reinterpret_cast<int*>(s_out + kWarps);                  // [kMaxK]
+    int* s_rows = s_final + kMaxK;                                          // [kThreads]
+    int* s_long = s_rows + kThreads;                                        // [kThreads]
+    uint64_t* s_keys = reinterpret_cast<uint64_t*>(ring + kWarps * kSelCap * 8);
+    const int key_cap = (kStages * kStageBytes - kWarps * kSelCap * 8 - kSmallBytes) / 8;
     const int m = p.k - 1;
     __threadfence();                                   // this CTA's scores, device-wide
     // this CTA's items cover the contiguous rows r_first .. r_last
@@ -684,6 +692,11 @@ msa_status launch_index_decode(const msa_index_args& a, cudaStream_t stream) {
     e = cudaMemsetAsync(p.counter, 0, static_cast<size_t>(a.B) * a.Hkv * sizeof(int32_t), stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(index row counters)");
   }
+  // Two CTAs per SM, all resident at once: with the 1 KB the system keeps per
+  // CTA, two fit up to B = 1024 with per-group keys and B = 256 with a shared
+  // pool; a larger shared-pool batch runs the grid in two waves.
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(index_decode carveout)");
   const int grid = dev.num_sms * kCtasPerSm;
   kern<<<grid, kThreads, smem, stream>>>(kmap, p);
   e = cudaGetLastError();
