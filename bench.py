@@ -193,6 +193,10 @@ def read_profile_traffic(name: str, kernel_files):
 # decode workload
 # ---------------------------------------------------------------------------
 
+PREFILL_ATTN_FILES = ["block_sparse_attention_02_gb300/csrc/attn_prefill.cu",
+                      "block_sparse_attention_02_gb300/csrc/msa_ptx.cuh"]
+DENSE_FILES = {k: [f"block_sparse_attention_02_gb300/csrc/dense_{k}.cu", "block_sparse_attention_02_gb300/csrc/msa_ptx.cuh"]
+               for k in ("decode", "prefill")}
 DECODE_INDEX_FILES = ["block_sparse_attention_02_gb300/csrc/index_decode.cu",
                       "block_sparse_attention_02_gb300/csrc/msa_ptx.cuh",
                       "block_sparse_attention_02_gb300/csrc/select_warp.cuh"]
@@ -677,6 +681,8 @@ def run_prefill_ours(args, wl, world, rank):
     peaks = load_peaks()
     tc = flops / (part_ms[2] * 1e-3) / 1e12
     step_ms = total_ms / K
+    # DRAM bytes of the whole stage (CSR, attention, merge) of one layer
+    traffic, traffic_src = read_profile_traffic(f"attn_stage_{wl.name}.txt", PREFILL_ATTN_FILES)
     res = {
         "metric": METRIC, "value": wl.B * wl.S * world / (step_ms * 1e-3), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
@@ -686,8 +692,9 @@ def run_prefill_ours(args, wl, world, rank):
                    "l2": "no flush: inputs larger than L2", "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "kernel": "sparse attention (a4+a6)", "achieved": tc,
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": tc / peaks["bf16_tflops"],
-                     "peak_src": peaks["src"], "traffic": None, "algorithmic_flops_per_launch": flops,
-                     "launch_ms": part_ms[2],
+                     "peak_src": peaks["src"], "traffic": traffic, "traffic_src": traffic_src,
+                     "traffic_gbs": None if traffic is None else traffic / (part_ms[2] * 1e-3) / 1e9,
+                     "algorithmic_flops_per_launch": flops, "launch_ms": part_ms[2],
                      "index_tflops": idx_flops / (part_ms[0] * 1e-3) / 1e12,
                      "index_frac": idx_flops / (part_ms[0] * 1e-3) / 1e12 / peaks["bf16_tflops"]},
         "breakdown_ms": {"index_score": part_ms[0], "topk": part_ms[1], "sparse_attention": part_ms[2]},
@@ -866,7 +873,10 @@ def run_dense_ours(args, wl, world, rank):
         ach = work / (step_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "kernel": "dense_prefill_kernel", "achieved": ach, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "algorithmic_flops_per_launch": work}
-    roof.update({"peak_src": peaks["src"], "traffic": None, "launch_ms": step_ms})
+    kind = "decode" if decode else "prefill"
+    short = wl.name[len("decode_"):] if decode else wl.name[len("prefill_"):]
+    traffic, traffic_src = read_profile_traffic(f"dense_{kind}_{short}_dram.txt", DENSE_FILES[kind])
+    roof.update({"peak_src": peaks["src"], "traffic": traffic, "traffic_src": traffic_src, "launch_ms": step_ms})
     res = {"value": tokens * world / (step_ms * 1e-3), "unit": UNIT, "ms_per_step": step_ms, "steps": K,
            "warmup": args.warmup,
            "config": {"workload": wl.name, "comparator": "dense attention over every token (no index branch)",
