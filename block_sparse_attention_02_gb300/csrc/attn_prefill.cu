@@ -49,7 +49,7 @@ constexpr int kEntries = 16;          // queries (entries) per tile, 8 rows each
 constexpr int kHalf = 128 * 64 * 2;   // 16 KiB: 128 rows x 64 bf16, 128-byte swizzled
 constexpr int kQStage = 2 * kHalf;    // 32 KiB: 128 rows x 128
 constexpr int kKV = 4 * kHalf;        // 64 KiB: K (2 halves) + V (2 halves)
-constexpr int kEntryPart = 16 * 8 * 8; // bf16 elements of one entry's partial: 16 chunks x 8 rows x 8
+constexpr int kEntryPart = 16 * 8 * 8; // bf16 elements reserved per entry's partial (16 chunks x G <= 8 rows x 8)
 constexpr int kTmemCols = 512;        // 2 slots x (S/P 128 + O 128)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -280,7 +280,7 @@ struct AttnParams {
   const int32_t* tile_off;   // tile_off[n_items] = number of tiles
   const int4* tile_info;
   const int32_t* tile_q;
-  __nv_bfloat16* o_part;     // [tiles][16 entries][16 column chunks][8 head rows][8] bf16
+  __nv_bfloat16* o_part;     // [tiles][16 entries][16 column chunks][G head rows][8] bf16, entries kEntryPart apart
   float* lse_part;           // [tiles * 128]
   int32_t* dev_err;
 };
@@ -651,11 +651,14 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
       const float inv = 1.0f / l;
       const uint64_t inv2 = pack2f(inv, inv);
       const int64_t prow = (t0 + n) * 128 + r;
-      // partial layout: one contiguous 2 KiB block per tile entry (a query's
-      // partial for this block, all its heads), [16-byte column chunk][head
-      // row] inside: the merge reads each (query, slot) partial as one block,
-      // and each store of a warp writes four whole 128-byte lines
+      // partial layout: one contiguous block of G * 256 bytes per tile entry
+      // (a query's partial for this block, all its heads; entries 2 KiB
+      // apart), [16-byte column chunk][head row] inside, no padding rows: the
+      // merge reads each (query, slot) partial as exactly its G * 256 bytes
+      // (with 8-row groups DRAM also fetched the two padding rows of every
+      // 128-byte line)
       __nv_bfloat16* obase = p.o_part + ((t0 + n) * kEntries + e) * kEntryPart + h * 8;
+      const int cstride = p.G * 8;                   // elements per 16-byte column chunk
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t v[2][32];
@@ -676,7 +679,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
                 w4[x] = pack_bf16x2(a0, a1);
               }
               const int chunk = hh * 8 + c * 4 + (e8 >> 3);
-              st_cs_v4(obase + chunk * 64, w4[0], w4[1], w4[2], w4[3]);
+              st_cs_v4(obase + chunk * cstride, w4[0], w4[1], w4[2], w4[3]);
             }
           }
         }
@@ -700,7 +703,8 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
 // merge: O = sum_s e^{LSE_s - LSE} O_s, LSE = ln sum_s e^{LSE_s} over the k
 // slots of each (query, head).  One warp per (query, group): lane L owns head
 // h = L % 8 (idle if h >= G) and the column chunks c = L / 8 + 4x, x = 0..3,
-// so that for each part the 8 lanes of a chunk read its 8 contiguous rows.
+// so that for each part and x the live lanes read chunks 4x .. 4x+3 of all G
+// rows: one contiguous run of 4 * G * 16 bytes.
 // ---------------------------------------------------------------------------
 
 constexpr int kMergeWarps = 8;
@@ -777,9 +781,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 2) prefill_merge_kernel(cons
       const int b = __shfl_sync(0xffffffffu, base[y], src_lane);
       if (live && b >= 0 && w4[u] != 0.f) {
         const int64_t t = b >> 7, eb = (b & 127) >> 3;
-        const __nv_bfloat16* src = p.o_part + (t * kEntries + eb) * kEntryPart + c0 * 64 + h * 8;
+        const int cstride = p.G * 8;         // [chunk][G head rows][8] per entry
+        const __nv_bfloat16* src = p.o_part + (t * kEntries + eb) * kEntryPart + c0 * cstride + h * 8;
 #pragma unroll
-        for (int x = 0; x < 4; ++x) raw[u][x] = __ldcs(reinterpret_cast<const uint4*>(src + x * 4 * 64));
+        for (int x = 0; x < 4; ++x) raw[u][x] = __ldcs(reinterpret_cast<const uint4*>(src + x * 4 * cstride));
       } else {
         w4[u] = 0.f;
       }
