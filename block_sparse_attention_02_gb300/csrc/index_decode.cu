@@ -52,6 +52,9 @@ constexpr int kRedBufs = 2 * kSlots;
 
 struct Params {
   int B, Hkv, HI, Bk;
+  int S;                                  // multi-token mode: tokens per sequence (1 otherwise)
+  const int32_t* q_pos;                   // multi-token mode: position of token 0 of sequence b
+  int64_t qs_s, ws_s, cs_s;               // multi-token mode: q_idx, w and C strides of the token
   const __nv_bfloat16* q_idx;
   int64_t qs0, qs1, qs2;
   const float* w;
@@ -235,12 +238,17 @@ __device__ void select_long_row(const Params& p, int b, int g, int own, uint64_t
   __syncthreads();
 }
 
-template <bool SHARED>
+// SHARED: one index-key pool for all groups, items (b, j), B rows (g, h).
+// MQ (multi-token): S <= 8 tokens per sequence at positions q_pos[b] + s over
+// per-group keys, items (b, g, j), B rows (s, h) with h < HI <= 4; token s
+// keeps the blocks before its own, (q_pos[b] + s) / Bk.
+template <bool SHARED, bool MQ>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
-  constexpr int QROWS = SHARED ? kSharedRows : 16;            // rows of the B operand (N)
-  constexpr int SLOT = SHARED ? kSharedRows : kSlotCols;      // TMEM columns per slot
-  constexpr int TCOLS = SHARED ? 2 * kTmemCols : kTmemCols;
+  constexpr bool WIDE = SHARED || MQ;                          // 32 B rows, 8 sums per token
+  constexpr int QROWS = WIDE ? kSharedRows : 16;              // rows of the B operand (N)
+  constexpr int SLOT = WIDE ? kSharedRows : kSlotCols;        // TMEM columns per slot
+  constexpr int TCOLS = WIDE ? 2 * kTmemCols : kTmemCols;
   constexpr int QTILE = QROWS * kDI * 2;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -248,6 +256,7 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
   uint8_t* s_q = smem + kStages * kStageBytes;               // 2 q_idx tiles
   int* s_pre = reinterpret_cast<int*>(s_q + 2 * QTILE);      // B + 1
   int* s_own = s_pre + (p.B + 1);                             // B
+  int* s_q0 = s_own + p.B;                                    // B (multi-token mode): q_pos, -1 if rejected
   // items per (b, j): one per group, or one for all groups with a shared index
   const int hkv_items = SHARED ? 1 : p.Hkv;
 
@@ -256,7 +265,7 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
   __shared__ __align__(8) uint64_t bar_qdone[2], bar_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ uint32_t s_red[kRedBufs][4][SHARED ? 8 : 1];
+  __shared__ uint32_t s_red[kRedBufs][4][WIDE ? 8 : 1];
   __shared__ int s_cnt[kRedBufs];
   __shared__ int s_chunk[kThreads];
 
@@ -264,12 +273,23 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
 
   // ---- per-sequence own blocks and the prefix over (b, g, j) items ----
   for (int b = tid; b < p.B; b += kThreads) {
-    const int L = p.seq_len[b];
     int own = 0;
-    if (L < 1 || static_cast<int64_t>(L) > p.max_pages * p.Bk || (L - 1) / p.Bk >= p.nb_stride) {
-      if (blockIdx.x == 0) report(p.dev_err, MSA_DEVERR_BAD_LEN);
+    if constexpr (MQ) {
+      // the items score the blocks before the last token's own block; a
+      // sequence is rejected as a whole when its tokens start before 0 or the
+      // last one leaves the pages or the score rows
+      const int64_t q0 = p.q_pos[b], last = q0 + p.S - 1;
+      const bool ok = q0 >= 0 && last < p.max_pages * p.Bk && last / p.Bk < p.nb_stride;
+      if (!ok && blockIdx.x == 0) report(p.dev_err, MSA_DEVERR_BAD_LEN);
+      own = ok ? static_cast<int>(last / p.Bk) : 0;
+      s_q0[b] = ok ? static_cast<int>(q0) : -1;
     } else {
-      own = (L - 1) / p.Bk;
+      const int L = p.seq_len[b];
+      if (L < 1 || static_cast<int64_t>(L) > p.max_pages * p.Bk || (L - 1) / p.Bk >= p.nb_stride) {
+        if (blockIdx.x == 0) report(p.dev_err, MSA_DEVERR_BAD_LEN);
+      } else {
+        own = (L - 1) / p.Bk;
+      }
     }
     s_own[b] = own;
   }
@@ -306,16 +326,24 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
 
   // ---- -inf for the own block and everything after it ----
   {
-    const int64_t total = static_cast<int64_t>(p.B) * p.Hkv * p.nb_stride;
+    // rows (b, g), or (b, s, g) in multi-token mode (token s: from its own block on)
+    const int64_t total = static_cast<int64_t>(p.B) * p.S * p.Hkv * p.nb_stride;
     for (int64_t e = static_cast<int64_t>(blockIdx.x) * kThreads + tid; e < total;
          e += static_cast<int64_t>(gridDim.x) * kThreads) {
       int j = static_cast<int>(e % p.nb_stride);
-      int64_t bg = e / p.nb_stride;
-      int b = static_cast<int>(bg / p.Hkv), g = static_cast<int>(bg % p.Hkv);
-      if (j >= s_own[b]) p.C[b * p.cs0 + g * p.cs1 + j] = -INFINITY;
+      int64_t r = e / p.nb_stride;
+      const int g = static_cast<int>(r % p.Hkv);
+      r /= p.Hkv;
+      const int tk = static_cast<int>(r % p.S), b = static_cast<int>(r / p.S);
+      if constexpr (MQ) {
+        const int own_t = s_q0[b] < 0 ? 0 : (s_q0[b] + tk) / p.Bk;
+        if (j >= own_t) p.C[b * p.cs0 + tk * p.cs_s + g * p.cs1 + j] = -INFINITY;
+      } else {
+        if (j >= s_own[b]) p.C[b * p.cs0 + g * p.cs1 + j] = -INFINITY;
+      }
     }
   }
-  if (p.sel != nullptr && blockIdx.x == 0) {
+  if (!MQ && p.sel != nullptr && blockIdx.x == 0) {
     // rows with nothing to score: own block only (or nothing for a bad length)
     for (int r = tid; r < p.B * p.Hkv; r += kThreads) {
       const int b = r / p.Hkv;
@@ -409,6 +437,10 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
             if (r < p.Hkv * kSharedHI)
               v = *reinterpret_cast<const uint4*>(p.q_idx + it.b * p.qs0 + (r / kSharedHI) * p.qs1 +
                                                   (r % kSharedHI) * p.qs2 + ch * 8);
+          } else if constexpr (MQ) {   // row r = (token r / 4, head r % 4)
+            if (r / kSharedHI < p.S && r % kSharedHI < p.HI)
+              v = *reinterpret_cast<const uint4*>(p.q_idx + it.b * p.qs0 + (r / kSharedHI) * p.qs_s + it.g * p.qs1 +
+                                                  (r % kSharedHI) * p.qs2 + ch * 8);
           } else {
             if (r < p.HI)
               v = *reinterpret_cast<const uint4*>(p.q_idx + it.b * p.qs0 + it.g * p.qs1 + r * p.qs2 + ch * 8);
@@ -458,8 +490,8 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
       page_cur = p.seq_pt[it.b * p.max_pages + it.j];
     }
     int cur_b = -1, cur_g = -1;
-    constexpr int NW = SHARED ? kSharedRows : kMaxHI;   // weights: (g, h) pairs, or the HI heads of one group
-    constexpr int NG = SHARED ? 8 : 1;                  // groups scored per item
+    constexpr int NW = WIDE ? kSharedRows : kMaxHI;     // weights: (g, h) or (token, h) pairs, or the HI heads
+    constexpr int NG = WIDE ? 8 : 1;                    // groups (or tokens) scored per item
     float wv[NW];
 #pragma unroll
     for (int c = 0; c < NW; ++c) wv[c] = 0.f;
@@ -477,6 +509,9 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
         for (int c = 0; c < NW; ++c) {
           if constexpr (SHARED)
             wv[c] = c < p.Hkv * kSharedHI ? p.w[it.b * p.ws0 + (c / kSharedHI) * p.ws1 + c % kSharedHI] : 0.f;
+          else if constexpr (MQ)
+            wv[c] = c / kSharedHI < p.S && c % kSharedHI < p.HI
+                        ? p.w[it.b * p.ws0 + (c / kSharedHI) * p.ws_s + it.g * p.ws1 + c % kSharedHI] : 0.f;
           else
             wv[c] = c < p.HI ? p.w[it.b * p.ws0 + it.g * p.ws1 + c] : 0.f;
         }
@@ -487,7 +522,7 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
       if (!__all_sync(0xffffffffu, mbar_wait(&bar_tfull[slot], (n / kSlots) & 1, abort_flag, p.dev_err))) break;
       tc_fence_after();
       uint32_t wmax[NG];
-      if constexpr (SHARED) {
+      if constexpr (WIDE) {
         uint32_t v[kSharedRows];
         tmem_ld32(tmem + lane_addr + slot * SLOT, v);
         tmem_ld_wait();
@@ -534,12 +569,18 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
       if (__shfl_sync(0xffffffffu, last, 0)) {
         const bool bad = page_cur < 0 || page_cur >= p.num_pages;
         if (bad && lane == 0) report(p.dev_err, MSA_DEVERR_BAD_PAGE);
-        const int ng = SHARED ? p.Hkv : 1;
+        const int ng = SHARED ? p.Hkv : MQ ? p.S : 1;
         if (lane < ng) {
-          const int g = SHARED ? lane : 0;
+          const int g = WIDE ? lane : 0;
           const uint32_t mk = max(max(s_red[rb][0][g], s_red[rb][1][g]), max(s_red[rb][2][g], s_red[rb][3][g]));
-          const int gg = SHARED ? g : it.g;
-          p.C[it.b * p.cs0 + gg * p.cs1 + it.j] = bad ? -INFINITY : float_from_order_key(mk);
+          if constexpr (MQ) {
+            // token g keeps the blocks before its own (the -inf fill covers the rest)
+            if (it.j < (s_q0[it.b] + g) / p.Bk)
+              p.C[it.b * p.cs0 + g * p.cs_s + it.g * p.cs1 + it.j] = bad ? -INFINITY : float_from_order_key(mk);
+          } else {
+            const int gg = SHARED ? g : it.g;
+            p.C[it.b * p.cs0 + gg * p.cs1 + it.j] = bad ? -INFINITY : float_from_order_key(mk);
+          }
         }
       }
       it = nxt;
@@ -555,7 +596,7 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
   }
 
   // ---- fused selection: the CTA whose scores complete a (b, g) row selects it ----
-  if (p.sel != nullptr && !*abort_flag && count > 0) {
+  if (!MQ && p.sel != nullptr && !*abort_flag && count > 0) {
     __shared__ int s_nrows, s_nlong;
     // The TMA ring is idle now and holds the selection's scratch (static
     // shared memory would keep two CTAs of the shared-index variant from
@@ -644,7 +685,9 @@ index_decode_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
 
 }  // namespace
 
-msa_status launch_index_decode(const msa_index_args& a, cudaStream_t stream) {
+namespace {
+
+msa_status launch_index_decode_impl(const msa_index_args& a, bool mq, cudaStream_t stream) {
   DeviceInfo dev;
   if (msa_status st = current_device(&dev); st != MSA_OK) return st;
   // k_idx pool as a 4-D tensor (dI, t, g, page) with a 64 x 128 x 1 x 1 box; a
@@ -667,25 +710,36 @@ msa_status launch_index_decode(const msa_index_args& a, cudaStream_t stream) {
   Params p;
   p.B = a.B; p.Hkv = a.Hkv; p.HI = a.HI; p.Bk = a.Bk;
   p.q_idx = static_cast<const __nv_bfloat16*>(a.q_idx);
-  p.qs0 = a.q_idx_stride[0]; p.qs1 = a.q_idx_stride[1]; p.qs2 = a.q_idx_stride[2];
-  p.w = a.w; p.ws0 = a.w_stride[0]; p.ws1 = a.w_stride[1];
-  p.num_pages = a.num_pages; p.seq_pt = a.seq_pt; p.max_pages = a.max_pages; p.seq_len = a.seq_len;
-  p.C = a.C; p.cs0 = a.C_stride[0]; p.cs1 = a.C_stride[1]; p.nb_stride = a.nb_stride;
+  p.w = a.w;
+  p.num_pages = a.num_pages; p.seq_pt = a.seq_pt; p.max_pages = a.max_pages;
+  p.C = a.C; p.nb_stride = a.nb_stride;
   p.dev_err = a.dev_err;
-  p.k = a.k; p.sel = a.sel; p.count = a.count; p.pt = a.pt; p.n_out = a.n; p.last_len = a.last_len;
+  if (mq) {   // chunk strides: q_idx (b, s, g, h), w and C (b, s, g)
+    p.S = a.S; p.q_pos = a.q_pos; p.seq_len = nullptr;
+    p.qs0 = a.q_idx_stride[0]; p.qs_s = a.q_idx_stride[1]; p.qs1 = a.q_idx_stride[2]; p.qs2 = a.q_idx_stride[3];
+    p.ws0 = a.w_stride[0]; p.ws_s = a.w_stride[1]; p.ws1 = a.w_stride[2];
+    p.cs0 = a.C_stride[0]; p.cs_s = a.C_stride[1]; p.cs1 = a.C_stride[2];
+  } else {    // decode strides: q_idx (b, g, h), w and C (b, g)
+    p.S = 1; p.q_pos = nullptr; p.seq_len = a.seq_len;
+    p.qs0 = a.q_idx_stride[0]; p.qs_s = 0; p.qs1 = a.q_idx_stride[1]; p.qs2 = a.q_idx_stride[2];
+    p.ws0 = a.w_stride[0]; p.ws_s = 0; p.ws1 = a.w_stride[1];
+    p.cs0 = a.C_stride[0]; p.cs_s = 0; p.cs1 = a.C_stride[1];
+  }
+  p.k = a.k; p.sel = mq ? nullptr : a.sel; p.count = a.count; p.pt = a.pt; p.n_out = a.n; p.last_len = a.last_len;
   p.counter = a.row_scratch;
   // With one pool for all groups every group row of a sequence is completed
   // by the same CTA, which would select them one after another; rows of more
   // than 2048 blocks are therefore selected by the top-k kernel instead (one
   // CTA per row, all rows at once) and mapped by the page-table kernel: the
   // same outputs, two more launches.
-  const bool select_after = shared && a.sel != nullptr && a.nb_stride > 2048;
+  const bool select_after = !mq && shared && a.sel != nullptr && a.nb_stride > 2048;
   if (select_after) p.sel = nullptr;
 
-  const size_t qtile = static_cast<size_t>(shared ? kSharedRows : 16) * kDI * 2;
-  const size_t smem = 1024 + kStages * kStageBytes + 2 * qtile + (2 * static_cast<size_t>(a.B) + 1) * 4;
+  const size_t qtile = static_cast<size_t>(shared || mq ? kSharedRows : 16) * kDI * 2;
+  const size_t smem = 1024 + kStages * kStageBytes + 2 * qtile + ((mq ? 3 : 2) * static_cast<size_t>(a.B) + 1) * 4;
   if (smem > dev.max_smem_optin) return fail(MSA_ERR_UNSUPPORTED, "decode index score: batch too large for shared memory");
-  auto kern = shared ? index_decode_kernel<true> : index_decode_kernel<false>;
+  auto kern = mq ? index_decode_kernel<false, true>
+                 : shared ? index_decode_kernel<true, false> : index_decode_kernel<false, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(index_decode)");
   if (p.sel != nullptr && !a.scratch_zeroed) {   // otherwise zero by contract (and unused without p.sel)
@@ -712,6 +766,21 @@ msa_status launch_index_decode(const msa_index_args& a, cudaStream_t stream) {
   if (a.pt == nullptr) return MSA_OK;
   return launch_page_table(a.sel, a.count, a.seq_pt, a.max_pages, a.seq_len, a.B, a.Hkv, a.k, a.Bk, a.pt, a.n,
                            a.last_len, a.dev_err, stream);
+}
+
+}  // namespace
+
+msa_status launch_index_decode(const msa_index_args& a, cudaStream_t stream) {
+  return launch_index_decode_impl(a, false, stream);
+}
+
+bool index_chunk_tokens_ok(const msa_index_args& a) {
+  return a.mode == MSA_MODE_CHUNK && a.S >= 1 && a.S <= kChunkDecodeMaxS && a.HI <= kSharedHI && a.dI == kDI &&
+         a.k_idx_stride[1] != 0 && a.B <= kMaxDecodeBatch;
+}
+
+msa_status launch_index_chunk_tokens(const msa_index_args& a, cudaStream_t stream) {
+  return launch_index_decode_impl(a, true, stream);
 }
 
 }  // namespace msa

@@ -574,6 +574,10 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
 }  // namespace
 
 msa_status launch_index_prefill(const msa_index_args& a, cudaStream_t stream) {
+  // a few tokens per sequence over per-group keys (draft verification,
+  // multi-token decode): the decode kernel streams each page once for all of
+  // them with two CTAs per SM
+  if (index_chunk_tokens_ok(a)) return launch_index_chunk_tokens(a, stream);
   DeviceInfo dev;
   if (msa_status st = current_device(&dev); st != MSA_OK) return st;
   CUtensorMap qmap, kmap;

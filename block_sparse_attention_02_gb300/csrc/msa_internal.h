@@ -33,6 +33,11 @@ msa_status encode_tiled_map(CUtensorMap* map, CUtensorMapDataType dtype, int ran
 
 // Launchers (validated arguments only).
 msa_status launch_index_decode(const msa_index_args& a, cudaStream_t stream);
+// Chunk scoring of S <= kChunkDecodeMaxS tokens per sequence over per-group
+// index keys through the decode index kernel (B rows = the tokens' heads);
+// index_chunk_tokens_ok tells whether a validated chunk call qualifies.
+bool index_chunk_tokens_ok(const msa_index_args& a);
+msa_status launch_index_chunk_tokens(const msa_index_args& a, cudaStream_t stream);
 msa_status launch_index_prefill(const msa_index_args& a, cudaStream_t stream);
 msa_status launch_topk(const msa_topk_args& a, cudaStream_t stream);
 msa_status launch_page_table(const int32_t* sel, const int32_t* count, const int32_t* seq_pt,

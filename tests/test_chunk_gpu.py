@@ -73,6 +73,12 @@ CASES = [
     ChunkWorkload("hi3_k64", prefix=(9000,), S=1300, shape=MSAShape(Hq=16, Hkv=2, HI=3, k=64), seed=65),
     # one query: a decode step through the chunk path
     ChunkWorkload("single_token", prefix=(777, 5), S=1, shape=MSAShape(Hq=12, Hkv=2, k=4), seed=66),
+    # 8 tokens per sequence straddling block boundaries (tokens of one sequence
+    # with different own blocks), HI = 3, a prefix inside block 0
+    ChunkWorkload("straddle_s8_hi3", prefix=(125, 1020, 250, 3), S=8, shape=MSAShape(Hq=12, Hkv=2, HI=3, k=4),
+                  seed=75),
+    # 5 tokens, MSA head shape, prefixes whose tokens cross a block boundary (60,030 + 2 = 60,032 = 469 * 128)
+    ChunkWorkload("verify_msa_s5", prefix=(60030, 383), S=5, shape=MSAShape(), seed=76),
 ]
 
 
@@ -86,6 +92,16 @@ def test_chunk_matches_oracle(msa, wl):
 def test_chunk_shared_index_pool(msa):
     """One index-key pool for all KV groups (group stride 0)."""
     wl = ChunkWorkload("shared", prefix=(2000, 700), S=300, shape=MSAShape(Hq=48, Hkv=8, k=8), seed=67)
+    inp = chunk_inputs(wl, device="cuda")
+    inp["kidx_pool"] = inp["kidx_pool"][:, :1].expand(-1, wl.shape.Hkv, -1, -1)
+    assert inp["kidx_pool"].stride(1) == 0
+    check_chunk(msa, wl, inp)
+
+
+def test_chunk_few_tokens_shared_index_pool(msa):
+    """A few tokens per sequence with one index-key pool for all KV groups
+    (scored by the prefill kernel's few-query variant)."""
+    wl = ChunkWorkload("shared_s4", prefix=(2000, 700), S=4, shape=MSAShape(Hq=48, Hkv=8, k=8), seed=77)
     inp = chunk_inputs(wl, device="cuda")
     inp["kidx_pool"] = inp["kidx_pool"][:, :1].expand(-1, wl.shape.Hkv, -1, -1)
     assert inp["kidx_pool"].stride(1) == 0
