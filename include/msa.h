@@ -130,6 +130,9 @@ const char *msa_status_string(msa_status s);
  * CHUNK: queries as in PREFILL (q_idx, w and C with the same shapes and
  *   strides, S = queries per sequence); index keys in pages as in DECODE
  *   (k_idx page pool, num_pages, seq_pt, max_pages; group stride 0 allowed).
+ *   (With S <= 8, HI <= 4 and per-group keys the scores are computed by the
+ *   decode kernel, all of a sequence's tokens per page read; the results are
+ *   the same.)
  *   q_pos [B] int32: absolute position of query 0 of sequence b.  Query s has
  *   own block (q_pos[b] + s) / Bk and scores the blocks before it;
  *   max over b of ceil((q_pos[b] + S) / Bk) <= nb_stride <= max_pages (a
