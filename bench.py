@@ -937,7 +937,10 @@ def main():
                          "sub-records under 'workloads' (empty: none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
-    ap.add_argument("--prefill-chunk", type=int, default=8192)
+    # queries per chunk of the prefill attention (CSR, attention, merge per
+    # chunk): fewer, larger chunks cost fewer launches; 65,536 queries need
+    # ~13 GB of bf16 partials in the workspace
+    ap.add_argument("--prefill-chunk", type=int, default=65536)
     ap.add_argument("--shared-index", action="store_true",
                     help="decode with one index-key pool for all KV groups (k_idx group stride 0)")
     ap.add_argument("--seq", type=int, default=None, help="override the prefill sequence length (profiling)")
