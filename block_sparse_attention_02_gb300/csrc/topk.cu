@@ -71,8 +71,11 @@ __device__ __forceinline__ void write_all(const RowInfo& r, int k, int lane_or_t
   if (lane_or_tid == 0) *r.cnt = r.valid ? r.own + 1 : 0;
 }
 
+// Rows are independent and each warp's row is latency-bound (its loads, then
+// shuffles): the long-row variants are held to 64 registers so that four
+// CTAs (32 rows) are in flight per SM instead of two.
 template <int NPL>
-__global__ void __launch_bounds__(kWarpsPerCta * 32)
+__global__ void __launch_bounds__(kWarpsPerCta * 32, NPL >= 16 ? 4 : 1)
 topk_warp_kernel(const msa_topk_args a, int64_t rows) {
   __shared__ uint64_t s_surv[kWarpsPerCta][kSelCap];
   __shared__ int s_pick[kWarpsPerCta][kMaxK];
