@@ -97,6 +97,7 @@ SMALL = [
     DecodeWorkload("k1", lengths=(3000, 129), shape=MSAShape(Hq=12, Hkv=2, HI=2, k=1), seed=34),
     DecodeWorkload("k64", lengths=(20000, 8000, 64 * 128 + 5), shape=MSAShape(Hq=24, Hkv=4, k=64), seed=35),
     DecodeWorkload("unshuffled", lengths=(2500,) * 3, shape=MSAShape(), seed=36, shuffle_pages=False),
+    DecodeWorkload("gqa3", lengths=(5000, 130, 1500), shape=MSAShape(Hq=9, Hkv=3, k=8), seed=37),
 ]
 
 

@@ -76,6 +76,9 @@ SMALL = [
     PrefillWorkload("edge_s64", B=1, S=64, shape=MSAShape(), seed=49),
     # one query block pair with a partial second 64-query block
     PrefillWorkload("edge_s200_hi2", B=2, S=200, shape=MSAShape(Hq=12, Hkv=2, HI=2, k=2), seed=50),
+    # GQA ratios 5 and 3: an entry's packed partial rows are G * 16 bytes per column chunk
+    PrefillWorkload("gqa5", B=1, S=900, shape=MSAShape(Hq=10, Hkv=2, k=5), seed=51),
+    PrefillWorkload("gqa3_b2", B=2, S=700, shape=MSAShape(Hq=9, Hkv=3, k=3), seed=52),
 ]
 
 
