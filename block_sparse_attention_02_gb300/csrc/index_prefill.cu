@@ -53,7 +53,8 @@ constexpr int kQTile = kMaxHI * kQHead;             // 32 KiB
 constexpr int kKStages = 6;
 constexpr int kBufCols = 256;                       // TMEM per slot: HI x 64 columns
 constexpr int kTmemCols = 512;
-constexpr int kFlush = 32;                          // block scores staged per query before a store
+constexpr int kFlush = 8;                           // block scores staged per query before a store
+constexpr int kStRow = kQB + 4;                     // staged row: one block's warp maxima for 64 queries (+4 pad)
 
 struct Params {
   int B, S, Hkv, HI, nq, nb_stride;                 // nq = ceil(S / 64)
@@ -311,8 +312,10 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ __align__(16) float2 s_w[2][kQB / 2][kMaxHI];   // per slot: (w[2e][h], w[2e+1][h]) per query pair e
-  __shared__ __align__(16) float s_red[2][2][4][kQB];   // per slot and pass parity: warp maxima per query
-  __shared__ float s_cst[2][kQB][kFlush + 1];       // per slot: staged block scores per query row
+  // per slot, two alternating groups of kFlush blocks: each epilogue warp's
+  // max over its 32 tokens, per block and query; combined over the 4 warps
+  // when the group is stored
+  __shared__ __align__(16) float s_stage[2][2][4][kFlush][kStRow];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -460,7 +463,7 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
         // warp-uniform decision: the TMEM loads below are warp-collective
         const bool got = __all_sync(0xffffffffu, mbar_wait(&bar_tfull[sl], np & 1, abort_flag, p.dev_err));
         if (got) tc_fence_after();
-        float* red = &s_red[sl][np & 1][q4][q0];
+        float* red = &s_stage[sl][(j / kFlush) & 1][q4][j % kFlush][q0];
         // chunk c = queries 8c .. 8c+7; the TMEM loads of chunk c+1 are in flight
         // while chunk c is reduced
         uint32_t va[HI][kCQ], vb[HI][kCQ];
@@ -529,32 +532,36 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
             if (c + 2 < kNC) wait(va);
           }
         }
-        // all four warps' maxima of this pass are staged (or some warp gave up waiting)
-        if (!(ok = named_bar_and(bar_id, 128, got))) break;
-        if (tw < kQW) {
-          const float* rp = &s_red[sl][np & 1][0][q0 + tw];
-          s_cst[sl][q0 + tw][j % kFlush] = fmaxf(fmaxf(rp[0], rp[kQB]), fmaxf(rp[2 * kQB], rp[3 * kQB]));
-        }
+        // a warp that gave up waiting goes on (its later waits fail at once:
+        // the abort flag is set) so that all four meet at the next store
+        ok = ok && got;
         ++np;
         if (j % kFlush == kFlush - 1 || j == it.je - 1) {
-          named_bar_sync(bar_id, 128);
-          // staged blocks j0 .. j (s_cst column = block mod kFlush)
+          // all four warps' maxima of the group are staged, or some warp gave up
+          if (!(ok = named_bar_and(bar_id, 128, ok))) break;
+          // staged blocks j0 .. j (row = block mod kFlush, group (block / kFlush) mod 2)
           const int jal = j - j % kFlush, j0 = max(it.jb, jal), cnt = j - j0 + 1;
+          const int jj = lane % kFlush, r4 = lane / kFlush;     // block and row of this lane
+          const int x = j0 - jal + jj;
+          const float(*stg)[kFlush][kStRow] = s_stage[sl][(j / kFlush) & 1];
           // a chunk's block whose page id is outside the pool was not loaded: -inf
           bool badpg = false;
           if constexpr (CHUNK) {
-            if (lane < cnt) {
-              const int pg = p.seq_pt[it.b * p.max_pages + j0 + lane];
+            if (jj < cnt) {
+              const int pg = p.seq_pt[it.b * p.max_pages + j0 + jj];
               badpg = pg < 0 || pg >= p.num_pages;
             }
           }
-          for (int rr = 0; rr < kQW / 4; ++rr) {     // warp q4: query rows q0 + 8 q4 .. q0 + 8 q4 + 7
-            const int qrow = q0 + q4 * (kQW / 4) + rr;
+#pragma unroll
+          for (int rr = 0; rr < kQW / 4; rr += 32 / kFlush) {   // warp q4: query rows q0 + 8 q4 .. q0 + 8 q4 + 7
+            const int qrow = q0 + q4 * (kQW / 4) + rr + r4;
             const int i = it.qb * kQB + qrow;
             // a query before the item's last own block has its own block among the passes: -inf
-            if (i < p.S && lane < cnt)
-              p.C[it.b * p.cs0 + static_cast<int64_t>(i) * p.cs1 + it.g * p.cs2 + j0 + lane] =
-                  (j0 + lane < (pos0 + i) / kBk && !badpg) ? s_cst[sl][qrow][j0 - jal + lane] : -INFINITY;
+            if (i < p.S && jj < cnt) {
+              const float v = fmaxf(fmaxf(stg[0][x][qrow], stg[1][x][qrow]), fmaxf(stg[2][x][qrow], stg[3][x][qrow]));
+              p.C[it.b * p.cs0 + static_cast<int64_t>(i) * p.cs1 + it.g * p.cs2 + j0 + jj] =
+                  (j0 + jj < (pos0 + i) / kBk && !badpg) ? v : -INFINITY;
+            }
           }
         }
       }
