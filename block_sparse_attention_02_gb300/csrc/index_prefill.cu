@@ -293,6 +293,7 @@ __device__ __forceinline__ void regs_after_wait(uint32_t (&r)[8]) {
 }
 
 constexpr int kCQ = 8;                               // queries per epilogue chunk
+constexpr int kReluAlu = 2;                          // heads whose ReLU is a max; the others use x + |x|
 constexpr int kNC = kQW / kCQ;                       // chunks per pass and warp
 
 // FEW: a chunk of at most kCQ queries per sequence (a few decode tokens):
@@ -448,7 +449,7 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
         const float* wp = p.w + it.b * p.ws0 + static_cast<int64_t>(i) * p.ws1 + it.g * p.ws2;
         float* sw = reinterpret_cast<float*>(&s_w[sl][(q0 + tw) >> 1][0]) + (tw & 1);
 #pragma unroll
-        for (int h = 0; h < HI; ++h) sw[2 * h] = i < p.S ? wp[h] : 0.f;
+        for (int h = 0; h < HI; ++h) sw[2 * h] = i < p.S ? (h < kReluAlu ? wp[h] : 0.5f * wp[h]) : 0.f;
       }
       named_bar_sync(bar_id, 128);
       // -inf for every entry from the item's block count on (the last split
@@ -487,10 +488,13 @@ index_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_cons
             const float wx[4] = {w01.x, w01.z, w23.x, w23.z}, wy[4] = {w01.y, w01.w, w23.y, w23.w};
             uint64_t acc = 0ull;
 #pragma unroll
-            for (int h = 0; h < HI; ++h)
-              acc = fma2(pack2(wx[h], wy[h]),
-                         pack2(fmaxf(__uint_as_float(v[h][2 * e]), 0.f), fmaxf(__uint_as_float(v[h][2 * e + 1]), 0.f)),
-                         acc);
+            for (int h = 0; h < HI; ++h) {
+              const float x0 = __uint_as_float(v[h][2 * e]), x1 = __uint_as_float(v[h][2 * e + 1]);
+              // ReLU as a max (ALU pipe) for the first heads and as x + |x| against a
+              // halved weight (FMA pipe) for the rest: (w / 2)(x + |x|) = w ReLU(x) exactly
+              acc = h < kReluAlu ? fma2(pack2(wx[h], wy[h]), pack2(fmaxf(x0, 0.f), fmaxf(x1, 0.f)), acc)
+                                 : fma2(pack2(wx[h], wy[h]), pack2(x0 + fabsf(x0), x1 + fabsf(x1)), acc);
+            }
             float s0, s1;
             unpack2(acc, s0, s1);
             km[2 * e] = warp_max_f32(s0);
