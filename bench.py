@@ -26,7 +26,7 @@ launching stream over exactly K steps bracketed by barrier + synchronize.  The
 default step reads 557 MB (the 491 MB of index keys alone exceed the 129 MB
 L2), so nothing is flushed; a step that reads less than twice the L2 (one
 index-key pool shared by the KV groups at this size) has a 258 MB buffer
-rewritten before each step, outside the timed region, and its per-step event
+read before each step, outside the timed region, and its per-step event
 times are summed.  ``roofline`` reports the dominant kernel (decode index
 scoring): algorithmic bytes per launch / its mean event-timed duration against
 the measured HBM copy bandwidth.  ``e2e`` repeats the step through the same C
@@ -222,17 +222,19 @@ def decode_algorithmic_bytes(wl, shared_index=False):
 class L2Flush:
     """Times steps on one stream.  Without a flush, one event pair brackets all
     K steps.  With a flush (a step whose bytes do not clearly exceed the L2),
-    a buffer of twice the L2 is rewritten before every step, outside the timed
-    region, and the per-step event times are summed."""
+    a buffer of twice the L2 is read before every step, outside the timed
+    region, and the per-step event times are summed.  A read, not a write: a
+    rewritten buffer would leave the L2 full of dirty lines whose write-back
+    (up to the L2's 129 MB) would then be charged to the timed step."""
 
     def __init__(self, enabled, device="cuda"):
         import torch
         self.enabled = enabled
-        self.buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=device) if enabled else None
+        self.buf = torch.zeros(2 * L2_BYTES // 4, dtype=torch.int32, device=device) if enabled else None
 
     def flush(self):
         if self.enabled:
-            self.buf.fill_(1)
+            self.buf.sum()
 
     def time(self, fn, K, stream):
         """Total device milliseconds of K calls of ``fn`` on ``stream``."""
